@@ -1,1 +1,205 @@
-"""Centroid-masked sparse LM head for GB300 (placeholder, filled in with the binding)."""
+"""Centroid-masked sparse LM head for GB300 (sm_103a).
+
+Thin Python face of the C ABI in include/mtp_head.h: each function here has
+the name of the C entry point it calls, turns torch tensors into device
+pointers and the current stream into a ``cudaStream_t``, allocates outputs the
+caller did not pass, and raises ``MtpError`` on a non-OK status.  Every step of
+the head runs in the library's CUDA kernels; there is no other code path.
+
+The head is Gemma4MTPMaskedEmbedder of "Add Gemma4 MTP speculative decoding
+with centroids masking" (vLLM, gemma4_mtp.py): ``mtp_masked_topk_tokens`` is
+get_top_tokens, ``mtp_masked_scatter_logits`` is forward,
+``mtp_centroid_scores`` is the centroid Linear + topk of _select_and_score,
+and ``mtp_dense_lm_head`` is the dense comparator (compute_logits without the
+masked embedder, no softcapping).
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_MAX_BATCH,
+                   MtpError, MtpHeadDesc, check, lib)
+
+__all__ = ["MaskedHead", "MtpError", "mtp_workspace_bytes", "mtp_centroid_scores",
+           "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_dense_lm_head",
+           "mtp_read_device_error", "mtp_profile_events", "MTP_DEVERR_TOKEN_RANGE",
+           "MTP_DEVERR_OFFSETS", "lib"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class MaskedHead:
+    """The head's device tables and their C descriptor.
+
+    centroid_w       bf16 [C, H] contiguous
+    embed_w          bf16 [>= V, ld] with unit inner stride (row stride ld >= H)
+    token_ordering   int32 [V]: ordered position -> token id
+    cluster_offsets  int32 [C + 1] or None (uniform clusters of V / C)
+    """
+
+    def __init__(self, centroid_w, embed_w, token_ordering, top_k, cluster_offsets=None,
+                 vocab_size=None):
+        torch = _torch()
+        if centroid_w is not None:
+            assert centroid_w.dtype == torch.bfloat16 and centroid_w.is_contiguous()
+        assert embed_w.dtype == torch.bfloat16 and embed_w.stride(1) == 1
+        if token_ordering is not None:
+            assert token_ordering.dtype == torch.int32 and token_ordering.is_contiguous()
+        if cluster_offsets is not None:
+            assert cluster_offsets.dtype == torch.int32 and cluster_offsets.is_contiguous()
+        self.centroid_w = centroid_w
+        self.embed_w = embed_w
+        self.token_ordering = token_ordering
+        self.cluster_offsets = cluster_offsets
+        self.device = embed_w.device
+        V = int(vocab_size if vocab_size is not None else token_ordering.shape[0])
+        H = int(embed_w.shape[1]) if centroid_w is None else int(centroid_w.shape[1])
+        C = 0 if centroid_w is None else int(centroid_w.shape[0])
+        self.vocab_size, self.hidden_size, self.num_centroids, self.top_k = V, H, C, int(top_k)
+        self.desc = MtpHeadDesc(
+            vocab_size=V, hidden_size=H, num_centroids=C, top_k=int(top_k),
+            device=self.device.index or 0, reserved0=0,
+            centroid_w=None if centroid_w is None else centroid_w.data_ptr(),
+            embed_w=embed_w.data_ptr(), ld_embed=int(embed_w.stride(0)),
+            token_ordering=None if token_ordering is None else token_ordering.data_ptr(),
+            cluster_offsets=None if cluster_offsets is None else cluster_offsets.data_ptr())
+        self._ws = None
+
+    @classmethod
+    def from_host(cls, centroid_w, embed_w, token_ordering, cluster_offsets, top_k,
+                  device="cuda", vocab_size=None):
+        """Copy host numpy tables (bf16 as uint16 bit patterns) to the device."""
+        torch = _torch()
+        import numpy as np
+
+        def bf16(a):
+            if a is None:
+                return None
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(
+                torch.bfloat16)
+
+        def i32(a):
+            return None if a is None else torch.from_numpy(
+                np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+        return cls(bf16(centroid_w), bf16(embed_w), i32(token_ordering), top_k,
+                   i32(cluster_offsets), vocab_size)
+
+    def workspace(self, batch):
+        """A cached workspace big enough for `batch` rows (grown on demand)."""
+        torch = _torch()
+        need = mtp_workspace_bytes(self, max(1, batch))
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+
+def mtp_workspace_bytes(head: MaskedHead, max_batch: int) -> int:
+    return int(lib().mtp_workspace_bytes(ctypes.byref(head.desc), int(max_batch)))
+
+
+def _hidden_ok(head, hidden):
+    torch = _torch()
+    assert hidden.dtype == torch.bfloat16 and hidden.is_contiguous() and hidden.dim() == 2
+    assert hidden.shape[1] == head.hidden_size and hidden.device == head.device
+    return int(hidden.shape[0])
+
+
+def mtp_centroid_scores(head, hidden, scores=None, topk_idx=None, with_topk=True, stream=None):
+    """(scores fp32 [B, C], topk int32 [B, K] sorted by (score desc, index asc) or None)."""
+    torch = _torch()
+    B = _hidden_ok(head, hidden)
+    if scores is None:
+        scores = torch.empty(B, head.num_centroids, dtype=torch.float32, device=head.device)
+    if with_topk and topk_idx is None:
+        topk_idx = torch.empty(B, head.top_k, dtype=torch.int32, device=head.device)
+    check(lib().mtp_centroid_scores(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(scores),
+                                    _ptr(topk_idx), _stream_ptr(stream, head.device)),
+          "mtp_centroid_scores")
+    return scores, topk_idx
+
+
+def mtp_masked_topk_tokens(head, hidden, out_tokens=None, out_max=None, workspace=None,
+                           with_max=True, stream=None):
+    """(token ids int32 [B], max logit fp32 [B] or None): the sparse argmax."""
+    torch = _torch()
+    B = _hidden_ok(head, hidden)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, dtype=torch.int32, device=head.device)
+    if with_max and out_max is None:
+        out_max = torch.empty(B, dtype=torch.float32, device=head.device)
+    ws = workspace if workspace is not None else head.workspace(B)
+    check(lib().mtp_masked_topk_tokens(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_tokens),
+                                       _ptr(out_max), _ptr(ws), ws.numel() * ws.element_size(),
+                                       _stream_ptr(stream, head.device)),
+          "mtp_masked_topk_tokens")
+    return out_tokens, out_max
+
+
+def mtp_masked_scatter_logits(head, hidden, out=None, workspace=None, stream=None):
+    """fp32 [B, V]: candidates' logits, -inf elsewhere."""
+    torch = _torch()
+    B = _hidden_ok(head, hidden)
+    if out is None:
+        out = torch.empty(B, head.vocab_size, dtype=torch.float32, device=head.device)
+    ws = workspace if workspace is not None else head.workspace(B)
+    check(lib().mtp_masked_scatter_logits(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out),
+                                          _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream_ptr(stream, head.device)),
+          "mtp_masked_scatter_logits")
+    return out
+
+
+def mtp_dense_lm_head(head, hidden, out_logits=None, out_tokens=None, out_max=None,
+                      want_logits=True, want_tokens=False, workspace=None, stream=None):
+    """(logits fp32 [B, V] or None, token ids int32 [B] or None, max fp32 [B] or None)."""
+    torch = _torch()
+    B = _hidden_ok(head, hidden)
+    if want_logits and out_logits is None:
+        out_logits = torch.empty(B, head.vocab_size, dtype=torch.float32, device=head.device)
+    if want_tokens and out_tokens is None:
+        out_tokens = torch.empty(B, dtype=torch.int32, device=head.device)
+        if out_max is None:
+            out_max = torch.empty(B, dtype=torch.float32, device=head.device)
+    ws = None
+    if out_tokens is not None:
+        ws = workspace if workspace is not None else head.workspace(B)
+    check(lib().mtp_dense_lm_head(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_logits),
+                                  _ptr(out_tokens), _ptr(out_max), _ptr(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(),
+                                  _stream_ptr(stream, head.device)),
+          "mtp_dense_lm_head")
+    return out_logits, out_tokens, out_max
+
+
+def mtp_read_device_error(workspace, stream=None) -> int:
+    """The device error word of the last call that used `workspace` (synchronises the stream)."""
+    torch = _torch()
+    word = ctypes.c_uint32(0)
+    st = torch.cuda.current_stream(workspace.device) if stream is None else stream
+    check(lib().mtp_read_device_error(_ptr(workspace), ctypes.byref(word),
+                                      ctypes.c_void_p(st.cuda_stream)), "mtp_read_device_error")
+    st.synchronize()
+    return int(word.value)
+
+
+def mtp_profile_events(kernel: str, start=None, stop=None) -> None:
+    """Record torch.cuda.Event pair around one kernel of every following call (None clears)."""
+    check(lib().mtp_profile_events(KERNEL_IDS[kernel],
+                                   None if start is None else ctypes.c_void_p(start.cuda_event),
+                                   None if stop is None else ctypes.c_void_p(stop.cuda_event)),
+          "mtp_profile_events")

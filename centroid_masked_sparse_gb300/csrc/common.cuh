@@ -1,0 +1,179 @@
+// Device helpers and launch parameters shared by the head's kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mtp_head.h"
+
+namespace mtp {
+
+constexpr int kWarp = 32;
+
+// Workspace control words (uint32 at the start of the workspace).
+constexpr int kCtrlError = 0;    // MTP_DEVERR_* bits
+constexpr int kCtrlItems = 1;    // number of gather work items built by the top-K kernel
+constexpr int kCtrlTicket = 2;   // CTAs of the gather-score kernel that have finished
+constexpr int kCtrlNext = 3;     // next work item to hand out (dynamic scheduling)
+constexpr int kCtrlWords = 16;
+
+// ---------------------------------------------------------------------------
+// Loads
+// ---------------------------------------------------------------------------
+
+// 16-byte read-only load that bypasses L1 (rows are read once) and asks L2 to
+// fetch the surrounding 256 bytes (embedding rows are long contiguous runs).
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// 16-byte read-only load through the normal cache path (small, reused data).
+__device__ __forceinline__ uint4 ld_ro16(const void *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// ---------------------------------------------------------------------------
+// bf16 arithmetic: a bf16 is the top half of an fp32, so unpacking is a shift
+// or a mask; products of two bf16 values are exact in fp32.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// acc + sum of the 8 products of two 16-byte groups of bf16 values.
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc)
+{
+    acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
+    acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
+    acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
+    acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
+    acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
+    acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
+    acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
+    acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+    return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Order-preserving keys
+// ---------------------------------------------------------------------------
+
+// fp32 -> uint32 whose unsigned order is the float order; -0 and +0 map to
+// the same key.
+__device__ __forceinline__ uint32_t ord_key(float f)
+{
+    f = __fadd_rn(f, 0.0f);  // -0 -> +0
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float ord_value(uint32_t k)
+{
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+
+// 64-bit argmax key: larger logit wins, then lower token id.  Never 0 for a
+// finite logit, so 0 means "no candidate".
+__device__ __forceinline__ unsigned long long argmax_key(float v, int32_t token)
+{
+    return ((unsigned long long)ord_key(v) << 32) |
+           (unsigned long long)(0xffffffffu - (uint32_t)token);
+}
+
+__device__ __forceinline__ void decode_argmax_key(unsigned long long k, int32_t *token, float *v)
+{
+    if (k == 0ull) {
+        *token = -1;
+        *v = __int_as_float(0xff800000);  // -inf
+    } else {
+        *token = (int32_t)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+        *v = ord_value((uint32_t)(k >> 32));
+    }
+}
+
+// Ordered positions [lo, hi) of centroid c; false (and the error bit) when the
+// offsets are malformed.
+__device__ __forceinline__ bool cluster_range(const int32_t *offsets, int32_t V, int32_t S, int c,
+                                              int *lo, int *hi, uint32_t *err_word)
+{
+    if (offsets == nullptr) {
+        *lo = c * S;
+        *hi = *lo + S;
+        return true;
+    }
+    int a = __ldg(offsets + c), b = __ldg(offsets + c + 1);
+    if (a < 0 || b < a || b > V) {
+        if (err_word) atomicOr(err_word, MTP_DEVERR_OFFSETS);
+        *lo = *hi = 0;
+        return false;
+    }
+    *lo = a;
+    *hi = b;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Launch parameters
+// ---------------------------------------------------------------------------
+struct ProjParams {
+    const uint16_t *hidden;  // [B, H]
+    const uint16_t *wc;      // [C, H]
+    float *scores;           // [B, C]
+    uint32_t *zero;          // words to clear before the top-K kernel runs (may be null)
+    int zero_words;
+    int B, H, C;
+    int rows_per_group;      // hidden rows staged in shared memory at a time
+};
+
+struct TopkParams {
+    const float *scores;     // [B, C]
+    int32_t *topk;           // [B, K] out, sorted by (score desc, index asc)
+    int B, C, K, V, S;
+    const int32_t *offsets;  // [C+1] or null (uniform clusters of S)
+    // bucketing (null rowmask = no bucketing)
+    uint32_t *rowmask;       // [C, W] bit b%32 of word b/32: row b selected c
+    int W;
+    int32_t *ccount;         // [C] rows that selected c
+    int2 *items;             // (centroid, first position offset) work items
+    int items_cap;           // capacity of items
+    uint32_t *ctrl;
+    int chunk;               // tokens per work item
+};
+
+enum ScoreMode { kMaskedArgmax = 0, kMaskedScatter = 1, kDense = 2 };
+
+struct ScoreParams {
+    const uint16_t *hidden;         // [B, H]
+    const uint16_t *embed;          // [>=V, ld]
+    long long ld;
+    const int32_t *ordering;        // [V] (masked modes)
+    const int32_t *offsets;         // [C+1] or null
+    const uint32_t *rowmask;        // [C, W]
+    const int2 *items;
+    int items_cap;
+    uint32_t *ctrl;
+    unsigned long long *keys;       // [B] argmax keys (or null)
+    float *out_logits;              // [B, V] (scatter / dense logits) or null
+    int32_t *out_tokens;            // [B] (argmax modes) or null
+    float *out_max;                 // [B] or null
+    int B, H, V, S, W, C;
+    int chunk;                      // tokens per work item
+    int rows_per_group;             // hidden rows staged in shared memory at a time
+    int dense_items;                // dense mode: ceil(V / chunk)
+};
+
+}  // namespace mtp

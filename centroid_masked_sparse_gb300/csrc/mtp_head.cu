@@ -1,0 +1,435 @@
+// C ABI of the centroid-masked sparse LM head: argument checks, workspace
+// layout and the launch sequence of each call.  Declarations and the contract
+// of every entry point are in include/mtp_head.h.
+#include <mutex>
+#include <unordered_map>
+
+#include "internal.h"
+
+namespace mtp {
+
+int chunks_for_hidden(int H)
+{
+    static const int sizes[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16};
+    const int need = (H / 8 + kWarp - 1) / kWarp;
+    for (int s : sizes)
+        if (s >= need) return s;
+    return 0;
+}
+
+static std::mutex g_cache_mu;
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    static std::unordered_map<int, int> cache;
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cache[dev] = n;
+    return n;
+}
+
+struct FnKey {
+    const void *fn;
+    int dev;
+    size_t smem;
+    bool operator==(const FnKey &o) const { return fn == o.fn && dev == o.dev && smem == o.smem; }
+};
+struct FnKeyHash {
+    size_t operator()(const FnKey &k) const
+    {
+        return std::hash<const void *>()(k.fn) ^ (std::hash<size_t>()(k.smem) * 31u) ^ (size_t)k.dev;
+    }
+};
+
+int blocks_per_sm(const void *kernel, int block, size_t smem)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static std::unordered_map<FnKey, int, FnKeyHash> cache;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        auto it = cache.find(FnKey{kernel, dev, smem});
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess) n = 1;
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    cache[FnKey{kernel, dev, smem}] = n;
+    return n;
+}
+
+cudaError_t allow_smem(const void *kernel, size_t smem)
+{
+    if (smem <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static std::unordered_map<FnKey, size_t, FnKeyHash> done;  // keyed by (fn, dev)
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        auto it = done.find(FnKey{kernel, dev, 0});
+        if (it != done.end() && it->second >= smem) return cudaSuccess;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    done[FnKey{kernel, dev, 0}] = smem;
+    return cudaSuccess;
+}
+
+}  // namespace mtp
+
+using namespace mtp;
+
+namespace {
+
+constexpr int kMinChunk = 8;     // smallest work item (ordered positions); sizes the item list
+constexpr int kMaxChunk = 128;
+
+void *g_prof[5][2] = {};
+
+struct Layout {
+    size_t ctrl, keys, ccount, rowmask, zero_end, scores, topk, items, total;
+    int W;
+    int items_cap;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Layout layout_for(const mtp_head_desc *d, int B)
+{
+    Layout L{};
+    const size_t C = (size_t)d->num_centroids, K = (size_t)d->top_k, V = (size_t)d->vocab_size;
+    L.W = (B + 31) / 32;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    L.ctrl = take(kCtrlWords * sizeof(uint32_t));
+    L.keys = take((size_t)B * sizeof(unsigned long long));
+    L.ccount = take(C * sizeof(int32_t));
+    L.rowmask = take(C * (size_t)L.W * sizeof(uint32_t));
+    L.zero_end = off;
+    L.scores = take((size_t)B * C * sizeof(float));
+    L.topk = take((size_t)B * K * sizeof(int32_t));
+    const size_t nsel = C < (size_t)B * K ? C : (size_t)B * K;
+    const size_t max_items = V / kMinChunk + nsel + 1;
+    L.items = take(max_items * sizeof(int2));
+    L.items_cap = (int)max_items;
+    L.total = off;
+    return L;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Checks of the descriptor.  `centroids`: the call reads the centroid table
+// (and needs C, K); `embed`: it reads the embedding table; `ordering`: it
+// reads token_ordering.
+mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool ordering)
+{
+    if (!d) return MTP_ERR_NULL;
+    if ((embed && !d->embed_w) || (centroids && !d->centroid_w) || (ordering && !d->token_ordering))
+        return MTP_ERR_NULL;
+    if (d->vocab_size < 1 || d->hidden_size < 8 || d->hidden_size % 8 != 0) return MTP_ERR_SHAPE;
+    if (d->hidden_size > MTP_MAX_HIDDEN) return MTP_ERR_UNSUPPORTED;
+    if (d->device < 0) return MTP_ERR_SHAPE;
+    if (embed) {
+        if (d->ld_embed < d->hidden_size) return MTP_ERR_SHAPE;
+        if (d->ld_embed % 8 != 0 || !aligned16(d->embed_w)) return MTP_ERR_ALIGN;
+    }
+    if (centroids) {
+        if (d->num_centroids < 1 || d->top_k < 1 || d->top_k > d->num_centroids) return MTP_ERR_SHAPE;
+        if (d->num_centroids > MTP_MAX_CENTROIDS) return MTP_ERR_UNSUPPORTED;
+        if (!aligned16(d->centroid_w)) return MTP_ERR_ALIGN;
+    }
+    if (ordering && !d->cluster_offsets && d->vocab_size % d->num_centroids != 0) return MTP_ERR_SHAPE;
+    return MTP_OK;
+}
+
+mtp_status check_batch(int32_t B)
+{
+    if (B < 0) return MTP_ERR_SHAPE;
+    if (B > MTP_MAX_BATCH) return MTP_ERR_UNSUPPORTED;
+    return MTP_OK;
+}
+
+mtp_status use_device(int dev)
+{
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return MTP_ERR_CUDA;
+    if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return MTP_ERR_CUDA;
+    return MTP_OK;
+}
+
+int rows_per_group(int B, int H)
+{
+    int r = 32768 / (2 * H);
+    if (r > 32) r = 32;
+    if (r < 1) r = 1;
+    return r < B ? r : B;
+}
+
+int proj_rows_per_group(int B, int H)
+{
+    int r = 49152 / (2 * H);
+    if (r < 1) r = 1;
+    return r < B ? r : B;
+}
+
+struct Prof {
+    int id;
+    cudaStream_t s;
+    Prof(int id_, cudaStream_t s_) : id(id_), s(s_)
+    {
+        if (g_prof[id][0]) cudaEventRecord((cudaEvent_t)g_prof[id][0], s);
+    }
+    ~Prof()
+    {
+        if (g_prof[id][1]) cudaEventRecord((cudaEvent_t)g_prof[id][1], s);
+    }
+};
+
+mtp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA; }
+
+// Steps 1-2: projection (+ workspace reset) and top-K (+ bucketing when rowmask is set).
+mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *scores,
+                      int32_t *topk, char *ws, const Layout *L, int chunk, cudaStream_t s)
+{
+    ProjParams pp{};
+    pp.hidden = (const uint16_t *)hidden;
+    pp.wc = (const uint16_t *)d->centroid_w;
+    pp.scores = scores;
+    pp.zero = ws ? (uint32_t *)ws : nullptr;
+    pp.zero_words = ws ? (int)(L->zero_end / sizeof(uint32_t)) : 0;
+    pp.B = B;
+    pp.H = d->hidden_size;
+    pp.C = d->num_centroids;
+    pp.rows_per_group = proj_rows_per_group(B, d->hidden_size);
+    {
+        Prof pr(MTP_KERNEL_PROJECTION, s);
+        mtp_status st = cuda_status(launch_projection(pp, s));
+        if (st != MTP_OK) return st;
+    }
+    if (!topk) return MTP_OK;
+    TopkParams tp{};
+    tp.scores = scores;
+    tp.topk = topk;
+    tp.B = B;
+    tp.C = d->num_centroids;
+    tp.K = d->top_k;
+    tp.V = d->vocab_size;
+    tp.S = d->cluster_offsets ? 0 : d->vocab_size / d->num_centroids;
+    tp.offsets = d->cluster_offsets;
+    if (ws) {
+        tp.rowmask = (uint32_t *)(ws + L->rowmask);
+        tp.W = L->W;
+        tp.ccount = (int32_t *)(ws + L->ccount);
+        tp.items = (int2 *)(ws + L->items);
+        tp.items_cap = L->items_cap;
+        tp.ctrl = (uint32_t *)ws;
+        tp.chunk = chunk;
+    }
+    Prof pr(MTP_KERNEL_TOPK, s);
+    return cuda_status(launch_topk(tp, s));
+}
+
+// Positions per work item: aim for ~8 items per resident CTA of the gather kernel.
+int choose_chunk(const mtp_head_desc *d, int B)
+{
+    const double avg = (double)d->vocab_size / d->num_centroids;
+    const double est = (double)B * d->top_k * avg;
+    const double target = est / (8.0 * sm_count() * 4.0);
+    int ch = kMinChunk;
+    while (ch < kMaxChunk && 2.0 * ch <= target) ch *= 2;
+    return ch;
+}
+
+mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t *out_tokens,
+                      float *out_max, float *out_logits, void *workspace, size_t ws_bytes,
+                      cudaStream_t s)
+{
+    const Layout L = layout_for(d, B);
+    if (!workspace || ws_bytes < L.total) return MTP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MTP_ERR_ALIGN;
+    mtp_status st = use_device(d->device);
+    if (st != MTP_OK) return st;
+    char *ws = (char *)workspace;
+    if (out_logits) {
+        Prof pr(MTP_KERNEL_FILL, s);
+        st = cuda_status(launch_fill_neg_inf(out_logits, (size_t)B * d->vocab_size, s));
+        if (st != MTP_OK) return st;
+    }
+    const int chunk = choose_chunk(d, B);
+    st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s);
+    if (st != MTP_OK) return st;
+
+    ScoreParams sp{};
+    sp.hidden = (const uint16_t *)hidden;
+    sp.embed = (const uint16_t *)d->embed_w;
+    sp.ld = d->ld_embed;
+    sp.ordering = d->token_ordering;
+    sp.offsets = d->cluster_offsets;
+    sp.rowmask = (const uint32_t *)(ws + L.rowmask);
+    sp.items = (const int2 *)(ws + L.items);
+    sp.items_cap = L.items_cap;
+    sp.C = d->num_centroids;
+    sp.ctrl = (uint32_t *)ws;
+    sp.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
+    sp.out_logits = out_logits;
+    sp.out_tokens = out_tokens;
+    sp.out_max = out_max;
+    sp.B = B;
+    sp.H = d->hidden_size;
+    sp.V = d->vocab_size;
+    sp.S = d->cluster_offsets ? 0 : d->vocab_size / d->num_centroids;
+    sp.W = L.W;
+    sp.chunk = chunk;
+    sp.rows_per_group = rows_per_group(B, d->hidden_size);
+    sp.dense_items = 0;
+    int grid = 0;
+    Prof pr(MTP_KERNEL_GATHER_SCORE, s);
+    return cuda_status(launch_score(sp, kMaskedArgmax, s, &grid));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mtp_workspace_bytes(const mtp_head_desc *desc, int32_t max_batch)
+{
+    if (!desc || max_batch < 1 || max_batch > MTP_MAX_BATCH) return 0;
+    if (desc->vocab_size < 1 || desc->num_centroids < 1 || desc->top_k < 1 ||
+        desc->top_k > desc->num_centroids || desc->num_centroids > MTP_MAX_CENTROIDS)
+        return 0;
+    return layout_for(desc, max_batch).total;
+}
+
+mtp_status mtp_centroid_scores(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                               float *scores, int32_t *topk_idx, void *stream)
+{
+    mtp_status st = check_desc(desc, true, false, false);
+    if (st != MTP_OK) return st;
+    if ((st = check_batch(batch)) != MTP_OK) return st;
+    if (batch == 0) return MTP_OK;
+    if (!hidden || !scores) return MTP_ERR_NULL;
+    if (!aligned16(hidden)) return MTP_ERR_ALIGN;
+    if ((st = use_device(desc->device)) != MTP_OK) return st;
+    return run_select(desc, hidden, batch, scores, topk_idx, nullptr, nullptr, kMinChunk,
+                      (cudaStream_t)stream);
+}
+
+mtp_status mtp_masked_topk_tokens(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                                  int32_t *out_tokens, float *out_max, void *workspace,
+                                  size_t workspace_bytes, void *stream)
+{
+    mtp_status st = check_desc(desc, true, true, true);
+    if (st != MTP_OK) return st;
+    if ((st = check_batch(batch)) != MTP_OK) return st;
+    if (batch == 0) return MTP_OK;
+    if (!hidden || !out_tokens) return MTP_ERR_NULL;
+    if (!aligned16(hidden)) return MTP_ERR_ALIGN;
+    return run_masked(desc, hidden, batch, out_tokens, out_max, nullptr, workspace, workspace_bytes,
+                      (cudaStream_t)stream);
+}
+
+mtp_status mtp_masked_scatter_logits(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                                     float *out_logits, void *workspace, size_t workspace_bytes,
+                                     void *stream)
+{
+    mtp_status st = check_desc(desc, true, true, true);
+    if (st != MTP_OK) return st;
+    if ((st = check_batch(batch)) != MTP_OK) return st;
+    if (batch == 0) return MTP_OK;
+    if (!hidden || !out_logits) return MTP_ERR_NULL;
+    if (!aligned16(hidden) || !aligned16(out_logits)) return MTP_ERR_ALIGN;
+    return run_masked(desc, hidden, batch, nullptr, nullptr, out_logits, workspace, workspace_bytes,
+                      (cudaStream_t)stream);
+}
+
+mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                             float *out_logits, int32_t *out_tokens, float *out_max,
+                             void *workspace, size_t workspace_bytes, void *stream)
+{
+    mtp_status st = check_desc(desc, false, true, false);
+    if (st != MTP_OK) return st;
+    if ((st = check_batch(batch)) != MTP_OK) return st;
+    if (batch == 0) return MTP_OK;
+    if (!hidden || (!out_logits && !out_tokens)) return MTP_ERR_NULL;
+    if (out_max && !out_tokens) return MTP_ERR_NULL;
+    if (!aligned16(hidden)) return MTP_ERR_ALIGN;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    Layout L{};
+    if (out_tokens) {
+        // the workspace layout only depends on V, C, K, B; C and K may be unset for a dense head
+        mtp_head_desc d = *desc;
+        if (d.num_centroids < 1) d.num_centroids = 1;
+        if (d.top_k < 1 || d.top_k > d.num_centroids) d.top_k = 1;
+        L = layout_for(&d, batch);
+        if (!ws || workspace_bytes < L.keys + (size_t)batch * sizeof(unsigned long long))
+            return MTP_ERR_WORKSPACE;
+        if (!aligned16(ws)) return MTP_ERR_ALIGN;
+    }
+    if ((st = use_device(desc->device)) != MTP_OK) return st;
+    if (out_tokens) {
+        st = cuda_status(cudaMemsetAsync(ws, 0, L.keys + (size_t)batch * sizeof(unsigned long long), s));
+        if (st != MTP_OK) return st;
+    }
+    ScoreParams sp{};
+    sp.hidden = (const uint16_t *)hidden;
+    sp.embed = (const uint16_t *)desc->embed_w;
+    sp.ld = desc->ld_embed;
+    sp.ctrl = out_tokens ? (uint32_t *)ws : nullptr;
+    sp.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
+    sp.out_logits = out_logits;
+    sp.out_tokens = out_tokens;
+    sp.out_max = out_max;
+    sp.B = batch;
+    sp.H = desc->hidden_size;
+    sp.V = desc->vocab_size;
+    sp.chunk = 64;
+    sp.rows_per_group = rows_per_group(batch, desc->hidden_size);
+    sp.dense_items = (desc->vocab_size + sp.chunk - 1) / sp.chunk;
+    int grid = 0;
+    Prof pr(MTP_KERNEL_DENSE, s);
+    return cuda_status(launch_score(sp, kDense, s, &grid));
+}
+
+mtp_status mtp_read_device_error(const void *workspace, uint32_t *host_word, void *stream)
+{
+    if (!workspace || !host_word) return MTP_ERR_NULL;
+    return cuda_status(cudaMemcpyAsync(host_word, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                       (cudaStream_t)stream));
+}
+
+const char *mtp_status_string(mtp_status status)
+{
+    switch (status) {
+    case MTP_OK: return "ok";
+    case MTP_ERR_NULL: return "a required pointer is NULL";
+    case MTP_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case MTP_ERR_ALIGN: return "a pointer or row stride is not 16-byte aligned";
+    case MTP_ERR_WORKSPACE: return "workspace missing or smaller than mtp_workspace_bytes";
+    case MTP_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case MTP_ERR_UNSUPPORTED: return "sizes outside this build's limits";
+    }
+    return "unknown status";
+}
+
+int32_t mtp_version(void) { return 100; }
+
+mtp_status mtp_profile_events(int32_t kernel, void *start_event, void *stop_event)
+{
+    if (kernel < 0 || kernel > MTP_KERNEL_DENSE) return MTP_ERR_SHAPE;
+    g_prof[kernel][0] = start_event;
+    g_prof[kernel][1] = stop_event;
+    return MTP_OK;
+}
+
+}  // extern "C"

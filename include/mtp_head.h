@@ -1,0 +1,187 @@
+/*
+ * mtp_head.h - C ABI of the centroid-masked sparse LM head for GB300 (sm_103a).
+ *
+ * The head computes, for each draft hidden state h (one row of the batch):
+ *   1. centroid scores   s[c] = sum_k h[k] * Wc[c, k]                (C scores)
+ *   2. top-K centroids   the K largest scores (lower index first on ties)
+ *   3. candidates        the token ids owned by those centroids: centroid c
+ *                        owns ordered positions [off[c], off[c+1]) and
+ *                        token_ordering[p] is the token id at position p
+ *   4. sparse logits     logit[t] = sum_k h[k] * E[t, k] for every candidate t
+ * and finishes either with the token id of the largest sparse logit, or with
+ * a full-vocabulary fp32 row holding each candidate's logit and -inf
+ * elsewhere.  This is Gemma4MTPMaskedEmbedder of "Add Gemma4 MTP speculative
+ * decoding with centroids masking" (vLLM, vllm/model_executor/models/
+ * gemma4_mtp.py): __init__ (V/C tokens per centroid, bias-free centroid Linear
+ * [C, H], token_ordering buffer [V]), _select_and_score (steps 1-4),
+ * get_top_tokens (sparse argmax) and forward (full-vocabulary scatter).  The
+ * dense comparator is the compute_logits fallback of Gemma4MTP (the
+ * LogitsProcessor over every vocabulary row) without final softcapping.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All array pointers are DEVICE pointers on desc->device and are owned by
+ *   the caller.  The library never allocates or frees device memory, never
+ *   synchronises, and never reads device memory on the host, so every call is
+ *   a pure sequence of kernel launches (and, for the dense head, one
+ *   cudaMemsetAsync) on `stream`.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ * - bf16 arrays are raw IEEE bfloat16 bit patterns (uint16 storage).
+ * - Rows are row-major.  hidden is [batch, H] with row stride H.
+ * - Host-side argument checks run before anything is launched; a failed check
+ *   returns its status and launches nothing.  A launch failure returns
+ *   MTP_ERR_CUDA.  Problems that only the device can see (a token id outside
+ *   [0, V), cluster offsets that are not ascending inside [0, V]) do not
+ *   fault: the offending entry is skipped and a bit is set in the workspace's
+ *   device error word (see mtp_read_device_error).
+ * - A workspace serves one call at a time: concurrent calls on different
+ *   streams need different workspaces.  Tables may be shared freely.
+ *
+ * Readings of the source that this library takes (where the page is silent or
+ * inconsistent): token ids are int32 (the page uses int64); scores and logits
+ * are fp32 with fp32 accumulation from bf16 inputs (the page's Linear/einsum
+ * produce bf16); top-K ties go to the lower centroid index; argmax ties go to
+ * the lower token id; the full-vocabulary fill is -inf (the docstring of
+ * forward), not the dtype's finite minimum; no final logit softcapping.
+ */
+#ifndef MTP_HEAD_H
+#define MTP_HEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MTP_API __attribute__((visibility("default")))
+#else
+#define MTP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mtp_status {
+    MTP_OK = 0,
+    MTP_ERR_NULL = -1,        /* a required pointer is NULL                         */
+    MTP_ERR_SHAPE = -2,       /* a size is out of range or inconsistent             */
+    MTP_ERR_ALIGN = -3,       /* a pointer or row stride is not 16-byte aligned     */
+    MTP_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than mtp_workspace_bytes */
+    MTP_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed               */
+    MTP_ERR_UNSUPPORTED = -6  /* valid but outside this build's limits (see below)  */
+} mtp_status;
+
+/* Limits of this build (MTP_ERR_UNSUPPORTED beyond them):
+ *   H % 8 == 0 and 8 <= H <= 4096; 1 <= K <= C <= 16384; 1 <= batch <= 1024;
+ *   1 <= V < 2^31; uniform clusters need V % C == 0. */
+#define MTP_MAX_HIDDEN 4096
+#define MTP_MAX_CENTROIDS 16384
+#define MTP_MAX_BATCH 1024
+
+/* Bits of the device error word (OR-ed together over one call). */
+#define MTP_DEVERR_TOKEN_RANGE 0x1u  /* token_ordering held an id outside [0, V) */
+#define MTP_DEVERR_OFFSETS 0x2u      /* cluster_offsets not ascending in [0, V]  */
+
+/* The head's tables.  Plain data: the struct is read on the host at each call
+ * and may live anywhere on the host.
+ *   vocab_size       V, number of tokens (rows of embed_w that are used)
+ *   hidden_size      H, length of a hidden state, of a centroid row, of an embedding row
+ *   num_centroids    C
+ *   top_k            K, centroids selected per row
+ *   device           CUDA ordinal that holds every buffer of the calls
+ *   centroid_w       bf16 [C, H] row-major (the Linear weight layout); 16-byte aligned
+ *   embed_w          bf16 [>= V, ld_embed], token-id order (the lm_head weight; rows
+ *                    at or beyond V, e.g. padding, are never read); 16-byte aligned
+ *   ld_embed         elements between consecutive rows of embed_w; >= H, multiple of 8
+ *   token_ordering   int32 [V]: ordered position -> token id; must be a permutation of
+ *                    0..V-1 (not checked; a duplicate id makes the scatter's winner
+ *                    for that id unspecified)
+ *   cluster_offsets  int32 [C+1] ascending, off[0] = 0, off[C] = V: centroid c owns
+ *                    positions [off[c], off[c+1]); empty clusters are allowed.  NULL
+ *                    means uniform clusters of V/C positions (the page's layout). */
+typedef struct mtp_head_desc {
+    int32_t vocab_size;
+    int32_t hidden_size;
+    int32_t num_centroids;
+    int32_t top_k;
+    int32_t device;
+    int32_t reserved0;
+    const void *centroid_w;
+    const void *embed_w;
+    int64_t ld_embed;
+    const int32_t *token_ordering;
+    const int32_t *cluster_offsets;
+} mtp_head_desc;
+
+/* Bytes of device workspace that the masked calls and the dense head's argmax
+ * need for batches of up to max_batch rows.  Pure host arithmetic; returns 0
+ * if the descriptor's sizes or max_batch are invalid.  The workspace needs no
+ * initialisation: every call resets the parts it uses.  Its first 4 bytes are
+ * the device error word of the last call that used it. */
+MTP_API size_t mtp_workspace_bytes(const mtp_head_desc *desc, int32_t max_batch);
+
+/* Steps 1-2 (the centroid Linear and topk of _select_and_score).
+ *   hidden    bf16 [batch, H], 16-byte aligned
+ *   scores    fp32 [batch, C] out: s[b, c]
+ *   topk_idx  int32 [batch, K] out, or NULL: the selected centroids of each row,
+ *             sorted by (score desc, index asc) like a sorted topk
+ * Needs no workspace. */
+MTP_API mtp_status mtp_centroid_scores(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                               float *scores, int32_t *topk_idx, void *stream);
+
+/* get_top_tokens: steps 1-4 and the sparse argmax, without a full-vocabulary row.
+ *   out_tokens  int32 [batch] out: token id of the largest sparse logit of each row
+ *               (lower id on exact ties); -1 if the row's selected clusters are all
+ *               empty
+ *   out_max     fp32 [batch] out, or NULL: that logit (-inf for a -1 row)
+ *   workspace   device buffer of at least mtp_workspace_bytes(desc, batch) bytes,
+ *               16-byte aligned */
+MTP_API mtp_status mtp_masked_topk_tokens(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                                  int32_t *out_tokens, float *out_max,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* forward: steps 1-4 written into a full-vocabulary row.
+ *   out_logits  fp32 [batch, V] out, row stride V, 16-byte aligned: the sparse
+ *               logit at each candidate token id, -inf at every other id */
+MTP_API mtp_status mtp_masked_scatter_logits(const mtp_head_desc *desc, const void *hidden,
+                                     int32_t batch, float *out_logits,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Dense comparator: logit[b, t] = sum_k h[b, k] * E[t, k] for every t < V.
+ *   out_logits  fp32 [batch, V] out (row stride V), or NULL
+ *   out_tokens  int32 [batch] out, or NULL: dense argmax, lower id on ties
+ *   out_max     fp32 [batch] out, or NULL (only with out_tokens)
+ *   workspace   needed only when out_tokens != NULL (same size rule as above)
+ * centroid_w, token_ordering and cluster_offsets are not read; at least one of
+ * out_logits and out_tokens must be non-NULL. */
+MTP_API mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                             float *out_logits, int32_t *out_tokens, float *out_max,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* Enqueue an asynchronous copy of the workspace's device error word (a set of
+ * MTP_DEVERR_* bits, reset by each masked call) into *host_word; the value is
+ * valid once `stream` has been synchronised. */
+MTP_API mtp_status mtp_read_device_error(const void *workspace, uint32_t *host_word, void *stream);
+
+/* Static English text for a status code. */
+MTP_API const char *mtp_status_string(mtp_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MTP_API int32_t mtp_version(void);
+
+/* Profiling aid (not part of the head): while set, every call records
+ * `start_event` on its stream just before launching kernel `kernel` and
+ * `stop_event` just after it (events are cudaEvent_t passed as void*; NULL
+ * clears).  kernel: 0 projection, 1 top-K/bucket, 2 gather-score, 3 -inf
+ * fill, 4 dense head.  Process-wide, not thread-safe. */
+#define MTP_KERNEL_PROJECTION 0
+#define MTP_KERNEL_TOPK 1
+#define MTP_KERNEL_GATHER_SCORE 2
+#define MTP_KERNEL_FILL 3
+#define MTP_KERNEL_DENSE 4
+MTP_API mtp_status mtp_profile_events(int32_t kernel, void *start_event, void *stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTP_HEAD_H */

@@ -1,0 +1,371 @@
+"""Parity of the CUDA library against the CPU oracle, element by element.
+
+Every workload of the head is covered at its full size: the tiny head, the
+Gemma-scale uniform clusters at batches 1..64, lognormal variable clusters, the
+full-vocabulary scatter, and the shared-centroid stress case (both finishes),
+plus the dense comparator and edge cases (ragged and maximum batches, small and
+maximum hidden sizes, empty and oversized clusters, padded tables, exact
+integer inputs with forced ties, corrupt orderings caught on the device).
+Tolerances are those of tests/helpers.py.
+"""
+import numpy as np
+import pytest
+
+from centroid_masked_sparse_gb300 import synth
+from oracle import oracle
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="session")
+def build_lib():
+    from centroid_masked_sparse_gb300 import build
+    build.build()
+    import centroid_masked_sparse_gb300 as m
+    return m
+
+
+_DEV = {}
+
+
+def device_head(m, name, top_k=None):
+    w = synth.WORKLOADS[name]
+    key = (w.table_from or name, top_k)
+    if key not in _DEV:
+        t = helpers.tables(name)
+        k = top_k if top_k is not None else w.top_k
+        _DEV[key] = (oracle.Head.from_tables(t, k),
+                     m.MaskedHead.from_host(t.centroid_w, t.embed_w, t.token_ordering,
+                                            t.cluster_offsets, k))
+    return _DEV[key]
+
+
+def run_topk(m, dh, hidden_np):
+    h = helpers.bf16_tensor(hidden_np)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    torch.cuda.synchronize()
+    return tok.cpu().numpy(), mx.cpu().numpy()
+
+
+def check_topk(m, name, B, row0=0):
+    oh, dh = device_head(m, name)
+    hidden, ref, _ = helpers.clean_batch(name, oh, B, row0=row0)
+    tok, mx = run_topk(m, dh, hidden)
+    np.testing.assert_array_equal(tok, ref["tokens"])
+    helpers.assert_close(mx, ref["max_logit"], f"{name} B={B} max logit")
+    return hidden, ref
+
+
+def check_selection(m, dh, oh, hidden, ref_sel=None):
+    h = helpers.bf16_tensor(hidden)
+    scores, topk = m.mtp_centroid_scores(dh, h)
+    torch.cuda.synchronize()
+    ref_scores = oracle.centroid_scores(oh, hidden)
+    helpers.assert_close(scores.cpu().numpy(), ref_scores, "centroid scores")
+    topk = topk.cpu().numpy()
+    if ref_sel is not None:
+        for b in range(hidden.shape[0]):
+            assert set(topk[b].tolist()) == set(ref_sel[b].tolist()), f"row {b} selection"
+            # order: wherever consecutive oracle scores are well separated, it is the same
+            gaps = ref_scores[b, ref_sel[b][:-1]] - ref_scores[b, ref_sel[b][1:]]
+            sep = np.nonzero(gaps > helpers.MARGIN)[0]
+            for i in sep:
+                assert ref_scores[b, topk[b][i]] >= ref_scores[b, topk[b][i + 1]]
+    return scores, topk
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_tiny_every_call(build_lib, B):
+    m = build_lib
+    oh, dh = device_head(m, "tiny")
+    hidden, ref = check_topk(m, "tiny", B)
+    check_selection(m, dh, oh, hidden, ref["sel"])
+    h = helpers.bf16_tensor(hidden)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    logits, dtok, dmax = m.mtp_dense_lm_head(dh, h, want_tokens=True)
+    torch.cuda.synchronize()
+    helpers.assert_close(sc.cpu().numpy(), oracle.masked_scatter_logits(oh, hidden), "tiny scatter")
+    dref = oracle.dense_logits(oh, hidden)
+    helpers.assert_close(logits.cpu().numpy(), dref, "tiny dense")
+    top2 = np.sort(dref, axis=1)[:, -2:]
+    clear = (top2[:, 1] - top2[:, 0]) > helpers.MARGIN
+    np.testing.assert_array_equal(dtok.cpu().numpy()[clear], np.argmax(dref, axis=1)[clear])
+    helpers.assert_close(dmax.cpu().numpy(), dref.max(axis=1), "tiny dense max")
+
+
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 16, 32, 64])
+def test_uniform_topk_tokens(build_lib, B):
+    m = build_lib
+    hidden, ref = check_topk(m, "uniform", B)
+    if B in (1, 64):
+        oh, dh = device_head(m, "uniform")
+        check_selection(m, dh, oh, hidden, ref["sel"])
+
+
+def test_variable_clusters_topk_tokens(build_lib):
+    m = build_lib
+    hidden, ref = check_topk(m, "variable", 64)
+    oh, dh = device_head(m, "variable")
+    check_selection(m, dh, oh, hidden, ref["sel"])
+
+
+def test_full_vocab_scatter(build_lib):
+    m = build_lib
+    oh, dh = device_head(m, "scatter")
+    hidden, ref, _ = helpers.clean_batch("scatter", oh, 64)
+    h = helpers.bf16_tensor(hidden)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    tok, _ = m.mtp_masked_topk_tokens(dh, h)
+    torch.cuda.synchronize()
+    sc_np = sc.cpu().numpy()
+    helpers.assert_close(sc_np, oracle.masked_scatter_logits(oh, hidden), "scatter B=64")
+    # invariants: exactly K*S finite entries per row; argmax(scatter row) == sparse argmax
+    assert (np.isfinite(sc_np).sum(axis=1) == 32 * 128).all()
+    np.testing.assert_array_equal(np.argmax(sc_np, axis=1), tok.cpu().numpy())
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+
+
+@pytest.mark.parametrize("mode", ["argmax", "scatter"])
+def test_shared_centroids(build_lib, mode):
+    m = build_lib
+    oh, dh = device_head(m, "shared")
+    hidden, ref, _ = helpers.clean_batch("shared", oh, 256, need_logit_margin=(mode == "argmax"))
+    h = helpers.bf16_tensor(hidden)
+    if mode == "argmax":
+        tok, mx = m.mtp_masked_topk_tokens(dh, h)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+        helpers.assert_close(mx.cpu().numpy(), ref["max_logit"], "shared max")
+    else:
+        sc = m.mtp_masked_scatter_logits(dh, h)
+        torch.cuda.synchronize()
+        helpers.assert_close(sc.cpu().numpy(), oracle.masked_scatter_logits(oh, hidden),
+                             "shared scatter")
+    # heavy overlap is what this workload is for
+    assert len(np.unique(ref["sel"])) < 256 * 128 / 4
+
+
+def test_dense_head_full_size_sampled(build_lib):
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    hidden = synth.hidden_batch("scatter", 64)
+    h = helpers.bf16_tensor(hidden)
+    logits, dtok, dmax = m.mtp_dense_lm_head(dh, h, want_tokens=True)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    g = np.random.default_rng(5)
+    rows = g.integers(0, 64, 20000)
+    toks = g.integers(0, oh.V, 20000)
+    helpers.assert_close(lg[rows, toks], oracle.dense_logits_at(oh, hidden, rows, toks),
+                         "dense sampled")
+    # the fused argmax agrees with the logits it wrote (lower id on ties)
+    np.testing.assert_array_equal(dtok.cpu().numpy(), np.argmax(lg, axis=1))
+    np.testing.assert_array_equal(dmax.cpu().numpy(), lg.max(axis=1))
+    # and with the oracle on rows whose dense top-2 gap is clear
+    ref4 = oracle.dense_logits(oh, hidden[:4])
+    top2 = np.sort(ref4, axis=1)[:, -2:]
+    clear = (top2[:, 1] - top2[:, 0]) > helpers.MARGIN
+    np.testing.assert_array_equal(dtok.cpu().numpy()[:4][clear], np.argmax(ref4, axis=1)[clear])
+
+
+def test_k_equals_c_is_dense(build_lib):
+    m = build_lib
+    oh, dh = device_head(m, "tiny", top_k=64)
+    hidden = synth.hidden_batch("tiny", 5)
+    h = helpers.bf16_tensor(hidden)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    dl, _, _ = m.mtp_dense_lm_head(dh, h)
+    torch.cuda.synchronize()
+    ref = oracle.dense_logits(oh, hidden)
+    helpers.assert_close(sc.cpu().numpy(), ref, "masked K=C")
+    helpers.assert_close(dl.cpu().numpy(), ref, "dense")
+    # both finishes sum the same products in the same order: identical fp32
+    np.testing.assert_array_equal(sc.cpu().numpy(), dl.cpu().numpy())
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B", [3, 17, 63, 65])
+def test_ragged_batches(build_lib, B):
+    check_topk(build_lib, "uniform", B, row0=1000)
+
+
+def test_maximum_batch(build_lib):
+    check_topk(build_lib, "tiny", 1024)
+
+
+def _custom(m, V, H, C, K, seed, sizes=None, identity=False, pad_rows=0, pad_cols=0):
+    t = synth.custom_tables(V, H, C, seed, std=0.05, sizes=sizes, identity=identity)
+    ew = t.embed_w
+    if pad_rows or pad_cols:
+        big = np.zeros((V + pad_rows, H + pad_cols), dtype=np.uint16)
+        big[:V, :H] = ew
+        big[V:, :] = 0x7FC0  # NaN padding: must never be read
+        big[:, H:] = 0x7FC0
+        ew = big
+    oh = oracle.Head(t.centroid_w, ew, t.token_ordering, t.cluster_offsets, K, vocab=V)
+    torch_ew = helpers.bf16_tensor(ew)
+    dh = m.MaskedHead(helpers.bf16_tensor(t.centroid_w), torch_ew,
+                      torch.from_numpy(t.token_ordering).cuda(), K,
+                      None if t.cluster_offsets is None else torch.from_numpy(t.cluster_offsets).cuda(),
+                      vocab_size=V)
+    return t, oh, dh
+
+
+def _full_check(m, oh, dh, hidden, what):
+    ref = oracle.masked_topk_tokens(oh, hidden)
+    clear = (ref["score_margin"] > helpers.MARGIN) & (ref["logit_margin"] > helpers.MARGIN)
+    h = helpers.bf16_tensor(hidden)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(tok.cpu().numpy()[clear], ref["tokens"][clear])
+    sref = oracle.masked_scatter_logits(oh, hidden)
+    sc_np = sc.cpu().numpy()
+    sel_clear = ref["score_margin"] > helpers.MARGIN
+    helpers.assert_close(sc_np[sel_clear], sref[sel_clear], what)
+    helpers.assert_close(mx.cpu().numpy()[sel_clear], ref["max_logit"][sel_clear], what + " max")
+    return ref
+
+
+@pytest.mark.parametrize("H", [8, 72, 264, 4096])
+def test_hidden_sizes(build_lib, H):
+    m = build_lib
+    t, oh, dh = _custom(m, 2048, H, 32, 3, seed=H)
+    hidden = synth.random_hidden(7, H, H + 1)
+    _full_check(m, oh, dh, hidden, f"H={H}")
+
+
+def test_variable_clusters_empty_and_oversized(build_lib):
+    m = build_lib
+    sizes = [0] * 5 + [1, 2, 3] + [700, 1] + [37] * 20 + [0, 19]
+    V = int(sum(sizes))
+    t, oh, dh = _custom(m, V, 64, len(sizes), 6, seed=77, sizes=sizes)
+    hidden = synth.random_hidden(9, 64, 78)
+    assert (9 * V) % 4 != 0  # the -inf fill ends in a scalar tail
+    _full_check(m, oh, dh, hidden, "ragged clusters")
+
+
+def test_only_empty_clusters_selected(build_lib):
+    m = build_lib
+    sizes = [0, 0, 10, 6]
+    t, oh, dh = _custom(m, 16, 8, 4, 2, seed=3, sizes=sizes)
+    # make the empty clusters win: their centroid rows point along the hidden state
+    hidden = synth.bf16_bits(np.ones((2, 8), np.float32))
+    cw = np.zeros((4, 8), np.float32)
+    cw[0] = 1.0
+    cw[1] = 0.5
+    cw[2] = -1.0
+    cw[3] = -2.0
+    cwb = synth.bf16_bits(cw)
+    oh = oracle.Head(cwb, t.embed_w, t.token_ordering, t.cluster_offsets, 2, vocab=16)
+    dh = m.MaskedHead(helpers.bf16_tensor(cwb), dh.embed_w, dh.token_ordering, 2, dh.cluster_offsets,
+                      vocab_size=16)
+    h = helpers.bf16_tensor(hidden)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    torch.cuda.synchronize()
+    assert tok.cpu().tolist() == [-1, -1]
+    assert np.isneginf(mx.cpu().numpy()).all()
+    assert np.isneginf(sc.cpu().numpy()).all()
+    assert oracle.masked_topk_tokens(oh, hidden)["tokens"].tolist() == [-1, -1]
+
+
+def test_padded_table_and_identity_ordering(build_lib):
+    m = build_lib
+    t, oh, dh = _custom(m, 4096, 128, 64, 5, seed=21, identity=True, pad_rows=64, pad_cols=8)
+    hidden = synth.random_hidden(6, 128, 22)
+    _full_check(m, oh, dh, hidden, "padded")
+
+
+def test_integer_inputs_bit_exact_with_ties(build_lib):
+    """Small-integer inputs make every sum exact in fp32 and fp64: logits must be
+    bit-identical, and forced ties exercise both tie-break rules."""
+    m = build_lib
+    g = np.random.default_rng(11)
+    V, C, H, K, B = 512, 16, 64, 3, 12
+    cw = g.integers(-2, 3, size=(C, H)).astype(np.float32)
+    cw[5] = cw[9]          # centroids 5 and 9 always tie
+    ew = g.integers(-2, 3, size=(V, H)).astype(np.float32)
+    perm = g.permutation(V).astype(np.int32)
+    S = V // C
+    for c in range(C):     # duplicate rows inside each cluster: argmax ties between token ids
+        toks = perm[c * S:(c + 1) * S]
+        ew[toks[1]] = ew[toks[0]]
+    hid = g.integers(-2, 3, size=(B, H)).astype(np.float32)
+    cwb, ewb, hb = synth.bf16_bits(cw), synth.bf16_bits(ew), synth.bf16_bits(hid)
+    oh = oracle.Head(cwb, ewb, perm, None, K)
+    dh = m.MaskedHead(helpers.bf16_tensor(cwb), helpers.bf16_tensor(ewb),
+                      torch.from_numpy(perm).cuda(), K)
+    h = helpers.bf16_tensor(hb)
+    scores, topk = m.mtp_centroid_scores(dh, h)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    torch.cuda.synchronize()
+    ref = oracle.masked_topk_tokens(oh, hb)
+    np.testing.assert_array_equal(scores.cpu().numpy(), oracle.centroid_scores(oh, hb))
+    np.testing.assert_array_equal(topk.cpu().numpy(), ref["sel"])
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+    np.testing.assert_array_equal(mx.cpu().numpy(), ref["max_logit"])
+    np.testing.assert_array_equal(sc.cpu().numpy(), oracle.masked_scatter_logits(oh, hb))
+
+
+def test_corrupt_ordering_sets_device_error(build_lib):
+    m = build_lib
+    t, oh, dh = _custom(m, 1024, 64, 16, 16, seed=5)
+    bad = t.token_ordering.copy()
+    bad[10] = 1024 + 7       # out of range id, owned by centroid 0 (selected: K = C)
+    dbad = m.MaskedHead(dh.centroid_w, dh.embed_w, torch.from_numpy(bad).cuda(), 16, vocab_size=1024)
+    hidden = synth.random_hidden(2, 64, 6)
+    h = helpers.bf16_tensor(hidden)
+    ws = dbad.workspace(2)
+    tok, _ = m.mtp_masked_topk_tokens(dbad, h, workspace=ws)
+    assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_TOKEN_RANGE
+    # a clean call on the same workspace clears the word
+    m.mtp_masked_topk_tokens(dh, h, workspace=ws)
+    assert m.mtp_read_device_error(ws) == 0
+
+
+def test_corrupt_offsets_set_device_error(build_lib):
+    m = build_lib
+    sizes = [4, 4, 4, 4]
+    t, oh, dh = _custom(m, 16, 8, 4, 4, seed=8, sizes=sizes)
+    off = t.cluster_offsets.copy()
+    off[2] = 40              # beyond V and not ascending
+    dbad = m.MaskedHead(dh.centroid_w, dh.embed_w, dh.token_ordering, 4,
+                        torch.from_numpy(off).cuda(), vocab_size=16)
+    h = helpers.bf16_tensor(synth.random_hidden(1, 8, 9))
+    ws = dbad.workspace(1)
+    m.mtp_masked_topk_tokens(dbad, h, workspace=ws)
+    assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_OFFSETS
+
+
+def test_repeat_calls_are_deterministic(build_lib):
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    hidden = synth.hidden_batch("uniform", 64, row0=5000)
+    h = helpers.bf16_tensor(hidden)
+    ws = dh.workspace(64)
+    outs = [m.mtp_masked_topk_tokens(dh, h, workspace=ws) for _ in range(3)]
+    sc = [m.mtp_masked_scatter_logits(dh, h[:8], workspace=ws) for _ in range(2)]
+    torch.cuda.synchronize()
+    for t_, x_ in outs[1:]:
+        assert torch.equal(t_, outs[0][0]) and torch.equal(x_, outs[0][1])
+    assert torch.equal(sc[0], sc[1])
+
+
+def test_empty_batch_is_noop(build_lib):
+    m = build_lib
+    oh, dh = device_head(m, "tiny")
+    h = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    assert tok.numel() == 0
