@@ -157,6 +157,32 @@ MTP_API mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidd
                              float *out_logits, int32_t *out_tokens, float *out_max,
                              void *workspace, size_t workspace_bytes, void *stream);
 
+/* Sparse argmax for callers that cannot allocate device memory.  The paper
+ * has no counterpart of this call; it exists for callers that are handed only
+ * their input and output buffers (for example a plugin or custom-operator
+ * interface that passes tensors but no allocator) or that cannot afford
+ * cudaMalloc's possible device-wide synchronisation, and so cannot supply the
+ * workspace of mtp_masked_topk_tokens.
+ *
+ * Same arguments and results as mtp_masked_topk_tokens, without the
+ * workspace: the call uses a scratch array of MTP_NOALLOC_SCRATCH_BYTES that
+ * lives in the library's own device memory (every GPU that loads the library
+ * holds it until the process exits).  It calls no allocating routine.
+ *   - Sizes: accepted only if mtp_workspace_bytes(desc, batch) <=
+ *     MTP_NOALLOC_SCRATCH_BYTES; larger requests return MTP_ERR_UNSUPPORTED
+ *     and launch nothing.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress, with desc->device made current) and
+ *     caches it; make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, and the array keeps
+ *     the last call's contents (each call clears what must start at zero).
+ *     Calls whose kernels overlap on the GPU (different streams without
+ *     ordering between them) race on the array and give undefined results. */
+#define MTP_NOALLOC_SCRATCH_BYTES (8u << 20)
+MTP_API mtp_status mtp_masked_topk_tokens_noalloc(const mtp_head_desc *desc, const void *hidden,
+                                                  int32_t batch, int32_t *out_tokens,
+                                                  float *out_max, void *stream);
+
 /* Enqueue an asynchronous copy of the workspace's device error word (a set of
  * MTP_DEVERR_* bits, reset by each masked call) into *host_word; the value is
  * valid once `stream` has been synchronised. */
