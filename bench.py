@@ -199,22 +199,24 @@ class Timer:
             e.record()
         return evs
 
-    def run(self, fn, steps, warmup, kernel=None, ws=1):
-        """Per-step device times (ms) of fn(i) and, optionally, of one library kernel."""
+    def run(self, fn, steps, warmup, kernel=None, ws=1, extra_kernels=()):
+        """Per-step device times (ms) of fn(i) and of library kernels (events the library
+        records around each launch on the call's stream)."""
         torch, m = self.torch, self.m
         for i in range(warmup):
             self.flush.zero_()
             fn(i)
+        names = ([kernel] if kernel else []) + [k for k in extra_kernels if k != kernel]
         call_ev = self.events(2 * steps)
-        kern_ev = self.events(2 * steps) if kernel else None
+        kev = {k: self.events(2 * steps) for k in names}
         torch.cuda.synchronize()
         barrier(ws)
         torch.cuda.synchronize()
         t0 = time.time()
         for i in range(steps):
             self.flush.zero_()
-            if kernel:
-                m.mtp_profile_events(kernel, kern_ev[2 * i], kern_ev[2 * i + 1])
+            for k in names:
+                m.mtp_profile_events(k, kev[k][2 * i], kev[k][2 * i + 1])
             call_ev[2 * i].record()
             fn(i)
             call_ev[2 * i + 1].record()
@@ -222,10 +224,13 @@ class Timer:
         barrier(ws)
         torch.cuda.synchronize()
         t1 = time.time()
-        if kernel:
-            m.mtp_profile_events(kernel, None, None)
+        for k in names:
+            m.mtp_profile_events(k, None, None)
         call = [call_ev[2 * i].elapsed_time(call_ev[2 * i + 1]) for i in range(steps)]
-        kern = [kern_ev[2 * i].elapsed_time(kern_ev[2 * i + 1]) for i in range(steps)] if kernel else None
+        per = {k: [kev[k][2 * i].elapsed_time(kev[k][2 * i + 1]) for i in range(steps)] for k in names}
+        if names:
+            self.last_breakdown = {k: float(np.mean(v)) for k, v in per.items()}
+        kern = per[kernel] if kernel else None
         return call, kern, t0, t1
 
 
@@ -247,7 +252,16 @@ def measure_masked(ctx, t, dh, name, B, steps, warmup, scatter=False, rot=4, row
         mx = torch.empty(B, dtype=torch.float32, device=ctx["device"])
         fn = lambda i: m.mtp_masked_topk_tokens(dh, hs[i % rot], out_tokens=tok, out_max=mx,  # noqa: E731
                                                 workspace=ws)
-    call, kern, t0, t1 = timer.run(fn, steps, warmup, kernel="gather_score", ws=ctx["ws"])
+    # the headline: whole calls, no library events between the kernels (events recorded
+    # between launches would also stop the dependent-launch overlap)
+    call, _, t0, t1 = timer.run(fn, steps, warmup, ws=ctx["ws"])
+    # the per-kernel breakdown, in a separate shorter loop with the library's events
+    extra = ("projection", "topk") + (("fill",) if scatter else ())
+    _, kern, _, _ = timer.run(fn, max(20, steps // 4), 2, kernel="gather_score", ws=ctx["ws"],
+                              extra_kernels=extra)
+    breakdown = {k: round(v * 1e3, 2) for k, v in timer.last_breakdown.items()}
+    # every timed call must have run clean (no device-side error or timeout)
+    dev_err = m.mtp_read_device_error(ws)
     # byte model from the library's own selection of each rotated batch
     models = []
     for h in hs:
@@ -257,7 +271,8 @@ def measure_masked(ctx, t, dh, name, B, steps, warmup, scatter=False, rot=4, row
     call_ms = float(np.mean(call))
     kern_ms = float(np.mean(kern))
     return dict(call_ms=call_ms, kernel_ms=kern_ms, t0=t0, t1=t1, bytes=bm,
-                launches_per_call=4 if scatter else 3)
+                launches_per_call=4 if scatter else 3, kernels_us=breakdown,
+                max_call_us=round(float(np.max(call)) * 1e3, 2), device_error=dev_err)
 
 
 def measure_dense(ctx, t, dh, B, steps, warmup):
@@ -266,7 +281,8 @@ def measure_dense(ctx, t, dh, B, steps, warmup):
         torch.bfloat16)
     out = torch.empty(B, t.workload.vocab, dtype=torch.float32, device=ctx["device"])
     fn = lambda i: m.mtp_dense_lm_head(dh, h, out_logits=out)  # noqa: E731
-    call, kern, _, _ = timer.run(fn, steps, warmup, kernel="dense", ws=ctx["ws"])
+    call, _, _, _ = timer.run(fn, steps, warmup, ws=ctx["ws"])
+    _, kern, _, _ = timer.run(fn, max(10, steps // 2), 2, kernel="dense", ws=ctx["ws"])
     w = t.workload
     byts = w.vocab * w.hidden * 2 + B * w.hidden * 2 + B * w.vocab * 4
     ms = float(np.mean(kern))
@@ -376,6 +392,8 @@ def gpu_main(args):
                              "algorithmic_bytes": int(res["bytes"]["call"]),
                              "unique_clusters": res["bytes"]["unique_clusters"]},
            "roofline": roofline,
+           "kernels_us": res["kernels_us"],
+           "max_call_us": res["max_call_us"], "device_error": res["device_error"],
            "gpu_launches": res["launches_per_call"] * args.steps,
            "clocks": clocks}
 
@@ -395,7 +413,9 @@ def gpu_main(args):
                              "gather_us": round(r["kernel_ms"] * 1e3, 2),
                              "gather_gbs": round(ach, 1), "gather_frac": round(ach / hbm, 4),
                              "call_gbs": round(cg, 1), "call_frac": round(cg / hbm, 4),
-                             "unique_clusters": r["bytes"]["unique_clusters"]}
+                             "unique_clusters": r["bytes"]["unique_clusters"],
+                             "kernels_us": r["kernels_us"], "max_call_us": r["max_call_us"],
+                             "device_error": r["device_error"]}
         out["sweep"] = sweep
         if not args.no_extra:
             out["other_workloads"] = other_workloads(ctx, args, hbm)
@@ -427,7 +447,9 @@ def other_workloads(ctx, args, hbm):
                     "call_gbs": round(cg, 1), "call_frac": round(cg / hbm, 4),
                     "gather_us": round(r["kernel_ms"] * 1e3, 2), "gather_gbs": round(ga, 1),
                     "gather_frac": round(ga / hbm, 4),
-                    "unique_clusters": r["bytes"]["unique_clusters"]}
+                    "unique_clusters": r["bytes"]["unique_clusters"],
+                    "kernels_us": r["kernels_us"], "max_call_us": r["max_call_us"],
+                    "device_error": r["device_error"]}
         if name == "scatter":
             d = measure_dense(ctx, t, dh, w.batch, steps, args.warmup)
             gbs = d["bytes"] / (d["kernel_ms"] * 1e-3) / 1e9

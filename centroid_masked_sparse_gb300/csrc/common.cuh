@@ -15,6 +15,9 @@ constexpr int kCtrlError = 0;    // MTP_DEVERR_* bits
 constexpr int kCtrlItems = 1;    // number of gather work items built by the top-K kernel
 constexpr int kCtrlTicket = 2;   // CTAs of the gather-score kernel that have finished
 constexpr int kCtrlNext = 3;     // next work item to hand out (dynamic scheduling)
+constexpr int kCtrlWaitSite = 4; // first wait that gave up: site code (see score.cu)
+constexpr int kCtrlWaitCta = 5;  //   its CTA
+constexpr int kCtrlWaitSeq = 6;  //   its slot sequence number or h-buffer use
 constexpr int kCtrlWords = 16;
 
 // ---------------------------------------------------------------------------
@@ -56,6 +59,32 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc)
     acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
     acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
     acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+    return acc;
+}
+
+// The same sum with f32 FMAs that take the bf16 halves directly (sm_100 family):
+// products are exact and each step rounds once, so the result is bit-identical
+// to dot8_bf16 while skipping the unpacking instructions.
+__device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc)
+{
+    asm("{\n"
+        " .reg .b16 a0, a1, b0, b1;\n"
+        " mov.b32 {a0, a1}, %1;\n"
+        " mov.b32 {b0, b1}, %2;\n"
+        " fma.rn.f32.bf16 %0, a0, b0, %0;\n"
+        " fma.rn.f32.bf16 %0, a1, b1, %0;\n"
+        "}\n"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+
+__device__ __forceinline__ float dot8_bf16_mixed(uint4 a, uint4 b, float acc)
+{
+    acc = fma2_bf16(a.x, b.x, acc);
+    acc = fma2_bf16(a.y, b.y, acc);
+    acc = fma2_bf16(a.z, b.z, acc);
+    acc = fma2_bf16(a.w, b.w, acc);
     return acc;
 }
 
@@ -154,26 +183,24 @@ struct TopkParams {
     int chunk;               // tokens per work item
 };
 
-enum ScoreMode { kMaskedArgmax = 0, kMaskedScatter = 1, kDense = 2 };
-
-struct ScoreParams {
+struct GatherParams {
     const uint16_t *hidden;         // [B, H]
     const uint16_t *embed;          // [>=V, ld]
     long long ld;
-    const int32_t *ordering;        // [V] (masked modes)
+    const int32_t *ordering;        // [V]
     const int32_t *offsets;         // [C+1] or null
     const uint32_t *rowmask;        // [C, W]
     const int2 *items;
     int items_cap;
     uint32_t *ctrl;
-    unsigned long long *keys;       // [B] argmax keys (or null)
-    float *out_logits;              // [B, V] (scatter / dense logits) or null
-    int32_t *out_tokens;            // [B] (argmax modes) or null
+    unsigned long long *keys;       // [B] argmax keys (argmax finish)
+    float *out_logits;              // [B, V] (scatter finish)
+    int32_t *out_tokens;            // [B] (argmax finish)
     float *out_max;                 // [B] or null
     int B, H, V, S, W, C;
-    int chunk;                      // tokens per work item
-    int rows_per_group;             // hidden rows staged in shared memory at a time
-    int dense_items;                // dense mode: ceil(V / chunk)
+    int chunk;                      // ordered positions per work item
+    int ring;                       // embedding-row slots per CTA
+    int row_group;                  // hidden rows per h buffer
 };
 
 }  // namespace mtp

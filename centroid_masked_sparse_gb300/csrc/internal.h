@@ -20,16 +20,57 @@ int blocks_per_sm(const void *kernel, int block, size_t smem);
 // Raise a kernel's dynamic shared-memory limit once.
 cudaError_t allow_smem(const void *kernel, size_t smem);
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel on the stream is still running and must execute
+// griddepcontrol.wait before it reads that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kProjThreads = 256;
 constexpr int kProjRowsPerWarp = 2;
 constexpr int kTopkThreads = 256;
-constexpr int kScoreThreads = 128;
-constexpr int kScoreWarps = kScoreThreads / kWarp;
 
 cudaError_t launch_projection(const ProjParams &p, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
-// Launches the persistent gather-score (or dense) kernel; *grid receives the CTA count.
-cudaError_t launch_score(const ScoreParams &p, ScoreMode mode, cudaStream_t s, int *grid);
+// Gather-score kernel (score.cu): ring/row-group geometry, its shared memory, launch.
+void gather_geometry(int H, int B, int *ring, int *row_group);
+size_t gather_smem_bytes(const GatherParams &p);
+cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s);
 cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s);
+
+// Tensor-core skinny GEMM out[n, m] = sum_k table[m, k] * hidden[n, k] (gemm_tc.cu).
+struct TcGemmArgs {
+    const void *table;      // bf16 [M, K], row stride ld_table elements
+    long long ld_table;
+    int M;
+    const void *hidden;     // bf16 [N, K] contiguous
+    int N, K;
+    int splits;             // split-K factor (> 1: reduced inside a thread-block cluster)
+    float *out;             // fp32, out[n * ldo + m] (may be null with keys)
+    long long ldo;
+    unsigned long long *keys;  // per-row argmax keys (dense head) or null
+    uint32_t *ctrl;         // workspace control words: ticket for keys, error word
+    int32_t *out_tokens;    // with keys
+    float *out_max;         // with keys, optional
+    uint32_t *zero;         // words cleared at kernel start (may be null)
+    int zero_words;
+};
+constexpr int kTcProjMinBatch = 4;  // projection on tensor cores from this batch size up
+int tc_splits(int M, int N, int K);
+cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s);
 
 }  // namespace mtp

@@ -88,7 +88,7 @@ using namespace mtp;
 namespace {
 
 constexpr int kMinChunk = 8;     // smallest work item (ordered positions); sizes the item list
-constexpr int kMaxChunk = 128;
+constexpr int kMaxChunk = 64;
 
 void *g_prof[5][2] = {};
 
@@ -167,14 +167,6 @@ mtp_status use_device(int dev)
     return MTP_OK;
 }
 
-int rows_per_group(int B, int H)
-{
-    int r = 32768 / (2 * H);
-    if (r > 32) r = 32;
-    if (r < 1) r = 1;
-    return r < B ? r : B;
-}
-
 int proj_rows_per_group(int B, int H)
 {
     int r = 49152 / (2 * H);
@@ -201,17 +193,35 @@ mtp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MTP_OK : MTP_E
 mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *scores,
                       int32_t *topk, char *ws, const Layout *L, int chunk, cudaStream_t s)
 {
-    ProjParams pp{};
-    pp.hidden = (const uint16_t *)hidden;
-    pp.wc = (const uint16_t *)d->centroid_w;
-    pp.scores = scores;
-    pp.zero = ws ? (uint32_t *)ws : nullptr;
-    pp.zero_words = ws ? (int)(L->zero_end / sizeof(uint32_t)) : 0;
-    pp.B = B;
-    pp.H = d->hidden_size;
-    pp.C = d->num_centroids;
-    pp.rows_per_group = proj_rows_per_group(B, d->hidden_size);
-    {
+    if (B >= kTcProjMinBatch) {
+        // tensor cores: M = C centroid rows, N = batch, K = H, split-K in a cluster
+        TcGemmArgs g{};
+        g.table = d->centroid_w;
+        g.ld_table = d->hidden_size;
+        g.M = d->num_centroids;
+        g.hidden = hidden;
+        g.N = B;
+        g.K = d->hidden_size;
+        g.splits = tc_splits(g.M, g.N, g.K);
+        g.out = scores;
+        g.ldo = d->num_centroids;
+        g.ctrl = ws ? (uint32_t *)ws : nullptr;
+        g.zero = ws ? (uint32_t *)ws : nullptr;
+        g.zero_words = ws ? (int)(L->zero_end / sizeof(uint32_t)) : 0;
+        Prof pr(MTP_KERNEL_PROJECTION, s);
+        mtp_status st = cuda_status(launch_tc_gemm(g, s));
+        if (st != MTP_OK) return st;
+    } else {
+        ProjParams pp{};
+        pp.hidden = (const uint16_t *)hidden;
+        pp.wc = (const uint16_t *)d->centroid_w;
+        pp.scores = scores;
+        pp.zero = ws ? (uint32_t *)ws : nullptr;
+        pp.zero_words = ws ? (int)(L->zero_end / sizeof(uint32_t)) : 0;
+        pp.B = B;
+        pp.H = d->hidden_size;
+        pp.C = d->num_centroids;
+        pp.rows_per_group = proj_rows_per_group(B, d->hidden_size);
         Prof pr(MTP_KERNEL_PROJECTION, s);
         mtp_status st = cuda_status(launch_projection(pp, s));
         if (st != MTP_OK) return st;
@@ -239,12 +249,14 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
     return cuda_status(launch_topk(tp, s));
 }
 
-// Positions per work item: aim for ~8 items per resident CTA of the gather kernel.
+// Positions per work item: about 16 items per SM (one gather CTA per SM takes
+// items from a shared counter), between 8 and 64 positions (the producer warp
+// covers an item with at most two tokens per lane).
 int choose_chunk(const mtp_head_desc *d, int B)
 {
     const double avg = (double)d->vocab_size / d->num_centroids;
     const double est = (double)B * d->top_k * avg;
-    const double target = est / (8.0 * sm_count() * 4.0);
+    const double target = est / (16.0 * sm_count());
     int ch = kMinChunk;
     while (ch < kMaxChunk && 2.0 * ch <= target) ch *= 2;
     return ch;
@@ -269,32 +281,30 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s);
     if (st != MTP_OK) return st;
 
-    ScoreParams sp{};
-    sp.hidden = (const uint16_t *)hidden;
-    sp.embed = (const uint16_t *)d->embed_w;
-    sp.ld = d->ld_embed;
-    sp.ordering = d->token_ordering;
-    sp.offsets = d->cluster_offsets;
-    sp.rowmask = (const uint32_t *)(ws + L.rowmask);
-    sp.items = (const int2 *)(ws + L.items);
-    sp.items_cap = L.items_cap;
-    sp.C = d->num_centroids;
-    sp.ctrl = (uint32_t *)ws;
-    sp.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
-    sp.out_logits = out_logits;
-    sp.out_tokens = out_tokens;
-    sp.out_max = out_max;
-    sp.B = B;
-    sp.H = d->hidden_size;
-    sp.V = d->vocab_size;
-    sp.S = d->cluster_offsets ? 0 : d->vocab_size / d->num_centroids;
-    sp.W = L.W;
-    sp.chunk = chunk;
-    sp.rows_per_group = rows_per_group(B, d->hidden_size);
-    sp.dense_items = 0;
-    int grid = 0;
+    GatherParams gp{};
+    gp.hidden = (const uint16_t *)hidden;
+    gp.embed = (const uint16_t *)d->embed_w;
+    gp.ld = d->ld_embed;
+    gp.ordering = d->token_ordering;
+    gp.offsets = d->cluster_offsets;
+    gp.rowmask = (const uint32_t *)(ws + L.rowmask);
+    gp.items = (const int2 *)(ws + L.items);
+    gp.items_cap = L.items_cap;
+    gp.ctrl = (uint32_t *)ws;
+    gp.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
+    gp.out_logits = out_logits;
+    gp.out_tokens = out_tokens;
+    gp.out_max = out_max;
+    gp.B = B;
+    gp.H = d->hidden_size;
+    gp.V = d->vocab_size;
+    gp.S = d->cluster_offsets ? 0 : d->vocab_size / d->num_centroids;
+    gp.W = L.W;
+    gp.C = d->num_centroids;
+    gp.chunk = chunk;
+    gather_geometry(gp.H, B, &gp.ring, &gp.row_group);
     Prof pr(MTP_KERNEL_GATHER_SCORE, s);
-    return cuda_status(launch_score(sp, kMaskedArgmax, s, &grid));
+    return cuda_status(launch_gather(gp, out_logits != nullptr, s));
 }
 
 }  // namespace
@@ -381,24 +391,22 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
         st = cuda_status(cudaMemsetAsync(ws, 0, L.keys + (size_t)batch * sizeof(unsigned long long), s));
         if (st != MTP_OK) return st;
     }
-    ScoreParams sp{};
-    sp.hidden = (const uint16_t *)hidden;
-    sp.embed = (const uint16_t *)desc->embed_w;
-    sp.ld = desc->ld_embed;
-    sp.ctrl = out_tokens ? (uint32_t *)ws : nullptr;
-    sp.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
-    sp.out_logits = out_logits;
-    sp.out_tokens = out_tokens;
-    sp.out_max = out_max;
-    sp.B = batch;
-    sp.H = desc->hidden_size;
-    sp.V = desc->vocab_size;
-    sp.chunk = 64;
-    sp.rows_per_group = rows_per_group(batch, desc->hidden_size);
-    sp.dense_items = (desc->vocab_size + sp.chunk - 1) / sp.chunk;
-    int grid = 0;
+    TcGemmArgs g{};
+    g.table = desc->embed_w;
+    g.ld_table = desc->ld_embed;
+    g.M = desc->vocab_size;
+    g.hidden = hidden;
+    g.N = batch;
+    g.K = desc->hidden_size;
+    g.splits = 1;
+    g.out = out_logits;
+    g.ldo = desc->vocab_size;
+    g.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
+    g.ctrl = out_tokens ? (uint32_t *)ws : nullptr;
+    g.out_tokens = out_tokens;
+    g.out_max = out_max;
     Prof pr(MTP_KERNEL_DENSE, s);
-    return cuda_status(launch_score(sp, kDense, s, &grid));
+    return cuda_status(launch_tc_gemm(g, s));
 }
 
 mtp_status mtp_read_device_error(const void *workspace, uint32_t *host_word, void *stream)

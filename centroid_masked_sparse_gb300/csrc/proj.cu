@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(kProjThreads) k_projection(ProjParams p)
 {
     extern __shared__ uint4 hs[];  // [rows_per_group][H / 8]
     const int tid = threadIdx.x;
+    // let the next kernel of the call (the top-K) be scheduled now; it waits for our results
+    asm volatile("griddepcontrol.launch_dependents;");
     for (int i = blockIdx.x * kProjThreads + tid; i < p.zero_words; i += gridDim.x * kProjThreads)
         p.zero[i] = 0u;
 

@@ -1,4 +1,4 @@
-// Gather + sparse dot products + argmax / scatter, and the dense comparator.
+// Gather + sparse dot products + argmax / scatter.
 //
 // Steps 3-4 and the two finishes of Gemma4MTPMaskedEmbedder ("Add Gemma4 MTP
 // speculative decoding with centroids masking", vLLM gemma4_mtp.py):
@@ -8,170 +8,404 @@
 // forward scatters the logits into a full-vocabulary row that is -inf
 // elsewhere (the -inf fill is a separate kernel that runs first).
 //
-// Work is cluster-major: a work item is a chunk of one selected cluster's
-// ordered positions together with every batch row that selected the cluster
-// (the bucket built by the top-K kernel).  Each candidate embedding row is
-// therefore read from HBM once per call however many rows picked its
-// cluster.  A warp takes two candidate rows at a time, loads each with
-// 16-byte loads (512 contiguous bytes per warp instruction), and dots them
-// against the bucket's hidden rows staged in shared memory; a butterfly of
-// shuffles finishes each dot product.  Argmax keys (logit, lower token id)
-// are combined with a 64-bit atomicMax per row, and the last CTA to finish
-// turns them into token ids, so no grid-wide wait is ever needed.
+// Work is cluster-major and deduplicated: a work item is a chunk of one
+// selected cluster's ordered positions, together with every batch row that
+// selected the cluster (the bucket built by the top-K kernel), so each
+// candidate embedding row is read from HBM once per call however many rows
+// chose its cluster.
 //
-// Dense mode reuses the loop over every token in id order with every batch
-// row (the comparator head).
+// The kernel is a producer/consumer pipeline, one CTA per SM:
+//   - one producer warp takes work items from a global counter (prefetching
+//     the next item's metadata while it issues the current one), bulk-copies
+//     (cp.async.bulk, the TMA engine) the item's hidden rows into one of four
+//     h buffers and every candidate's embedding row (3 KB at H=1536) into a
+//     ring of ~50 shared-memory slots, one lane per slot, each completing on
+//     its own mbarrier, with an evict-first L2 policy (rows are read once);
+//   - sixteen consumer warps (eight when H > 2048) take slots in turn, dot the
+//     row against the item's hidden rows out of shared memory (16-byte lanes,
+//     f32 FMAs fed with bf16 halves, a butterfly of shuffles per dot), then
+//     either store the logit into the full-vocabulary row or keep the best
+//     (logit, lower token id) key per row in a register until the item
+//     changes, then fold it into a per-CTA 64-bit shared atomicMax.
+// So ~140 KB of candidate rows are in flight per SM without holding a single
+// register, which is what the HBM latency-bandwidth product needs.
+//
+// Barrier phases: a parity wait on an mbarrier is only meaningful while the
+// waiter is at most one phase ahead of the barrier.  Slot s carries sequence
+// numbers s, s+R, s+2R, ... and consumer warp w takes sequence numbers
+// w, w+NW, ...; with R a multiple of NW every phase of a slot goes to the same
+// warp, which waits for them in order, so no warp can wait on phase j of a slot
+// while phase j-1 is still in flight (and mistake the completed phase j-2 for
+// it).  The producer publishes at most min(32, R) consecutive sequence numbers
+// at once, so it never holds two phases of one slot either.  The last
+// CTA to finish (a ticket, never a wait) turns the per-row keys into token
+// ids.  Every mbarrier wait gives up after a wall-clock limit and records
+// MTP_DEVERR_TIMEOUT rather than hanging.
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace mtp {
 
-template <int NCH, int MODE>
-__global__ void __launch_bounds__(kScoreThreads) k_gather_score(ScoreParams p)
+using namespace sm100;
+
+namespace {
+
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kHBuffers = 4;
+constexpr int kMaxRowGroup = 8;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kTokDone = -2;
+
+// Sites of a wait that gave up, recorded once per call for diagnosis.
+enum WaitSite : uint32_t {
+    kSiteConsumerFull = 1,
+    kSiteConsumerHFull = 2,
+    kSiteConsumerLastHFull = 3,
+    kSiteProducerHEmpty = 4,
+    kSiteProducerEmpty = 5,
+    kSiteProducerDone = 6
+};
+
+__device__ __forceinline__ void record_timeout(const GatherParams &p, uint32_t site, uint32_t seq)
 {
-    extern __shared__ uint4 hs[];             // [rows_per_group][H / 8]
-    __shared__ int s_rows[MTP_MAX_BATCH];     // batch rows of the current item
-    __shared__ int s_item, s_nrows, s_last;
+    atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TIMEOUT);
+    if (atomicCAS(p.ctrl + kCtrlWaitSite, 0u, site) == 0u) {
+        p.ctrl[kCtrlWaitCta] = blockIdx.x;
+        p.ctrl[kCtrlWaitSeq] = seq;
+    }
+}
 
-    const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid / kWarp;
+struct SlotMeta {
+    int tok;      // token id, -1: skipped (invalid id), kTokDone: end of stream
+    uint32_t use; // h-buffer use number: buffer use % 4, phase parity (use / 4) & 1
+};
+
+struct HMeta {
+    int rows[kMaxRowGroup];
+    int gr;       // rows in this group
+    int left;     // slots of this item not yet consumed
+};
+
+struct Smem {
+    uint8_t *ring, *hbuf;
+    uint32_t full0, empty0, hfull0, hempty0;
+    SlotMeta *meta;
+    HMeta *hmeta;
+    unsigned long long *best;
+    int *prow;   // the producer's row list of the current item [B]
+};
+
+__device__ __forceinline__ Smem carve(uint8_t *base, const GatherParams &p)
+{
+    Smem s;
+    const size_t rb = (size_t)p.H * 2;
+    s.ring = base;
+    s.hbuf = base + (size_t)p.ring * rb;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s.hbuf + (size_t)kHBuffers * p.row_group * rb);
+    s.full0 = smem_u32(bars);
+    s.empty0 = s.full0 + 8u * p.ring;
+    s.hfull0 = s.empty0 + 8u * p.ring;
+    s.hempty0 = s.hfull0 + 8u * kHBuffers;
+    s.meta = reinterpret_cast<SlotMeta *>(bars + 2 * p.ring + 2 * kHBuffers);
+    s.hmeta = reinterpret_cast<HMeta *>(s.meta + p.ring);
+    s.best = reinterpret_cast<unsigned long long *>(s.hmeta + kHBuffers);
+    s.prow = reinterpret_cast<int *>(s.best + p.B);
+    return s;
+}
+
+// The producer warp's view of one work item; tok0/tok1 and mask are per lane.
+struct ItemMeta {
+    int valid;      // a real item (index below the item count)
+    int c, p0, nvalid;
+    int tok0, tok1; // token ids at positions p0 + lane and p0 + 32 + lane (-1 beyond nvalid)
+    uint32_t mask;  // row-mask word `lane` of the cluster (lane < W)
+};
+
+__device__ __forceinline__ int grab_item(const GatherParams &p, int lane)
+{
+    int v = 0;
+    if (lane == 0) v = (int)atomicAdd(p.ctrl + kCtrlNext, 1u);
+    return __shfl_sync(0xffffffffu, v, 0);
+}
+
+// Issue the loads of an item's metadata; the values are first used one item later,
+// so their latency overlaps the current item's copies.
+__device__ __forceinline__ void load_item(const GatherParams &p, int it, int n_items, int lane,
+                                          ItemMeta &m)
+{
+    m.valid = it < n_items;
+    m.c = -1;
+    m.p0 = 0;
+    m.nvalid = 0;
+    m.tok0 = -1;
+    m.tok1 = -1;
+    m.mask = 0u;
+    if (!m.valid) return;
+    const int2 item = p.items[it];
+    int lo = 0, hi = 0;
+    if ((unsigned)item.x < (unsigned)p.C && item.y >= 0)
+        cluster_range(p.offsets, p.V, p.S, item.x, &lo, &hi, nullptr);
+    const int p0 = item.y > hi - lo ? hi : lo + item.y;
+    const int nvalid = max(0, min(p.chunk, hi - p0));
+    m.c = item.x;
+    m.p0 = p0;
+    m.nvalid = nvalid;
+    if (nvalid == 0) return;
+    if (lane < nvalid) m.tok0 = __ldg(p.ordering + p0 + lane);
+    if (lane + kWarp < nvalid) m.tok1 = __ldg(p.ordering + p0 + kWarp + lane);
+    if (lane < p.W) m.mask = __ldcg(p.rowmask + (size_t)item.x * p.W + lane);
+}
+
+// Producer warp: takes items from the global counter and publishes, per row group,
+// the hidden rows into an h buffer and one ring slot per candidate position (each
+// lane issues its own slot's bulk copy).  False after a timed-out wait.
+__device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int consumers)
+{
+    const uint32_t rb = (uint32_t)p.H * 2;
+    const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
+    const uint64_t pol = l2_policy_evict_first();
+    const int step = min(kWarp, p.ring);
+    uint32_t seq = 0, huse = 0;
+    ItemMeta nxt;
+    load_item(p, grab_item(p, lane), n_items, lane, nxt);
+    for (;;) {
+        const ItemMeta cur = nxt;
+        if (!cur.valid) break;
+        load_item(p, grab_item(p, lane), n_items, lane, nxt);
+        if (cur.nvalid == 0) continue;
+        // the bucket's batch rows, in row order
+        const int cnt = __popc(cur.mask);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int pos = incl - cnt;
+        for (uint32_t mm = cur.mask; mm; mm &= mm - 1u) sm.prow[pos++] = lane * kWarp + __ffs(mm) - 1;
+        const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
+        __syncwarp();
+        for (int g0 = 0; g0 < total; g0 += p.row_group) {
+            const int gr = min(p.row_group, total - g0);
+            const int hb = (int)(huse % kHBuffers);
+            const uint32_t hpar = (huse / kHBuffers) & 1u;
+            int ok = 1;
+            if (lane == 0) {
+                ok = mbar_wait(sm.hempty0 + 8u * hb, hpar ^ 1u, kWaitNs);
+                if (!ok) record_timeout(p, kSiteProducerHEmpty, huse);
+                if (ok) {
+                    HMeta &hm = sm.hmeta[hb];
+                    for (int r = 0; r < gr; ++r) hm.rows[r] = sm.prow[g0 + r];
+                    hm.gr = gr;
+                    hm.left = cur.nvalid;
+                    __threadfence_block();
+                    mbar_arrive_expect_tx(sm.hfull0 + 8u * hb, (uint32_t)gr * rb);
+                }
+            }
+            // The slots of this use are published by every lane, and consumers read the
+            // metadata above once they see a slot: __syncwarp orders lane 0's stores before
+            // the other lanes' releases (a shuffle alone would not order memory).
+            __syncwarp();
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+            if (lane < gr)
+                bulk_copy_g2s(smem_u32(sm.hbuf + ((size_t)hb * p.row_group + lane) * rb),
+                              p.hidden + (size_t)sm.prow[g0 + lane] * p.H, rb, sm.hfull0 + 8u * hb);
+            ++huse;
+            for (int l0 = 0; l0 < cur.nvalid; l0 += step) {
+                const int q = l0 + lane;
+                const int a = __shfl_sync(0xffffffffu, cur.tok0, q & (kWarp - 1));
+                const int b = __shfl_sync(0xffffffffu, cur.tok1, q & (kWarp - 1));
+                bool lok = true;
+                if (lane < step && q < cur.nvalid) {
+                    int tok = q < kWarp ? a : b;
+                    if ((unsigned)tok >= (unsigned)p.V) {
+                        atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
+                        tok = -1;
+                    }
+                    const uint32_t sq = seq + (uint32_t)q;
+                    const uint32_t slot = sq % (uint32_t)p.ring;
+                    const uint32_t par = (sq / (uint32_t)p.ring) & 1u;
+                    lok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, kWaitNs);
+                    if (!lok) record_timeout(p, kSiteProducerEmpty, sq);
+                    if (lok) {
+                        sm.meta[slot].tok = tok;
+                        sm.meta[slot].use = huse - 1u;
+                        if (tok >= 0) {
+                            mbar_arrive_expect_tx(sm.full0 + 8u * slot, rb);
+                            bulk_copy_g2s_hint(smem_u32(sm.ring + (size_t)slot * rb),
+                                               p.embed + (long long)tok * p.ld, rb, sm.full0 + 8u * slot,
+                                               pol);
+                        } else {
+                            mbar_arrive(sm.full0 + 8u * slot);
+                        }
+                    }
+                }
+                if (__any_sync(0xffffffffu, !lok)) return false;
+            }
+            seq += (uint32_t)cur.nvalid;
+        }
+    }
+    // one end-of-stream marker per consumer warp
+    bool ok = true;
+    if (lane < consumers) {
+        const uint32_t sq = seq + (uint32_t)lane;
+        const uint32_t slot = sq % (uint32_t)p.ring;
+        const uint32_t par = (sq / (uint32_t)p.ring) & 1u;
+        ok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, kWaitNs);
+        if (!ok) record_timeout(p, kSiteProducerDone, sq);
+        if (ok) {
+            sm.meta[slot].tok = kTokDone;
+            sm.meta[slot].use = 0u;
+            mbar_arrive(sm.full0 + 8u * slot);
+        }
+    }
+    return !__any_sync(0xffffffffu, !ok);
+}
+
+template <int NCH, bool SCATTER, int NW>
+__device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lane)
+{
+    const uint32_t rb = (uint32_t)p.H * 2;
     const int hv = p.H >> 3;
-    const bool want_keys = p.keys != nullptr;
-    const bool want_logits = p.out_logits != nullptr;
-    const int n_items = (MODE == kDense) ? p.dense_items : (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-
-    for (int round = 0;; ++round) {
-        int it;
-        if (MODE == kDense) {
-            it = blockIdx.x + round * gridDim.x;
-        } else {
-            // dynamic hand-out: items differ in size (ragged clusters, bucket sizes)
-            if (tid == 0) s_item = (int)atomicAdd(p.ctrl + kCtrlNext, 1u);
-            __syncthreads();
-            it = s_item;
-        }
-        if (it >= n_items)
+    uint32_t ready_use = 0xffffffffu;   // h-buffer use whose rows are known to have landed
+    uint32_t best_use = 0xffffffffu;    // use whose argmax this warp holds in registers
+    unsigned long long best = 0ull;     // lane r: best key of row best_row of that use
+    int best_row = 0;
+    bool ok = true;
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t seq = (uint32_t)warp + k * NW;
+        const uint32_t slot = seq % (uint32_t)p.ring;
+        const uint32_t par = (seq / (uint32_t)p.ring) & 1u;
+        if (!mbar_wait(sm.full0 + 8u * slot, par, kWaitNs)) {
+            if (lane == 0) record_timeout(p, kSiteConsumerFull, seq);
+            ok = false;
             break;
-
-        int pbeg, pend, nrows;
-        if (MODE == kDense) {
-            pbeg = it * p.chunk;
-            pend = min(p.V, pbeg + p.chunk);
-            nrows = p.B;
-        } else {
-            int2 item = p.items[it];
-            int lo = 0, hi = 0;
-            // items are written by the top-K kernel; the checks only matter when malformed
-            // offsets made it drop some (then a slot may hold an earlier call's item)
-            if ((unsigned)item.x >= (unsigned)p.C || item.y < 0) item = make_int2(0, 0x7fffffff);
-            cluster_range(p.offsets, p.V, p.S, item.x, &lo, &hi, nullptr);
-            pbeg = (item.y > hi - lo) ? hi : lo + item.y;
-            pend = min(hi, pbeg + p.chunk);
-            if (warp == 0) {
-                uint32_t w = lane < p.W ? p.rowmask[(size_t)item.x * p.W + lane] : 0u;
-                const int cnt = __popc(w);
-                int incl = cnt;
-#pragma unroll
-                for (int o = 1; o < kWarp; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                int pos = incl - cnt;
-                while (w) {
-                    const int bit = __ffs(w) - 1;
-                    s_rows[pos++] = lane * kWarp + bit;
-                    w &= w - 1u;
-                }
-                if (lane == kWarp - 1) s_nrows = incl;
-            }
-            __syncthreads();
-            nrows = s_nrows;
         }
-
-        for (int g0 = 0; g0 < nrows; g0 += p.rows_per_group) {
-            const int gr = min(p.rows_per_group, nrows - g0);
-            for (int i = tid; i < gr * hv; i += kScoreThreads) {
-                const int r = i / hv, k = i - r * hv;
-                const int row = (MODE == kDense) ? g0 + r : s_rows[g0 + r];
-                hs[i] = ld_ro16(p.hidden + (size_t)row * p.H + (size_t)k * 8);
+        const SlotMeta m = sm.meta[slot];
+        if (m.tok == kTokDone) break;
+        const int hb = (int)(m.use % kHBuffers);
+        const uint32_t hpar = (m.use / kHBuffers) & 1u;
+        if (!SCATTER && m.use != best_use) {
+            // a new item: fold the previous item's per-row bests into the CTA's keys
+            if (best) atomicMax(sm.best + best_row, best);
+            best = 0ull;
+            best_use = m.use;
+        }
+        if (m.tok >= 0) {
+            if (m.use != ready_use) {
+                if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, kWaitNs)) {
+                    if (lane == 0) record_timeout(p, kSiteConsumerHFull, m.use);
+                    ok = false;
+                    break;
+                }
+                ready_use = m.use;
             }
-            __syncthreads();
-
-            // lane r keeps the running best of the group's r-th row
-            const int my_row = lane < gr ? ((MODE == kDense) ? g0 + lane : s_rows[g0 + lane]) : 0;
-            unsigned long long best = 0ull;
-
-            for (int pa = pbeg + warp; pa < pend; pa += 2 * kScoreWarps) {
-                const int pb = pa + kScoreWarps;
-                const bool has_b = pb < pend;
-                int ta, tb;
-                if (MODE == kDense) {
-                    ta = pa;
-                    tb = pb;
-                } else {
-                    ta = __ldg(p.ordering + pa);
-                    tb = has_b ? __ldg(p.ordering + pb) : 0;
-                }
-                const bool ok_a = (unsigned)ta < (unsigned)p.V;
-                const bool ok_b = has_b && (unsigned)tb < (unsigned)p.V;
-                if (MODE != kDense && lane == 0 && (!ok_a || (has_b && !ok_b)))
-                    atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
-                const uint16_t *ra = p.embed + (long long)(ok_a ? ta : 0) * p.ld;
-                const uint16_t *rb = p.embed + (long long)(ok_b ? tb : 0) * p.ld;
-
-                uint4 ea[NCH], eb[NCH];
+            const uint4 *erow = reinterpret_cast<const uint4 *>(sm.ring + (size_t)slot * rb);
+            uint4 e[NCH];
 #pragma unroll
-                for (int k = 0; k < NCH; ++k) {
-                    const int idx = k * kWarp + lane;
-                    const bool in = idx < hv;
-                    ea[k] = (in && ok_a) ? ld_stream16(ra + idx * 8) : zero;
-                    eb[k] = (in && ok_b) ? ld_stream16(rb + idx * 8) : zero;
-                }
-                for (int r = 0; r < gr; ++r) {
-                    float sa = 0.f, sb = 0.f;
+            for (int c = 0; c < NCH; ++c) {
+                const int idx = c * kWarp + lane;
+                e[c] = idx < hv ? erow[idx] : zero;
+            }
+            const HMeta &hm = sm.hmeta[hb];
+            const int gr = hm.gr;
+            for (int r = 0; r < gr; ++r) {
+                const uint4 *hrow =
+                    reinterpret_cast<const uint4 *>(sm.hbuf + ((size_t)hb * p.row_group + r) * rb);
+                float acc = 0.f;
 #pragma unroll
-                    for (int k = 0; k < NCH; ++k) {
-                        const int idx = k * kWarp + lane;
-                        if (idx < hv) {
-                            const uint4 x = hs[r * hv + idx];
-                            sa = dot8_bf16(ea[k], x, sa);
-                            sb = dot8_bf16(eb[k], x, sb);
-                        }
-                    }
-                    sa = warp_sum(sa);
-                    sb = warp_sum(sb);
-                    if (lane == r) {
-                        if (want_keys) {
-                            if (ok_a) best = max(best, argmax_key(sa, ta));
-                            if (ok_b) best = max(best, argmax_key(sb, tb));
-                        }
-                        if (want_logits) {
-                            float *orow = p.out_logits + (size_t)my_row * p.V;
-                            if (ok_a) orow[ta] = sa;
-                            if (ok_b) orow[tb] = sb;
-                        }
+                for (int c = 0; c < NCH; ++c) {
+                    const int idx = c * kWarp + lane;
+                    if (idx < hv) acc = dot8_bf16_mixed(e[c], hrow[idx], acc);
+                }
+                acc = warp_sum(acc);
+                if (lane == r) {
+                    const int row = hm.rows[r];
+                    if (SCATTER) {
+                        p.out_logits[(size_t)row * p.V + m.tok] = acc;
+                    } else {
+                        const unsigned long long key = argmax_key(acc, m.tok);
+                        best = key > best ? key : best;
+                        best_row = row;
                     }
                 }
             }
-            if (want_keys && lane < gr && best != 0ull)
-                atomicMax(p.keys + my_row, best);
-            __syncthreads();  // hs and s_rows are rewritten next
         }
+        // release the slot (and, for the item's last slot, its h buffer)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(sm.empty0 + 8u * slot);
+            if (atomicSub(&sm.hmeta[hb].left, 1) == 1) {
+                // the item's last slot: its hidden rows must have landed (a skipped slot never
+                // waited for them) before the producer may refill the buffer
+                if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, kWaitNs)) {
+                    record_timeout(p, kSiteConsumerLastHFull, m.use);
+                    ok = false;
+                }
+                mbar_arrive(sm.hempty0 + 8u * hb);
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
     }
+    if (!SCATTER && best) atomicMax(sm.best + best_row, best);
+    return ok;
+}
 
-    if (!want_keys)
+template <int NCH, bool SCATTER, int NW>
+__global__ void __launch_bounds__((NW + 1) * kWarp, 1) k_gather_score(const GatherParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int s_last;
+    constexpr int kThreads = (NW + 1) * kWarp;
+    const Smem sm = carve(smem, p);
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x & (kWarp - 1);
+
+    if (p.ring % NW != 0) {
+        // a slot shared by two consumer warps could be waited one phase early: refuse
+        if (threadIdx.x == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TIMEOUT);
         return;
-    // Last CTA to finish decodes the per-row keys (threadfence-reduction pattern).
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned t = atomicAdd(p.ctrl + kCtrlTicket, 1u);
-        s_last = (t == gridDim.x - 1);
     }
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < p.ring; ++r) {
+            mbar_init(sm.full0 + 8u * r, 1);
+            mbar_init(sm.empty0 + 8u * r, 1);
+        }
+        for (int b = 0; b < kHBuffers; ++b) {
+            mbar_init(sm.hfull0 + 8u * b, 1);
+            mbar_init(sm.hempty0 + 8u * b, 1);
+        }
+        fence_barrier_init();
+    }
+    if (!SCATTER)
+        for (int b = threadIdx.x; b < p.B; b += kThreads) sm.best[b] = 0ull;
     __syncthreads();
-    if (!s_last)
-        return;
+    // the work items, row masks and counters come from the top-K kernel before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    bool ok = true;
+    if (warp == NW) {
+        ok = produce(p, sm, lane, NW);
+    } else {
+        ok = consume<NCH, SCATTER, NW>(p, sm, warp, lane);
+    }
+    if (!ok && lane == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TIMEOUT);
+    __syncthreads();
+
+    if (SCATTER) return;
+    for (int b = threadIdx.x; b < p.B; b += kThreads) {
+        const unsigned long long k = sm.best[b];
+        if (k) atomicMax(p.keys + b, k);
+    }
+    // the last CTA to finish turns the keys into token ids
     __threadfence();
-    for (int b = tid; b < p.B; b += kScoreThreads) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(p.ctrl + kCtrlTicket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int b = threadIdx.x; b < p.B; b += kThreads) {
         const unsigned long long k = atomicAdd(p.keys + b, 0ull);
         int32_t tok;
         float v;
@@ -181,46 +415,84 @@ __global__ void __launch_bounds__(kScoreThreads) k_gather_score(ScoreParams p)
     }
 }
 
-template <int NCH, int MODE>
-static cudaError_t run_score(const ScoreParams &p, cudaStream_t s, int *grid_out)
+// 16 consumer warps while the row registers allow it (H <= 2048), else 8.
+template <int NCH>
+constexpr int consumer_warps()
 {
-    const size_t smem = (size_t)p.rows_per_group * p.H * sizeof(uint16_t);
-    const void *fn = (const void *)k_gather_score<NCH, MODE>;
-    cudaError_t e = allow_smem(fn, smem);
-    if (e != cudaSuccess)
-        return e;
-    int per_sm = blocks_per_sm(fn, kScoreThreads, smem);
-    if (per_sm < 1) per_sm = 1;
-    int grid = sm_count() * per_sm;
-    if (MODE == kDense && grid > p.dense_items) grid = p.dense_items;
-    if (grid < 1) grid = 1;
-    *grid_out = grid;
-    k_gather_score<NCH, MODE><<<grid, kScoreThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return NCH <= 8 ? 16 : 8;  // keep in step with gather_consumer_warps()
 }
 
-template <int MODE>
-static cudaError_t dispatch_score(const ScoreParams &p, cudaStream_t s, int *grid)
+template <int NCH, bool SCATTER>
+cudaError_t run_gather(const GatherParams &p, cudaStream_t s)
+{
+    constexpr int NW = consumer_warps<NCH>();
+    const void *fn = (const void *)k_gather_score<NCH, SCATTER, NW>;
+    const size_t smem = gather_smem_bytes(p);
+    cudaError_t e = allow_smem(fn, smem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(k_gather_score<NCH, SCATTER, NW>, dim3(sm_count()), dim3((NW + 1) * kWarp),
+                            smem, s, p);
+}
+
+template <bool SCATTER>
+cudaError_t dispatch_gather(const GatherParams &p, cudaStream_t s)
 {
     switch (chunks_for_hidden(p.H)) {
-    case 1: return run_score<1, MODE>(p, s, grid);
-    case 2: return run_score<2, MODE>(p, s, grid);
-    case 3: return run_score<3, MODE>(p, s, grid);
-    case 4: return run_score<4, MODE>(p, s, grid);
-    case 5: return run_score<5, MODE>(p, s, grid);
-    case 6: return run_score<6, MODE>(p, s, grid);
-    case 8: return run_score<8, MODE>(p, s, grid);
-    case 10: return run_score<10, MODE>(p, s, grid);
-    case 12: return run_score<12, MODE>(p, s, grid);
-    case 16: return run_score<16, MODE>(p, s, grid);
+    case 1: return run_gather<1, SCATTER>(p, s);
+    case 2: return run_gather<2, SCATTER>(p, s);
+    case 3: return run_gather<3, SCATTER>(p, s);
+    case 4: return run_gather<4, SCATTER>(p, s);
+    case 5: return run_gather<5, SCATTER>(p, s);
+    case 6: return run_gather<6, SCATTER>(p, s);
+    case 8: return run_gather<8, SCATTER>(p, s);
+    case 10: return run_gather<10, SCATTER>(p, s);
+    case 12: return run_gather<12, SCATTER>(p, s);
+    case 16: return run_gather<16, SCATTER>(p, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_score(const ScoreParams &p, ScoreMode mode, cudaStream_t s, int *grid)
+}  // namespace
+
+size_t gather_smem_bytes(const GatherParams &p)
 {
-    return mode == kDense ? dispatch_score<kDense>(p, s, grid)
-                          : dispatch_score<kMaskedArgmax>(p, s, grid);
+    const size_t rb = (size_t)p.H * 2;
+    return (size_t)p.ring * rb + (size_t)kHBuffers * p.row_group * rb +
+           (size_t)(2 * p.ring + 2 * kHBuffers) * 8 + (size_t)p.ring * sizeof(SlotMeta) +
+           kHBuffers * sizeof(HMeta) + (size_t)p.B * 12;
+}
+
+// Consumer warps of the gather kernel for rows of H elements.
+static int gather_consumer_warps(int H)
+{
+    const int nch = chunks_for_hidden(H);
+    return nch <= 8 ? 16 : 8;
+}
+
+// Ring slots and hidden rows per h buffer for a given H and batch, within the
+// shared-memory budget of one CTA per SM.  The ring is a multiple of the
+// consumer warp count, so each slot always belongs to the same warp (see the
+// kernel's comment on barrier phases).
+void gather_geometry(int H, int B, int *ring, int *row_group)
+{
+    const size_t rb = (size_t)H * 2;
+    int rg = (int)(16384 / rb);
+    rg = rg < 1 ? 1 : (rg > kMaxRowGroup ? kMaxRowGroup : rg);
+    if (rg > B) rg = B;
+    const size_t budget = 212 * 1024;
+    const size_t fixed = (size_t)kHBuffers * rg * rb + kHBuffers * (sizeof(HMeta) + 16) + (size_t)B * 12 + 64;
+    long long r = (long long)((budget - fixed) / (rb + 16 + sizeof(SlotMeta)));
+    const int nw = gather_consumer_warps(H);
+    if (r > 256) r = 256;
+    r = r / nw * nw;
+    if (r < nw) r = nw;
+    *ring = (int)r;
+    *row_group = rg;
+}
+
+cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s)
+{
+    return scatter ? dispatch_gather<true>(p, s) : dispatch_gather<false>(p, s);
 }
 
 // forward's fill: every entry of the [B, V] row block is -inf before the

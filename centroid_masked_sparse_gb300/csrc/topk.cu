@@ -5,10 +5,13 @@
 // the centroid scores of each row.  Ties go to the lower centroid index, and
 // the selected list is written sorted by (score desc, index asc).
 //
-// One CTA per row.  The K-th largest score is found by a 4-pass radix select
-// (8 bits a pass) over order-preserving uint32 keys held in shared memory; the
-// selection is then every key above it plus the lowest-indexed keys equal to
-// it.  No sort of the C scores is needed.
+// One CTA per row.  Fast path: 256 buckets linear in the score between the
+// row's min and max; the candidates are the scores in the bucket of the K-th
+// largest and above (a few dozen for Gaussian-like scores), ranked exactly by
+// 64-bit (score, lower index) keys.  When that bucket is crowded (ties, odd
+// distributions) the fallback is a 4-pass radix select (8 bits a pass) over
+// order-preserving uint32 keys, then every key above the K-th plus the
+// lowest-indexed keys equal to it.  No sort of the C scores is needed.
 //
 // Bucketing (masked calls): each selection (b, c) sets bit b of the cluster's
 // row mask, and the first row to select a cluster appends that cluster's work
@@ -50,6 +53,42 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int *s_scan, int *total
     return excl;
 }
 
+constexpr int kCandCap = 512;
+
+// Bucket of a score for the fast path: monotone non-decreasing in v (each float
+// step rounds monotonically), clamped so that any input stays in range.
+__device__ __forceinline__ int value_bucket(float v, float vmin, float scale)
+{
+    const float x = (v - vmin) * scale;
+    int q = x >= 0.f ? (int)x : 0;
+    return q > 255 ? 255 : q;
+}
+
+__device__ __forceinline__ unsigned long long select_key(uint32_t ord, int c)
+{
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xffffffffu - (uint32_t)c);
+}
+
+// Bucketing of one selection (row b picked centroid c): see the file comment.
+__device__ __forceinline__ void bucket_selection(const TopkParams &p, int b, int c)
+{
+    atomicOr(&p.rowmask[(size_t)c * p.W + (b >> 5)], 1u << (b & 31));
+    if (atomicAdd(&p.ccount[c], 1) == 0) {
+        int lo, hi;
+        if (cluster_range(p.offsets, p.V, p.S, c, &lo, &hi, p.ctrl + kCtrlError) && hi > lo) {
+            const int n = (hi - lo + p.chunk - 1) / p.chunk;
+            const uint32_t base = atomicAdd(p.ctrl + kCtrlItems, (uint32_t)n);
+            // Ascending offsets cannot overflow the list (it is sized for V / chunk + C
+            // items); overlapping ranges can, so they are reported and dropped.
+            if (base + (uint32_t)n > (uint32_t)p.items_cap) {
+                atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
+            } else {
+                for (int j = 0; j < n; ++j) p.items[base + j] = make_int2(c, j * p.chunk);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
 {
     extern __shared__ uint32_t sm[];
@@ -58,11 +97,102 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     __shared__ uint32_t hist[256];
     __shared__ int s_scan[kWarp + 1];
     __shared__ uint32_t s_digit, s_above;
+    __shared__ float s_min[kTopkThreads / kWarp], s_max[kTopkThreads / kWarp];
+    __shared__ unsigned long long s_cand[kCandCap];
+    __shared__ int s_ncand;
 
-    const int b = blockIdx.x, tid = threadIdx.x;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid / kWarp;
+    // the scores are written by the projection kernel that precedes this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const float *row = p.scores + (size_t)b * p.C;
+    float lmin = __int_as_float(0x7f800000), lmax = __int_as_float(0xff800000);
+    for (int c = tid; c < p.C; c += kTopkThreads) {
+        const float v = row[c];
+        keys[c] = ord_key(v);
+        lmin = fminf(lmin, v);
+        lmax = fmaxf(lmax, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+        lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    }
+    if (lane == 0) {
+        s_min[warp] = lmin;
+        s_max[warp] = lmax;
+    }
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
+    if (tid == 0) s_ncand = 0;
+    __syncthreads();
+
+    // Fast path: 256 buckets linear in the score between the row's min and max (the
+    // Gaussian-like scores then spread over many buckets), the bucket holding the
+    // K-th largest score, and an exact rank of every score in or above it.
+    float vmin = s_min[0], vmax = s_max[0];
+    for (int w = 1; w < kTopkThreads / kWarp; ++w) {
+        vmin = fminf(vmin, s_min[w]);
+        vmax = fmaxf(vmax, s_max[w]);
+    }
+    const float span = vmax - vmin;
+    const float scale = (span > 0.f && span < __int_as_float(0x7f800000)) ? 255.5f / span : 0.f;
     for (int c = tid; c < p.C; c += kTopkThreads)
-        keys[c] = ord_key(row[c]);
+        atomicAdd(&hist[value_bucket(row[c], vmin, scale)], 1u);
+    __syncthreads();
+    if (tid < kWarp) {
+        uint32_t loc[8], sum = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            loc[j] = hist[255 - (lane * 8 + j)];
+            sum += loc[j];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - sum;
+        const uint32_t need = (uint32_t)p.K;
+        if (excl < need && need <= incl) {
+            uint32_t run = excl;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (run + loc[j] >= need) {
+                    s_digit = 255u - (uint32_t)(lane * 8 + j);
+                    s_above = run + loc[j];   // candidates: this bucket and every one above
+                    break;
+                }
+                run += loc[j];
+            }
+        }
+    }
+    __syncthreads();
+    const int kbucket = (int)s_digit;
+    const int ncand = (int)s_above;
+    if (ncand <= kCandCap) {
+        for (int c = tid; c < p.C; c += kTopkThreads) {
+            if (value_bucket(row[c], vmin, scale) >= kbucket) {
+                const int pos = atomicAdd(&s_ncand, 1);
+                s_cand[pos] = select_key(keys[c], c);
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < ncand; i += kTopkThreads) {
+            const unsigned long long ki = s_cand[i];
+            int rank = 0;
+            for (int j = 0; j < ncand; ++j) rank += s_cand[j] > ki;
+            if (rank < p.K) {
+                const int c = (int)(0xffffffffu - (uint32_t)(ki & 0xffffffffull));
+                p.topk[(size_t)b * p.K + rank] = c;
+                sel[rank] = c;
+            }
+        }
+        __syncthreads();
+        if (p.rowmask)
+            for (int i = tid; i < p.K; i += kTopkThreads) bucket_selection(p, b, sel[i]);
+        return;
+    }
 
     // Radix select: after the passes, `prefix` is the K-th largest key and
     // `need` the number of keys equal to it that belong to the selection.
@@ -71,10 +201,16 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
         for (int i = tid; i < 256; i += kTopkThreads)
             hist[i] = 0u;
         __syncthreads();
-        for (int c = tid; c < p.C; c += kTopkThreads) {
-            const uint32_t u = keys[c];
-            if ((u & mask) == prefix)
-                atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        // Scores crowd into few bins of the high digits, so lanes that hit the same
+        // bin combine their increments (one shared atomic per bin per warp).
+        for (int c0 = 0; c0 < p.C; c0 += kTopkThreads) {
+            const int c = c0 + tid;
+            const uint32_t u = c < p.C ? keys[c] : 0u;
+            const bool hit = c < p.C && (u & mask) == prefix;
+            const uint32_t bin = (u >> shift) & 255u;
+            const unsigned peers = __match_any_sync(0xffffffffu, hit ? bin : 256u + (tid & 31));
+            if (hit && (tid & 31) == __ffs(peers) - 1)
+                atomicAdd(&hist[bin], (uint32_t)__popc(peers));
         }
         __syncthreads();
         if (tid < kWarp) {
@@ -156,25 +292,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
 
     if (p.rowmask == nullptr)
         return;
-    for (int i = tid; i < p.K; i += kTopkThreads) {
-        const int c = sel[i];
-        atomicOr(&p.rowmask[(size_t)c * p.W + (b >> 5)], 1u << (b & 31));
-        if (atomicAdd(&p.ccount[c], 1) == 0) {
-            int lo, hi;
-            if (cluster_range(p.offsets, p.V, p.S, c, &lo, &hi, p.ctrl + kCtrlError) && hi > lo) {
-                const int n = (hi - lo + p.chunk - 1) / p.chunk;
-                const uint32_t base = atomicAdd(p.ctrl + kCtrlItems, (uint32_t)n);
-                // Ascending offsets cannot overflow the list (it is sized for V / chunk + C
-                // items); overlapping ranges can, so they are reported and dropped.
-                if (base + (uint32_t)n > (uint32_t)p.items_cap) {
-                    atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
-                } else {
-                    for (int j = 0; j < n; ++j)
-                        p.items[base + j] = make_int2(c, j * p.chunk);
-                }
-            }
-        }
-    }
+    for (int i = tid; i < p.K; i += kTopkThreads) bucket_selection(p, b, sel[i]);
 }
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
@@ -183,8 +301,7 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
     cudaError_t e = allow_smem((const void *)k_topk, smem);
     if (e != cudaSuccess)
         return e;
-    k_topk<<<p.B, kTopkThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(k_topk, dim3(p.B), dim3(kTopkThreads), smem, s, p);
 }
 
 }  // namespace mtp

@@ -80,6 +80,8 @@ typedef enum mtp_status {
 /* Bits of the device error word (OR-ed together over one call). */
 #define MTP_DEVERR_TOKEN_RANGE 0x1u  /* token_ordering held an id outside [0, V) */
 #define MTP_DEVERR_OFFSETS 0x2u      /* cluster_offsets not ascending in [0, V]  */
+#define MTP_DEVERR_TIMEOUT 0x4u      /* a tensor-core pipeline wait gave up (its
+                                        results are invalid; nothing hung)        */
 
 /* The head's tables.  Plain data: the struct is read on the host at each call
  * and may live anywhere on the host.

@@ -186,8 +186,25 @@ def test_k_equals_c_is_dense(build_lib):
     ref = oracle.dense_logits(oh, hidden)
     helpers.assert_close(sc.cpu().numpy(), ref, "masked K=C")
     helpers.assert_close(dl.cpu().numpy(), ref, "dense")
-    # both finishes sum the same products in the same order: identical fp32
-    np.testing.assert_array_equal(sc.cpu().numpy(), dl.cpu().numpy())
+    # the masked path (CUDA cores) and the dense head (tensor cores) agree
+    helpers.assert_close(sc.cpu().numpy(), dl.cpu().numpy().astype(np.float64), "masked vs dense")
+
+
+def test_projection_paths_agree(build_lib):
+    """Batches below 4 rows use the CUDA-core projection, larger ones the tensor-core
+    GEMM with a cluster split-K: the same rows must score alike either way."""
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    hidden = synth.hidden_batch("uniform", 24, row0=900)
+    h = helpers.bf16_tensor(hidden)
+    big, big_top = m.mtp_centroid_scores(dh, h)
+    small = torch.cat([m.mtp_centroid_scores(dh, h[i:i + 1])[0] for i in range(24)])
+    torch.cuda.synchronize()
+    ref = oracle.centroid_scores(oh, hidden)
+    helpers.assert_close(big.cpu().numpy(), ref, "tensor-core projection")
+    helpers.assert_close(small.cpu().numpy(), ref, "CUDA-core projection")
+    d = np.abs(big.cpu().numpy().astype(np.float64) - small.cpu().numpy())
+    assert d.max() < 1e-3
 
 
 # ---------------------------------------------------------------------------
@@ -234,6 +251,12 @@ def _full_check(m, oh, dh, hidden, what):
     sel_clear = ref["score_margin"] > helpers.MARGIN
     helpers.assert_close(sc_np[sel_clear], sref[sel_clear], what)
     helpers.assert_close(mx.cpu().numpy()[sel_clear], ref["max_logit"][sel_clear], what + " max")
+    # the dense head (tensor-core GEMM) on the same tables
+    dl, dtok, _ = m.mtp_dense_lm_head(dh, h, want_tokens=True)
+    torch.cuda.synchronize()
+    dref = oracle.dense_logits(oh, hidden)
+    helpers.assert_close(dl.cpu().numpy(), dref, what + " dense")
+    np.testing.assert_array_equal(dtok.cpu().numpy(), np.argmax(dl.cpu().numpy(), axis=1))
     return ref
 
 
@@ -319,6 +342,26 @@ def test_integer_inputs_bit_exact_with_ties(build_lib):
     np.testing.assert_array_equal(sc.cpu().numpy(), oracle.masked_scatter_logits(oh, hb))
 
 
+@pytest.mark.parametrize("name", ["tiny", "uniform"])
+def test_all_equal_scores(build_lib, name):
+    """Zero hidden states make every centroid score and every logit 0: the selection is
+    the K lowest centroid indices and the token the lowest id among their candidates.
+    At C=2048 every score lands in one bucket, which exercises the radix fallback of
+    the top-K kernel; at C=64 the bucketed fast path handles the ties."""
+    m = build_lib
+    oh, dh = device_head(m, name)
+    hidden = np.zeros((5, oh.H), dtype=np.uint16)
+    h = helpers.bf16_tensor(hidden)
+    scores, topk = m.mtp_centroid_scores(dh, h)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    torch.cuda.synchronize()
+    ref = oracle.masked_topk_tokens(oh, hidden)
+    np.testing.assert_array_equal(topk.cpu().numpy(), np.tile(np.arange(oh.K), (5, 1)))
+    np.testing.assert_array_equal(topk.cpu().numpy(), ref["sel"])
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+    assert (mx.cpu().numpy() == 0).all()
+
+
 def test_corrupt_ordering_sets_device_error(build_lib):
     m = build_lib
     t, oh, dh = _custom(m, 1024, 64, 16, 16, seed=5)
@@ -361,6 +404,69 @@ def test_repeat_calls_are_deterministic(build_lib):
     for t_, x_ in outs[1:]:
         assert torch.equal(t_, outs[0][0]) and torch.equal(x_, outs[0][1])
     assert torch.equal(sc[0], sc[1])
+
+
+@pytest.mark.parametrize("name,B,calls", [("uniform", 64, 60), ("shared", 256, 12)])
+def test_repeated_calls_stay_identical(build_lib, name, B, calls):
+    """Many consecutive calls on one workspace, in both finishes: every call must report
+    a clean device error word (no pipeline wait gave up) and reproduce the first call's
+    output bit for bit (no stale shared-memory metadata, no lost work item)."""
+    m = build_lib
+    oh, dh = device_head(m, name)
+    t = helpers.tables(name)
+    hidden = synth.hidden_batch(name, B, None, t.prototypes, row0=3000)
+    h = helpers.bf16_tensor(hidden)
+    ws = dh.workspace(B)
+    first_tok, first_max = m.mtp_masked_topk_tokens(dh, h, workspace=ws)
+    first_sc = m.mtp_masked_scatter_logits(dh, h, workspace=ws)
+    assert m.mtp_read_device_error(ws) == 0
+    tok = torch.empty_like(first_tok)
+    mx = torch.empty_like(first_max)
+    sc = torch.empty_like(first_sc)
+    for i in range(calls):
+        m.mtp_masked_topk_tokens(dh, h, out_tokens=tok, out_max=mx, workspace=ws)
+        assert m.mtp_read_device_error(ws) == 0, f"argmax call {i}"
+        assert torch.equal(tok, first_tok) and torch.equal(mx, first_max), f"argmax call {i}"
+        m.mtp_masked_scatter_logits(dh, h, out=sc, workspace=ws)
+        assert m.mtp_read_device_error(ws) == 0, f"scatter call {i}"
+        assert torch.equal(sc, first_sc), f"scatter call {i}"
+
+
+@pytest.mark.parametrize("name,B,calls", [("uniform", 64, 120), ("shared", 256, 40)])
+def test_scatter_calls_with_profiling_events(build_lib, name, B, calls):
+    """The bench's per-kernel breakdown loop: consecutive scatter calls with the library
+    recording events around every kernel.  Each call must finish without any wait giving
+    up (the workspace records which wait and where if one does) and well under a second."""
+    m = build_lib
+    oh, dh = device_head(m, name)
+    t = helpers.tables(name)
+    hidden = synth.hidden_batch(name, B, None, t.prototypes, row0=5000)
+    h = helpers.bf16_tensor(hidden)
+    ws = dh.workspace(B)
+    out = torch.empty(B, oh.V, dtype=torch.float32, device="cuda")
+    first = m.mtp_masked_scatter_logits(dh, h, workspace=ws).clone()
+    kernels = ["projection", "topk", "gather_score", "fill"]
+    evs = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for k in kernels}
+    for a, b in evs.values():
+        a.record()
+        b.record()
+    call_s, call_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        for k in kernels:
+            m.mtp_profile_events(k, *evs[k])
+        for i in range(calls):
+            call_s.record()
+            m.mtp_masked_scatter_logits(dh, h, out=out, workspace=ws)
+            call_e.record()
+            word = m.mtp_read_device_error(ws)
+            ctrl = ws[:32].view(torch.int32).cpu().tolist()
+            assert word == 0, f"call {i}: error {word:#x}, wait site/cta/seq {ctrl[4:7]}"
+            assert call_s.elapsed_time(call_e) < 1000.0, f"call {i} took too long"
+            assert torch.equal(out, first), f"call {i}"
+    finally:
+        for k in kernels:
+            m.mtp_profile_events(k, None, None)
 
 
 def test_empty_batch_is_noop(build_lib):
