@@ -201,6 +201,9 @@ struct GatherParams {
     int chunk;                      // ordered positions per work item
     int ring;                       // embedding-row slots per CTA
     int row_group;                  // hidden rows per h buffer
+    int step;                       // slots the producer warp publishes per batch (<= 32, <= ring)
+    int consumer_warps;             // 8 or 16
+    int ctas_per_sm;                // gather CTAs per SM (1 or 2)
 };
 
 }  // namespace mtp

@@ -10,7 +10,7 @@
 // a multiple of 16, at most 256), so every table byte is read from HBM once
 // and the batch operand is reused out of shared memory.
 //
-// One CTA per SM, six warps:
+// Six warps per CTA (the persistent dense head runs one CTA per SM):
 //   warp 4  one thread issues TMA loads of 128x64 table tiles and Nx64 batch
 //           tiles (128-byte swizzle) into a ring of shared-memory stages;
 //   warp 5  one thread issues tcgen05.mma (kind::f16, fp32 accumulate) into a
@@ -98,7 +98,7 @@ __device__ __forceinline__ void report_timeout(const TcParams &p)
     if (p.err) atomicOr(p.err, MTP_DEVERR_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads)
     k_tc_gemm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
               const TcParams p)
 {
@@ -402,6 +402,16 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     const size_t budget = 220 * 1024 - 1024 - 256;
     int stages = (int)(budget / stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
+    if (p.splits > 1) {
+        // one unit per CTA: enough stages for its k-blocks and for the partial tile that the
+        // cluster reduction parks in the ring; less shared memory lets several CTAs share an
+        // SM, so every cluster of the grid is resident at once
+        const size_t red = (size_t)p.n_pad * kTileM * 4;
+        int need = p.kb_per_split;
+        while ((size_t)need * stage_bytes < red) ++need;
+        if (need < 2) need = 2;
+        if (need < stages) stages = need;
+    }
     if (stages < 2) return cudaErrorInvalidValue;
     p.stages = stages;
     p.out = a.out;
@@ -415,6 +425,8 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     p.zero = a.zero;
     p.zero_words = a.zero ? a.zero_words : 0;
     p.cluster_reduce = p.splits > 1;
+    if (p.cluster_reduce && (size_t)stages * stage_bytes < (size_t)p.n_pad * kTileM * 4)
+        return cudaErrorInvalidValue;
     if (p.cluster_reduce && (p.keys || p.splits > 8 || p.units > 65535)) return cudaErrorInvalidValue;
 
     alignas(64) CUtensorMap map_a;

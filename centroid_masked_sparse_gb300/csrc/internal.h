@@ -47,7 +47,7 @@ constexpr int kTopkThreads = 256;
 cudaError_t launch_projection(const ProjParams &p, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
 // Gather-score kernel (score.cu): ring/row-group geometry, its shared memory, launch.
-void gather_geometry(int H, int B, int *ring, int *row_group);
+void gather_geometry(GatherParams &p);
 size_t gather_smem_bytes(const GatherParams &p);
 cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s);
 cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s);

@@ -249,16 +249,17 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
     return cuda_status(launch_topk(tp, s));
 }
 
-// Positions per work item: about 16 items per SM (one gather CTA per SM takes
-// items from a shared counter), between 8 and 64 positions (the producer warp
-// covers an item with at most two tokens per lane).
+// Positions per work item.  Small batches: few positions in all, so each gather
+// CTA should get about one item (a CTA's producer walks its items one after the
+// other, each paying a few dependent global loads); large batches: up to 64
+// positions, which still leaves ~16 items per SM for the dynamic hand-out.
 int choose_chunk(const mtp_head_desc *d, int B)
 {
     const double avg = (double)d->vocab_size / d->num_centroids;
     const double est = (double)B * d->top_k * avg;
-    const double target = est / (16.0 * sm_count());
+    const double per_cta = est / sm_count();
     int ch = kMinChunk;
-    while (ch < kMaxChunk && 2.0 * ch <= target) ch *= 2;
+    while (ch < kMaxChunk && ch < per_cta) ch *= 2;
     return ch;
 }
 
@@ -302,7 +303,7 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     gp.W = L.W;
     gp.C = d->num_centroids;
     gp.chunk = chunk;
-    gather_geometry(gp.H, B, &gp.ring, &gp.row_group);
+    gather_geometry(gp);
     Prof pr(MTP_KERNEL_GATHER_SCORE, s);
     return cuda_status(launch_gather(gp, out_logits != nullptr, s));
 }

@@ -21,7 +21,7 @@
 //     h buffers and every candidate's embedding row (3 KB at H=1536) into a
 //     ring of ~50 shared-memory slots, one lane per slot, each completing on
 //     its own mbarrier, with an evict-first L2 policy (rows are read once);
-//   - sixteen consumer warps (eight when H > 2048) take slots in turn, dot the
+//   - sixteen consumer warps (eight when H > 3072) take slots in turn, dot the
 //     row against the item's hidden rows out of shared memory (16-byte lanes,
 //     f32 FMAs fed with bf16 halves, a butterfly of shuffles per dot), then
 //     either store the logit into the full-vocabulary row or keep the best
@@ -50,7 +50,6 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kMaxConsumerWarps = 16;
 constexpr int kHBuffers = 4;
 constexpr int kMaxRowGroup = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -164,8 +163,10 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
     const uint32_t rb = (uint32_t)p.H * 2;
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
     const uint64_t pol = l2_policy_evict_first();
-    const int step = min(kWarp, p.ring);
+    const int step = p.step;
+    const uint32_t ring = (uint32_t)p.ring;
     uint32_t seq = 0, huse = 0;
+    uint32_t seq_slot = 0, seq_par = 0;   // slot and phase parity of sequence number `seq`
     ItemMeta nxt;
     load_item(p, grab_item(p, lane), n_items, lane, nxt);
     for (;;) {
@@ -223,8 +224,11 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
                         tok = -1;
                     }
                     const uint32_t sq = seq + (uint32_t)q;
-                    const uint32_t slot = sq % (uint32_t)p.ring;
-                    const uint32_t par = (sq / (uint32_t)p.ring) & 1u;
+                    uint32_t slot = seq_slot + (uint32_t)q, par = seq_par;
+                    while (slot >= ring) {   // q < 64: at most a couple of wraps
+                        slot -= ring;
+                        par ^= 1u;
+                    }
                     lok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, kWaitNs);
                     if (!lok) record_timeout(p, kSiteProducerEmpty, sq);
                     if (lok) {
@@ -243,14 +247,22 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
                 if (__any_sync(0xffffffffu, !lok)) return false;
             }
             seq += (uint32_t)cur.nvalid;
+            seq_slot += (uint32_t)cur.nvalid;
+            while (seq_slot >= ring) {
+                seq_slot -= ring;
+                seq_par ^= 1u;
+            }
         }
     }
     // one end-of-stream marker per consumer warp
     bool ok = true;
     if (lane < consumers) {
         const uint32_t sq = seq + (uint32_t)lane;
-        const uint32_t slot = sq % (uint32_t)p.ring;
-        const uint32_t par = (sq / (uint32_t)p.ring) & 1u;
+        uint32_t slot = seq_slot + (uint32_t)lane, par = seq_par;
+        while (slot >= ring) {
+            slot -= ring;
+            par ^= 1u;
+        }
         ok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, kWaitNs);
         if (!ok) record_timeout(p, kSiteProducerDone, sq);
         if (ok) {
@@ -273,10 +285,15 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
     unsigned long long best = 0ull;     // lane r: best key of row best_row of that use
     int best_row = 0;
     bool ok = true;
-    for (uint32_t k = 0;; ++k) {
+    // this warp's sequence numbers are warp, warp + NW, ...; with the ring a multiple of
+    // NW its slots are warp, warp + NW, ... < ring, then the same slots one phase later
+    uint32_t slot = (uint32_t)warp, par = 0u;
+    for (uint32_t k = 0;; ++k, slot += NW) {
+        if (slot >= (uint32_t)p.ring) {
+            slot -= (uint32_t)p.ring;
+            par ^= 1u;
+        }
         const uint32_t seq = (uint32_t)warp + k * NW;
-        const uint32_t slot = seq % (uint32_t)p.ring;
-        const uint32_t par = (seq / (uint32_t)p.ring) & 1u;
         if (!mbar_wait(sm.full0 + 8u * slot, par, kWaitNs)) {
             if (lane == 0) record_timeout(p, kSiteConsumerFull, seq);
             ok = false;
@@ -313,13 +330,20 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
             for (int r = 0; r < gr; ++r) {
                 const uint4 *hrow =
                     reinterpret_cast<const uint4 *>(sm.hbuf + ((size_t)hb * p.row_group + r) * rb);
-                float acc = 0.f;
+                // four independent chains (one per 32-bit word of a 16-byte group)
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     const int idx = c * kWarp + lane;
-                    if (idx < hv) acc = dot8_bf16_mixed(e[c], hrow[idx], acc);
+                    if (idx < hv) {
+                        const uint4 x = hrow[idx];
+                        a0 = fma2_bf16(e[c].x, x.x, a0);
+                        a1 = fma2_bf16(e[c].y, x.y, a1);
+                        a2 = fma2_bf16(e[c].z, x.z, a2);
+                        a3 = fma2_bf16(e[c].w, x.w, a3);
+                    }
                 }
-                acc = warp_sum(acc);
+                const float acc = warp_sum((a0 + a1) + (a2 + a3));
                 if (lane == r) {
                     const int row = hm.rows[r];
                     if (SCATTER) {
@@ -354,7 +378,7 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
 }
 
 template <int NCH, bool SCATTER, int NW>
-__global__ void __launch_bounds__((NW + 1) * kWarp, 1) k_gather_score(const GatherParams p)
+__global__ void __launch_bounds__((NW + 1) * kWarp, NW == 16 ? 1 : 2) k_gather_score(const GatherParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_last;
@@ -362,7 +386,7 @@ __global__ void __launch_bounds__((NW + 1) * kWarp, 1) k_gather_score(const Gath
     const Smem sm = carve(smem, p);
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x & (kWarp - 1);
 
-    if (p.ring % NW != 0) {
+    if (p.ring % NW != 0 || p.consumer_warps != NW || p.step > p.ring || p.step > kWarp) {
         // a slot shared by two consumer warps could be waited one phase early: refuse
         if (threadIdx.x == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TIMEOUT);
         return;
@@ -415,23 +439,22 @@ __global__ void __launch_bounds__((NW + 1) * kWarp, 1) k_gather_score(const Gath
     }
 }
 
-// 16 consumer warps while the row registers allow it (H <= 2048), else 8.
-template <int NCH>
-constexpr int consumer_warps()
+template <int NCH, bool SCATTER, int NW>
+cudaError_t run_gather_nw(const GatherParams &p, cudaStream_t s)
 {
-    return NCH <= 8 ? 16 : 8;  // keep in step with gather_consumer_warps()
+    const void *fn = (const void *)k_gather_score<NCH, SCATTER, NW>;
+    const size_t smem = gather_smem_bytes(p);
+    cudaError_t e = allow_smem(fn, smem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(k_gather_score<NCH, SCATTER, NW>, dim3(sm_count() * p.ctas_per_sm),
+                            dim3((NW + 1) * kWarp), smem, s, p);
 }
 
 template <int NCH, bool SCATTER>
 cudaError_t run_gather(const GatherParams &p, cudaStream_t s)
 {
-    constexpr int NW = consumer_warps<NCH>();
-    const void *fn = (const void *)k_gather_score<NCH, SCATTER, NW>;
-    const size_t smem = gather_smem_bytes(p);
-    cudaError_t e = allow_smem(fn, smem);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(k_gather_score<NCH, SCATTER, NW>, dim3(sm_count()), dim3((NW + 1) * kWarp),
-                            smem, s, p);
+    if (p.consumer_warps == 16 && NCH <= 12) return run_gather_nw<NCH, SCATTER, (NCH <= 12 ? 16 : 8)>(p, s);
+    return run_gather_nw<NCH, SCATTER, 8>(p, s);
 }
 
 template <bool SCATTER>
@@ -462,32 +485,29 @@ size_t gather_smem_bytes(const GatherParams &p)
            kHBuffers * sizeof(HMeta) + (size_t)p.B * 12;
 }
 
-// Consumer warps of the gather kernel for rows of H elements.
-static int gather_consumer_warps(int H)
+// Geometry of the gather kernel for p.H and p.B: consumer warps, CTAs per SM,
+// ring slots, hidden rows per h buffer and the producer's batch width.  The ring
+// is a multiple of the consumer warp count, so each slot always belongs to the
+// same warp (see the kernel's comment on barrier phases).
+void gather_geometry(GatherParams &p)
 {
-    const int nch = chunks_for_hidden(H);
-    return nch <= 8 ? 16 : 8;
-}
-
-// Ring slots and hidden rows per h buffer for a given H and batch, within the
-// shared-memory budget of one CTA per SM.  The ring is a multiple of the
-// consumer warp count, so each slot always belongs to the same warp (see the
-// kernel's comment on barrier phases).
-void gather_geometry(int H, int B, int *ring, int *row_group)
-{
-    const size_t rb = (size_t)H * 2;
+    const size_t rb = (size_t)p.H * 2;
+    const int nch = chunks_for_hidden(p.H);
+    p.consumer_warps = nch <= 12 ? 16 : 8;
+    p.ctas_per_sm = 1;
     int rg = (int)(16384 / rb);
     rg = rg < 1 ? 1 : (rg > kMaxRowGroup ? kMaxRowGroup : rg);
-    if (rg > B) rg = B;
-    const size_t budget = 212 * 1024;
-    const size_t fixed = (size_t)kHBuffers * rg * rb + kHBuffers * (sizeof(HMeta) + 16) + (size_t)B * 12 + 64;
-    long long r = (long long)((budget - fixed) / (rb + 16 + sizeof(SlotMeta)));
-    const int nw = gather_consumer_warps(H);
+    if (rg > p.B) rg = p.B;
+    p.row_group = rg;
+    const size_t budget = (size_t)(212 * 1024) / (size_t)p.ctas_per_sm;
+    const size_t fixed = (size_t)kHBuffers * rg * rb + kHBuffers * (sizeof(HMeta) + 16) + (size_t)p.B * 12 + 64;
+    long long r = fixed < budget ? (long long)((budget - fixed) / (rb + 16 + sizeof(SlotMeta))) : 0;
+    const int nw = p.consumer_warps;
     if (r > 256) r = 256;
     r = r / nw * nw;
     if (r < nw) r = nw;
-    *ring = (int)r;
-    *row_group = rg;
+    p.ring = (int)r;
+    p.step = p.ring < kWarp ? p.ring : kWarp;
 }
 
 cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s)
