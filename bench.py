@@ -366,6 +366,20 @@ def gpu_main(args):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:  # noqa: BLE001
         uuid = None
+    if args.finish != "argmax":
+        # profiling aid: one finish only, a short line with its timing (not the headline)
+        if args.finish == "dense":
+            r = measure_dense(ctx, t, dh, B, args.steps, args.warmup)
+            print(json.dumps({"finish": "dense", "workload": workload_label(w, B),
+                              "us_per_call": round(r["call_ms"] * 1e3, 2),
+                              "kernel_us": round(r["kernel_ms"] * 1e3, 2),
+                              "gbs": round(r["bytes"] / (r["kernel_ms"] * 1e-3) / 1e9, 1)}))
+        else:
+            r = measure_masked(ctx, t, dh, name, B, args.steps, args.warmup, scatter=True)
+            print(json.dumps({"finish": "scatter", "workload": workload_label(w, B),
+                              "us_per_call": round(r["call_ms"] * 1e3, 2),
+                              "kernels_us": r["kernels_us"], "device_error": r["device_error"]}))
+        return
     sampler = ClockSampler(uuid) if rank == 0 else None
     res = measure_masked(ctx, t, dh, name, B, args.steps, args.warmup, row0=rank * 100000)
     clocks = sampler.stop(res["t0"], res["t1"]) if sampler else None
@@ -506,7 +520,7 @@ def reference_main(args):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="uniform")
@@ -514,6 +528,8 @@ def parse():
     ap.add_argument("--quick", action="store_true", help="headline line only")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--finish", default="argmax", choices=["argmax", "scatter", "dense"],
+                    help="profiling aid: time only this finish on the workload's tables")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     return a
