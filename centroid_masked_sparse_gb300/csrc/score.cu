@@ -15,13 +15,13 @@
 // chose its cluster.
 //
 // The kernel is a producer/consumer pipeline, one CTA per SM:
-//   - one producer warp takes work items from a global counter (prefetching
-//     the next item's metadata while it issues the current one), bulk-copies
+//   - one producer warp walks this CTA's share of the work items (records and
+//     metadata prefetched two and one items ahead), bulk-copies
 //     (cp.async.bulk, the TMA engine) the item's hidden rows into one of four
 //     h buffers and every candidate's embedding row (3 KB at H=1536) into a
 //     ring of ~50 shared-memory slots, one lane per slot, each completing on
 //     its own mbarrier, with an evict-first L2 policy (rows are read once);
-//   - sixteen consumer warps (eight when H > 3072) take slots in turn, dot the
+//   - 24 consumer warps (16 for H up to 3072, else 8) take slots in turn, dot the
 //     row against the item's hidden rows out of shared memory (16-byte lanes,
 //     f32 FMAs fed with bf16 halves, a butterfly of shuffles per dot), then
 //     either store the logit into the full-vocabulary row or keep the best
@@ -120,27 +120,20 @@ struct ItemMeta {
     uint32_t mask;  // row-mask word `lane` of the cluster (lane < W)
 };
 
-__device__ __forceinline__ int grab_item(const GatherParams &p, int lane)
-{
-    int v = 0;
-    if (lane == 0) v = (int)atomicAdd(p.ctrl + kCtrlNext, 1u);
-    return __shfl_sync(0xffffffffu, v, 0);
-}
-
-// Issue the loads of an item's metadata; the values are first used one item later,
-// so their latency overlaps the current item's copies.
-__device__ __forceinline__ void load_item(const GatherParams &p, int it, int n_items, int lane,
+// Metadata of an item whose record (cluster, first position) is already in
+// registers: the loads issued here are first used one item later, so their
+// latency overlaps the current item's copies.
+__device__ __forceinline__ void load_item(const GatherParams &p, int2 item, bool valid, int lane,
                                           ItemMeta &m)
 {
-    m.valid = it < n_items;
+    m.valid = valid;
     m.c = -1;
     m.p0 = 0;
     m.nvalid = 0;
     m.tok0 = -1;
     m.tok1 = -1;
     m.mask = 0u;
-    if (!m.valid) return;
-    const int2 item = p.items[it];
+    if (!valid) return;
     int lo = 0, hi = 0;
     if ((unsigned)item.x < (unsigned)p.C && item.y >= 0)
         cluster_range(p.offsets, p.V, p.S, item.x, &lo, &hi, nullptr);
@@ -155,9 +148,12 @@ __device__ __forceinline__ void load_item(const GatherParams &p, int it, int n_i
     if (lane < p.W) m.mask = __ldcg(p.rowmask + (size_t)item.x * p.W + lane);
 }
 
-// Producer warp: takes items from the global counter and publishes, per row group,
-// the hidden rows into an h buffer and one ring slot per candidate position (each
-// lane issues its own slot's bulk copy).  False after a timed-out wait.
+// Producer warp: walks the items of this CTA (CTA j takes items j, j + G, j + 2G, ...
+// for a grid of G CTAs; items are chunks of randomly chosen clusters, so the
+// interleaved split is balanced and needs no atomic hand-out) and publishes, per
+// row group, the hidden rows into an h buffer and one ring slot per candidate
+// position (each lane issues its own slot's bulk copy).  The item records and
+// their metadata are loaded two and one items ahead.  False after a timed-out wait.
 __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int consumers)
 {
     const uint32_t rb = (uint32_t)p.H * 2;
@@ -167,12 +163,18 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
     const uint32_t ring = (uint32_t)p.ring;
     uint32_t seq = 0, huse = 0;
     uint32_t seq_slot = 0, seq_par = 0;   // slot and phase parity of sequence number `seq`
+    const int G = (int)gridDim.x;
+    int it1 = (int)blockIdx.x, it2 = it1 + G;
+    const int2 invalid_item = make_int2(-1, 0);
     ItemMeta nxt;
-    load_item(p, grab_item(p, lane), n_items, lane, nxt);
+    load_item(p, it1 < n_items ? p.items[it1] : invalid_item, it1 < n_items, lane, nxt);
+    int2 rec2 = it2 < n_items ? p.items[it2] : invalid_item;   // record of the item after next
     for (;;) {
         const ItemMeta cur = nxt;
         if (!cur.valid) break;
-        load_item(p, grab_item(p, lane), n_items, lane, nxt);
+        load_item(p, rec2, it2 < n_items, lane, nxt);
+        it2 += G;
+        rec2 = it2 < n_items ? p.items[it2] : invalid_item;
         if (cur.nvalid == 0) continue;
         // the bucket's batch rows, in row order
         const int cnt = __popc(cur.mask);
@@ -274,7 +276,7 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
     return !__any_sync(0xffffffffu, !ok);
 }
 
-template <int NCH, bool SCATTER, int NW>
+template <int NCH, bool SCATTER, int NW, bool FULL>
 __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lane)
 {
     const uint32_t rb = (uint32_t)p.H * 2;
@@ -309,6 +311,20 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
             best = 0ull;
             best_use = m.use;
         }
+        // Take the candidate row into registers and hand the slot straight back to the
+        // producer: the ring then holds copies in flight, not rows waiting for arithmetic.
+        uint4 e[NCH];
+        if (m.tok >= 0) {
+            const uint4 *erow = reinterpret_cast<const uint4 *>(sm.ring + (size_t)slot * rb);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                const int idx = c * kWarp + lane;
+                e[c] = (FULL || idx < hv) ? erow[idx] : zero;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty0 + 8u * slot);
         if (m.tok >= 0) {
             if (m.use != ready_use) {
                 if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, kWaitNs)) {
@@ -317,13 +333,6 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
                     break;
                 }
                 ready_use = m.use;
-            }
-            const uint4 *erow = reinterpret_cast<const uint4 *>(sm.ring + (size_t)slot * rb);
-            uint4 e[NCH];
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                const int idx = c * kWarp + lane;
-                e[c] = idx < hv ? erow[idx] : zero;
             }
             const HMeta &hm = sm.hmeta[hb];
             const int gr = hm.gr;
@@ -335,7 +344,7 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     const int idx = c * kWarp + lane;
-                    if (idx < hv) {
+                    if (FULL || idx < hv) {
                         const uint4 x = hrow[idx];
                         a0 = fma2_bf16(e[c].x, x.x, a0);
                         a1 = fma2_bf16(e[c].y, x.y, a1);
@@ -356,20 +365,15 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
                 }
             }
         }
-        // release the slot (and, for the item's last slot, its h buffer)
-        fence_proxy_async_smem();
+        // for the item's last slot, release its h buffer once its hidden rows have landed
+        // (a skipped slot never waited for them)
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(sm.empty0 + 8u * slot);
-            if (atomicSub(&sm.hmeta[hb].left, 1) == 1) {
-                // the item's last slot: its hidden rows must have landed (a skipped slot never
-                // waited for them) before the producer may refill the buffer
-                if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, kWaitNs)) {
-                    record_timeout(p, kSiteConsumerLastHFull, m.use);
-                    ok = false;
-                }
-                mbar_arrive(sm.hempty0 + 8u * hb);
+        if (lane == 0 && atomicSub(&sm.hmeta[hb].left, 1) == 1) {
+            if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, kWaitNs)) {
+                record_timeout(p, kSiteConsumerLastHFull, m.use);
+                ok = false;
             }
+            mbar_arrive(sm.hempty0 + 8u * hb);
         }
         if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
     }
@@ -377,8 +381,8 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
     return ok;
 }
 
-template <int NCH, bool SCATTER, int NW>
-__global__ void __launch_bounds__((NW + 1) * kWarp, NW == 16 ? 1 : 2) k_gather_score(const GatherParams p)
+template <int NCH, bool SCATTER, int NW, bool FULL>
+__global__ void __launch_bounds__((NW + 1) * kWarp, NW >= 16 ? 1 : 2) k_gather_score(const GatherParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_last;
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__((NW + 1) * kWarp, NW == 16 ? 1 : 2) k_gather_s
     if (warp == NW) {
         ok = produce(p, sm, lane, NW);
     } else {
-        ok = consume<NCH, SCATTER, NW>(p, sm, warp, lane);
+        ok = consume<NCH, SCATTER, NW, FULL>(p, sm, warp, lane);
     }
     if (!ok && lane == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TIMEOUT);
     __syncthreads();
@@ -439,22 +443,27 @@ __global__ void __launch_bounds__((NW + 1) * kWarp, NW == 16 ? 1 : 2) k_gather_s
     }
 }
 
-template <int NCH, bool SCATTER, int NW>
+template <int NCH, bool SCATTER, int NW, bool FULL>
 cudaError_t run_gather_nw(const GatherParams &p, cudaStream_t s)
 {
-    const void *fn = (const void *)k_gather_score<NCH, SCATTER, NW>;
+    const void *fn = (const void *)k_gather_score<NCH, SCATTER, NW, FULL>;
     const size_t smem = gather_smem_bytes(p);
     cudaError_t e = allow_smem(fn, smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_gather_score<NCH, SCATTER, NW>, dim3(sm_count() * p.ctas_per_sm),
+    return launch_dependent(k_gather_score<NCH, SCATTER, NW, FULL>, dim3(sm_count() * p.ctas_per_sm),
                             dim3((NW + 1) * kWarp), smem, s, p);
 }
 
+// Consumer warps: 24 while the row registers allow it (H <= 2048), 16 up to H = 3072,
+// else 8; FULL when H is a whole number of 256-element chunks (no tail lanes).
 template <int NCH, bool SCATTER>
 cudaError_t run_gather(const GatherParams &p, cudaStream_t s)
 {
-    if (p.consumer_warps == 16 && NCH <= 12) return run_gather_nw<NCH, SCATTER, (NCH <= 12 ? 16 : 8)>(p, s);
-    return run_gather_nw<NCH, SCATTER, 8>(p, s);
+    const bool full = p.H == NCH * 256;
+    constexpr int NW = NCH <= 8 ? 24 : (NCH <= 12 ? 16 : 8);
+    if (p.consumer_warps == NW)
+        return full ? run_gather_nw<NCH, SCATTER, NW, true>(p, s) : run_gather_nw<NCH, SCATTER, NW, false>(p, s);
+    return cudaErrorInvalidValue;
 }
 
 template <bool SCATTER>
@@ -493,7 +502,7 @@ void gather_geometry(GatherParams &p)
 {
     const size_t rb = (size_t)p.H * 2;
     const int nch = chunks_for_hidden(p.H);
-    p.consumer_warps = nch <= 12 ? 16 : 8;
+    p.consumer_warps = nch <= 8 ? 24 : (nch <= 12 ? 16 : 8);
     p.ctas_per_sm = 1;
     int rg = (int)(16384 / rb);
     rg = rg < 1 ? 1 : (rg > kMaxRowGroup ? kMaxRowGroup : rg);
