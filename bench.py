@@ -361,6 +361,8 @@ def gpu_main(args):
     t = synth.make_tables(name)
     dh = m.MaskedHead.from_host(t.centroid_w, t.embed_w, t.token_ordering, t.cluster_offsets,
                                 w.top_k, device=device)
+    if args.ordered:
+        dh.use_ordered_table()
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
@@ -399,6 +401,7 @@ def gpu_main(args):
            "us_per_call": round(call_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": {"workload": workload_label(w, B), "finish": "sparse argmax",
+                      "embedding_layout": "cluster-ordered copy" if args.ordered else "token order",
                       "batch_per_gpu": B, "parallelism": "replicas" if ws > 1 else "single",
                       "l2": "flushed before every timed call (256 MB write, outside the events)"},
            "call_roofline": {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
@@ -446,15 +449,22 @@ def other_workloads(ctx, args, hbm):
     m, synth, torch = ctx["m"], ctx["synth"], ctx["torch"]
     res = {}
     steps = max(10, args.steps // 8)
-    for name, scatter in (("scatter", True), ("variable", False), ("shared", False), ("shared", True)):
+    cases = (("scatter", True, False), ("variable", False, False), ("shared", False, False),
+             ("shared", True, False), ("uniform", False, True), ("variable", False, True),
+             ("shared", False, True), ("shared", True, True))
+    for name, scatter, ordered in cases:
         w = synth.WORKLOADS[name]
         t = synth.make_tables(name)
         dh = m.MaskedHead.from_host(t.centroid_w, t.embed_w, t.token_ordering, t.cluster_offsets,
                                     w.top_k, device=ctx["device"])
+        if ordered:
+            dh.use_ordered_table()
         r = measure_masked(ctx, t, dh, name, w.batch, steps, args.warmup, scatter=scatter)
         cg = r["bytes"]["call"] / (r["call_ms"] * 1e-3) / 1e9
         ga = r["bytes"]["gather"] / (r["kernel_ms"] * 1e-3) / 1e9
         key = f"{name}_{'scatter' if scatter else 'argmax'}_b{w.batch}"
+        if ordered:
+            key += "_ordered_table"
         res[key] = {"workload": workload_label(w, w.batch),
                     "us_per_call": round(r["call_ms"] * 1e3, 2),
                     "tokens_per_s": round(w.batch / (r["call_ms"] * 1e-3), 1),
@@ -507,6 +517,7 @@ def reference_main(args):
            "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": workload_label(w, B), "finish": "sparse argmax",
+                      "embedding_layout": "cluster-ordered copy" if args.ordered else "token order",
                       "batch_per_gpu": B},
            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads,
                             "kind": "oracle",
@@ -528,6 +539,8 @@ def parse():
     ap.add_argument("--quick", action="store_true", help="headline line only")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ordered", action="store_true",
+                    help="attach the cluster-ordered embedding copy (built once, outside the timing)")
     ap.add_argument("--finish", default="argmax", choices=["argmax", "scatter", "dense"],
                     help="profiling aid: time only this finish on the workload's tables")
     a = ap.parse_args()

@@ -142,6 +142,7 @@ mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool o
     if (embed) {
         if (d->ld_embed < d->hidden_size) return MTP_ERR_SHAPE;
         if (d->ld_embed % 8 != 0 || !aligned16(d->embed_w)) return MTP_ERR_ALIGN;
+        if (!aligned16(d->embed_ordered)) return MTP_ERR_ALIGN;
     }
     if (centroids) {
         if (d->num_centroids < 1 || d->top_k < 1 || d->top_k > d->num_centroids) return MTP_ERR_SHAPE;
@@ -278,13 +279,16 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
         st = cuda_status(launch_fill_neg_inf(out_logits, (size_t)B * d->vocab_size, s));
         if (st != MTP_OK) return st;
     }
-    const int chunk = choose_chunk(d, B);
+    // large buckets (many rows per selected cluster) go to the tensor-core gather
+    const bool tc_gather = (long long)B * d->top_k >= (long long)kTcGatherMinReuse * d->num_centroids;
+    const int chunk = tc_gather ? kTcGatherChunk : choose_chunk(d, B);
     st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s);
     if (st != MTP_OK) return st;
 
     GatherParams gp{};
     gp.hidden = (const uint16_t *)hidden;
     gp.embed = (const uint16_t *)d->embed_w;
+    gp.embed_ordered = (const uint16_t *)d->embed_ordered;
     gp.ld = d->ld_embed;
     gp.ordering = d->token_ordering;
     gp.offsets = d->cluster_offsets;
@@ -303,8 +307,9 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     gp.W = L.W;
     gp.C = d->num_centroids;
     gp.chunk = chunk;
-    gather_geometry(gp);
     Prof pr(MTP_KERNEL_GATHER_SCORE, s);
+    if (tc_gather) return cuda_status(launch_gather_tc(gp, out_logits != nullptr, s));
+    gather_geometry(gp);
     return cuda_status(launch_gather(gp, out_logits != nullptr, s));
 }
 
@@ -408,6 +413,23 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
     g.out_max = out_max;
     Prof pr(MTP_KERNEL_DENSE, s);
     return cuda_status(launch_tc_gemm(g, s));
+}
+
+mtp_status mtp_reorder_embeddings(const mtp_head_desc *desc, void *embed_ordered_out, void *workspace,
+                                  void *stream)
+{
+    mtp_status st = check_desc(desc, false, true, false);
+    if (st != MTP_OK) return st;
+    if (!desc->token_ordering || !embed_ordered_out) return MTP_ERR_NULL;
+    if (!aligned16(embed_ordered_out) || !aligned16(workspace)) return MTP_ERR_ALIGN;
+    const char *src = (const char *)desc->embed_w, *dst = (const char *)embed_ordered_out;
+    const size_t bytes = (size_t)desc->vocab_size * desc->ld_embed * 2;
+    if (src < dst + bytes && dst < src + bytes) return MTP_ERR_SHAPE;   // overlapping tables
+    st = use_device(desc->device);
+    if (st != MTP_OK) return st;
+    return cuda_status(launch_reorder_rows((const uint16_t *)desc->embed_w, desc->ld_embed, desc->token_ordering,
+                                           desc->vocab_size, desc->hidden_size, (uint16_t *)embed_ordered_out,
+                                           (uint32_t *)workspace, (cudaStream_t)stream));
 }
 
 mtp_status mtp_read_device_error(const void *workspace, uint32_t *host_word, void *stream)

@@ -99,7 +99,14 @@ typedef enum mtp_status {
  *                    for that id unspecified)
  *   cluster_offsets  int32 [C+1] ascending, off[0] = 0, off[C] = V: centroid c owns
  *                    positions [off[c], off[c+1]); empty clusters are allowed.  NULL
- *                    means uniform clusters of V/C positions (the page's layout). */
+ *                    means uniform clusters of V/C positions (the page's layout).
+ *   embed_ordered    optional bf16 [V, ld_embed], 16-byte aligned: the embedding rows in
+ *                    ordered-position order, row p = embed_w row token_ordering[p] (see
+ *                    mtp_reorder_embeddings).  When set, the masked calls read every
+ *                    selected cluster's candidate rows as one contiguous block instead of
+ *                    gathering them row by row; results are identical either way.  NULL:
+ *                    gather from embed_w (the page's layout).  It must match embed_w and
+ *                    token_ordering; the library does not check that. */
 typedef struct mtp_head_desc {
     int32_t vocab_size;
     int32_t hidden_size;
@@ -112,6 +119,7 @@ typedef struct mtp_head_desc {
     int64_t ld_embed;
     const int32_t *token_ordering;
     const int32_t *cluster_offsets;
+    const void *embed_ordered;
 } mtp_head_desc;
 
 /* Bytes of device workspace that the masked calls and the dense head's argmax
@@ -184,6 +192,19 @@ MTP_API mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidd
 MTP_API mtp_status mtp_masked_topk_tokens_noalloc(const mtp_head_desc *desc, const void *hidden,
                                                   int32_t batch, int32_t *out_tokens,
                                                   float *out_max, void *stream);
+
+/* Build the cluster-ordered embedding table: row p of embed_ordered_out = row
+ * token_ordering[p] of desc->embed_w, for p < V (first H elements of each row;
+ * the row stride of the output is desc->ld_embed).  A one-time layout step
+ * (V * H * 2 bytes read and written); the result may then be passed as
+ * desc->embed_ordered.  The page gathers from the token-order table on every
+ * call; the ordered copy turns that gather into contiguous reads per cluster.
+ *   embed_ordered_out  bf16 [V, ld_embed] device buffer, 16-byte aligned, not
+ *                      overlapping embed_w
+ * Token ids outside [0, V) are skipped (their rows are left unwritten) and set
+ * MTP_DEVERR_TOKEN_RANGE in *workspace's error word if workspace is non-NULL. */
+MTP_API mtp_status mtp_reorder_embeddings(const mtp_head_desc *desc, void *embed_ordered_out,
+                                          void *workspace, void *stream);
 
 /* Enqueue an asynchronous copy of the workspace's device error word (a set of
  * MTP_DEVERR_* bits, reset by each masked call) into *host_word; the value is

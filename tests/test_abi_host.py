@@ -119,3 +119,24 @@ def test_dense_and_scores_reject_bad_arguments(L):
     assert L.mtp_read_device_error(None, None, None) == -1
     assert L.mtp_profile_events(7, None, None) == -2
     assert L.mtp_profile_events(0, None, None) == 0
+
+
+def test_ordered_table_checks(L):
+    # the optional cluster-ordered table must be 16-byte aligned like the embedding table
+    d = _desc()
+    d.embed_ordered = 0xA004
+    out = ctypes.c_void_p(0x8000)
+    assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 1 << 30, None) == -3
+    # building it: null, misaligned and overlapping tables are refused before any launch
+    d = _desc(V=1024, H=64, ew=0x100000)
+    assert L.mtp_reorder_embeddings(ctypes.byref(d), None, None, None) == -1
+    assert L.mtp_reorder_embeddings(None, ctypes.c_void_p(0x800000), None, None) == -1
+    assert L.mtp_reorder_embeddings(ctypes.byref(_desc(V=1024, H=64, ordering=None)),
+                                    ctypes.c_void_p(0x800000), None, None) == -1
+    assert L.mtp_reorder_embeddings(ctypes.byref(d), ctypes.c_void_p(0x800008), None, None) == -3
+    assert L.mtp_reorder_embeddings(ctypes.byref(d), ctypes.c_void_p(0x800000),
+                                    ctypes.c_void_p(0x9004), None) == -3
+    # [V, H] bf16 at 0x100000 spans 128 KiB: an output inside that range overlaps it
+    assert L.mtp_reorder_embeddings(ctypes.byref(d), ctypes.c_void_p(0x110000), None, None) == -2
+    assert L.mtp_reorder_embeddings(ctypes.byref(_desc(V=1024, H=12, ew=0x100000)),
+                                    ctypes.c_void_p(0x800000), None, None) == -2

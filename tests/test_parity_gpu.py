@@ -268,22 +268,33 @@ def test_hidden_sizes(build_lib, H):
     _full_check(m, oh, dh, hidden, f"H={H}")
 
 
-def test_variable_clusters_empty_and_oversized(build_lib):
+@pytest.mark.parametrize("H", [72, 264, 1536])
+def test_hidden_sizes_tensor_core_gather(build_lib, H):
+    """B*K >= 4C: large buckets, gathered onto the tensor cores (K tails at 72, 264)."""
+    m = build_lib
+    t, oh, dh = _custom(m, 4096, H, 32, 8, seed=H + 5)
+    hidden = synth.random_hidden(64, H, H + 6)
+    _full_check(m, oh, dh, hidden, f"tc H={H}")
+
+
+@pytest.mark.parametrize("B", [9, 41])
+def test_variable_clusters_empty_and_oversized(build_lib, B):
     m = build_lib
     sizes = [0] * 5 + [1, 2, 3] + [700, 1] + [37] * 20 + [0, 19]
     V = int(sum(sizes))
     t, oh, dh = _custom(m, V, 64, len(sizes), 6, seed=77, sizes=sizes)
-    hidden = synth.random_hidden(9, 64, 78)
-    assert (9 * V) % 4 != 0  # the -inf fill ends in a scalar tail
-    _full_check(m, oh, dh, hidden, "ragged clusters")
+    hidden = synth.random_hidden(B, 64, 78)
+    assert (B * V) % 4 != 0  # the -inf fill ends in a scalar tail
+    _full_check(m, oh, dh, hidden, f"ragged clusters B={B}")
 
 
-def test_only_empty_clusters_selected(build_lib):
+@pytest.mark.parametrize("B", [2, 8])
+def test_only_empty_clusters_selected(build_lib, B):
     m = build_lib
     sizes = [0, 0, 10, 6]
     t, oh, dh = _custom(m, 16, 8, 4, 2, seed=3, sizes=sizes)
     # make the empty clusters win: their centroid rows point along the hidden state
-    hidden = synth.bf16_bits(np.ones((2, 8), np.float32))
+    hidden = synth.bf16_bits(np.ones((B, 8), np.float32))
     cw = np.zeros((4, 8), np.float32)
     cw[0] = 1.0
     cw[1] = 0.5
@@ -297,10 +308,10 @@ def test_only_empty_clusters_selected(build_lib):
     tok, mx = m.mtp_masked_topk_tokens(dh, h)
     sc = m.mtp_masked_scatter_logits(dh, h)
     torch.cuda.synchronize()
-    assert tok.cpu().tolist() == [-1, -1]
+    assert tok.cpu().tolist() == [-1] * B
     assert np.isneginf(mx.cpu().numpy()).all()
     assert np.isneginf(sc.cpu().numpy()).all()
-    assert oracle.masked_topk_tokens(oh, hidden)["tokens"].tolist() == [-1, -1]
+    assert oracle.masked_topk_tokens(oh, hidden)["tokens"].tolist() == [-1] * B
 
 
 def test_padded_table_and_identity_ordering(build_lib):
@@ -310,12 +321,14 @@ def test_padded_table_and_identity_ordering(build_lib):
     _full_check(m, oh, dh, hidden, "padded")
 
 
-def test_integer_inputs_bit_exact_with_ties(build_lib):
+@pytest.mark.parametrize("B,K", [(12, 3), (32, 8)])
+def test_integer_inputs_bit_exact_with_ties(build_lib, B, K):
     """Small-integer inputs make every sum exact in fp32 and fp64: logits must be
-    bit-identical, and forced ties exercise both tie-break rules."""
+    bit-identical, and forced ties exercise both tie-break rules.  B*K >= 4C sends
+    the second case through the tensor-core gather."""
     m = build_lib
     g = np.random.default_rng(11)
-    V, C, H, K, B = 512, 16, 64, 3, 12
+    V, C, H = 512, 16, 64
     cw = g.integers(-2, 3, size=(C, H)).astype(np.float32)
     cw[5] = cw[9]          # centroids 5 and 9 always tie
     ew = g.integers(-2, 3, size=(V, H)).astype(np.float32)
@@ -362,15 +375,16 @@ def test_all_equal_scores(build_lib, name):
     assert (mx.cpu().numpy() == 0).all()
 
 
-def test_corrupt_ordering_sets_device_error(build_lib):
+@pytest.mark.parametrize("B", [2, 8])
+def test_corrupt_ordering_sets_device_error(build_lib, B):
     m = build_lib
     t, oh, dh = _custom(m, 1024, 64, 16, 16, seed=5)
     bad = t.token_ordering.copy()
     bad[10] = 1024 + 7       # out of range id, owned by centroid 0 (selected: K = C)
     dbad = m.MaskedHead(dh.centroid_w, dh.embed_w, torch.from_numpy(bad).cuda(), 16, vocab_size=1024)
-    hidden = synth.random_hidden(2, 64, 6)
+    hidden = synth.random_hidden(B, 64, 6)
     h = helpers.bf16_tensor(hidden)
-    ws = dbad.workspace(2)
+    ws = dbad.workspace(B)
     tok, _ = m.mtp_masked_topk_tokens(dbad, h, workspace=ws)
     assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_TOKEN_RANGE
     # a clean call on the same workspace clears the word
@@ -475,3 +489,87 @@ def test_empty_batch_is_noop(build_lib):
     h = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
     tok, mx = m.mtp_masked_topk_tokens(dh, h)
     assert tok.numel() == 0
+
+
+# ---------------------------------------------------------------------------
+# the cluster-ordered copy of the embedding table
+
+
+def test_reorder_embeddings_is_the_ordering_gather(build_lib):
+    """Row p of the ordered copy is embedding row token_ordering[p] (first H columns;
+    the row stride is the table's, padding columns are not written)."""
+    m = build_lib
+    t, oh, dh = _custom(m, 4096, 128, 64, 5, seed=31, pad_rows=64, pad_cols=8)
+    ordered = dh.use_ordered_table()
+    torch.cuda.synchronize()
+    got = ordered.view(torch.int16).cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(got[:, :128], t.embed_w[t.token_ordering])
+
+
+def test_reorder_embeddings_flags_bad_token_ids(build_lib):
+    m = build_lib
+    t, oh, dh = _custom(m, 1024, 64, 16, 4, seed=5)
+    bad = t.token_ordering.copy()
+    bad[10] = 1024 + 7
+    dbad = m.MaskedHead(dh.centroid_w, dh.embed_w, torch.from_numpy(bad).cuda(), 4, vocab_size=1024)
+    ws = dbad.workspace(1)
+    ws[:64].zero_()
+    out = torch.zeros(1024, 64, dtype=torch.bfloat16, device="cuda")
+    m.mtp_reorder_embeddings(dbad, out, workspace=ws)
+    assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_TOKEN_RANGE
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    keep = np.arange(1024) != 10
+    np.testing.assert_array_equal(got[keep], t.embed_w[bad[keep]])
+    assert not got[10].any()   # the bad row is left as it was
+
+
+def _same_outputs(m, dh, h):
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    torch.cuda.synchronize()
+    return tok.clone(), mx.clone(), sc.clone()
+
+
+@pytest.mark.parametrize("H,B,sizes", [
+    (264, 7, None),                # CUDA-core gather
+    (264, 64, None),               # tensor-core gather (B*K >= 4C), K tail
+    (64, 41, "ragged"),            # empty and oversized clusters, last cluster at the table's end
+])
+def test_ordered_table_parity(build_lib, H, B, sizes):
+    """With the ordered copy attached, every finish matches the oracle and is bit-identical
+    to the token-order path (same rows, same arithmetic)."""
+    m = build_lib
+    if sizes == "ragged":
+        sz = [0] * 5 + [1, 2, 3] + [700, 1] + [37] * 20 + [0, 19]
+        t, oh, dh = _custom(m, int(sum(sz)), H, len(sz), 6, seed=77, sizes=sz)
+    else:
+        t, oh, dh = _custom(m, 4096, H, 32, 8, seed=H + 5)
+    hidden = synth.random_hidden(B, H, H + 6)
+    h = helpers.bf16_tensor(hidden)
+    base = _same_outputs(m, dh, h)
+    dh.use_ordered_table()
+    try:
+        _full_check(m, oh, dh, hidden, f"ordered H={H} B={B}")
+        got = _same_outputs(m, dh, h)
+        for a, b in zip(base, got):
+            assert torch.equal(a, b)
+    finally:
+        dh.drop_ordered_table()
+
+
+@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64)])
+def test_ordered_table_full_size(build_lib, name, B):
+    m = build_lib
+    oh, dh = device_head(m, name)
+    t = helpers.tables(name)
+    hidden, ref, _ = helpers.clean_batch(name, oh, B)
+    h = helpers.bf16_tensor(hidden)
+    base = _same_outputs(m, dh, h)
+    dh.use_ordered_table()
+    try:
+        got = _same_outputs(m, dh, h)
+        np.testing.assert_array_equal(got[0].cpu().numpy(), ref["tokens"])
+        for a, b in zip(base, got):
+            assert torch.equal(a, b)
+    finally:
+        dh.drop_ordered_table()
