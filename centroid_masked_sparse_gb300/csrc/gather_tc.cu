@@ -1,33 +1,40 @@
-// Gather + sparse dot products on the tensor cores, for calls whose buckets are
-// large (many batch rows chose the same cluster).
+// Gather + sparse dot products on the tensor cores.
 //
 // Steps 3-4 and both finishes of Gemma4MTPMaskedEmbedder ("Add Gemma4 MTP
 // speculative decoding with centroids masking", vLLM gemma4_mtp.py), like
-// score.cu, but each work item is treated as the dense contraction it is when
-// its bucket holds many rows: logits[t, r] = sum_k E[tok_t, k] * h[row_r, k] for
-// the item's ≤128 candidate positions t and the bucket's rows r.
+// score.cu, but each work item is treated as the small dense contraction it is:
+// logits[t, r] = sum_k E[tok_t, k] * h[row_r, k] for the item's candidate
+// positions t (at most 128) and the rows r of the cluster's bucket.
 //
-// One unit = (work item, block of ≤128 bucket rows).  The candidate embedding
-// rows are the MMA's M side (one token per TMEM lane), the bucket's hidden rows
-// its N side (padded to a multiple of 16 per unit), K = H in 64-element blocks.
-// Both operands are gathered by TMA with tile::gather4 (four arbitrary rows of
-// 64 bf16 per instruction, 128-byte swizzle, the layout the MMA descriptors
-// expect); padding rows use an out-of-range row coordinate, which TMA fills
-// with zeros without reading memory.  With the cluster-ordered copy of the
-// embedding table the item's candidate rows are consecutive, and the A tile is
-// one plain 64 x 128 TMA tile load instead of 32 gathers (rows past the
-// cluster's end are loaded but their lanes are ignored).  Warp roles per CTA
-// (one CTA per SM):
-//   warp 4   producer: per unit, builds the token and row lists in a small
-//            metadata ring, then per k-block lets each lane issue one gather4 of
-//            candidate rows (and of hidden rows) into a ring of stages;
-//   warp 5   one thread issues tcgen05.mma (kind::f16, fp32 in TMEM,
-//            double-buffered accumulators);
+// One unit = (work item, block of at most nmax bucket rows).  The candidate
+// embedding rows are the MMA's M side (one token per TMEM lane, M = 128 with the
+// lanes past the chunk ignored), the bucket's hidden rows its N side (padded to
+// a multiple of 16), K = H in 64-element blocks.  Operands reach shared memory
+// by TMA in the 128-byte-swizzled layout the MMA descriptors expect:
+//   * with the cluster-ordered copy of the embedding table the chunk's candidate
+//     rows are consecutive, and the A tile is one plain tile load of 32, 64 or
+//     128 rows (the smallest box that holds the chunk);
+//   * with the token-order table they are gathered four rows per instruction
+//     (tile::gather4), skipping groups that are all padding;
+//   * the bucket's hidden rows are always gathered (tile::gather4); padding rows
+//     use an out-of-range row, which TMA fills with zeros without reading memory.
+// Tile rows that no load wrote hold stale data; they only feed TMEM lanes and
+// columns the epilogue ignores.
+//
+// Warp roles per CTA (one CTA per SM, 224 threads):
+//   warp 4   metadata: walks this CTA's items and publishes each unit's token
+//            and row lists into a ring of kMeta entries, running ahead of the
+//            loads so that its dependent global reads (item record, row mask,
+//            token ids) never stall the stream;
+//   warp 6   TMA issue: per unit and k-block, one stage of A and B loads;
+//   warp 5   one thread issues tcgen05.mma (kind::f16, fp32 in TMEM, two
+//            accumulators so the epilogue of one unit overlaps the next);
 //   warps 0-3 epilogue: tcgen05.ld of the unit's logits (thread = candidate),
 //            then the scatter store or the per-row argmax fold.
 // Every mbarrier wait is bounded and records MTP_DEVERR_TIMEOUT if it gives up.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -39,18 +46,23 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTileM = 128;        // candidate positions per unit
+constexpr int kThreads = 224;
+constexpr int kTileM = 128;        // MMA M: candidate positions per unit (at most)
 constexpr int kTileK = 64;         // bf16 per k-block (128-byte rows)
-constexpr int kMaxN = 128;         // bucket rows per unit
+constexpr int kMaxN = 128;         // bucket rows per unit (at most)
 constexpr int kMeta = 4;           // unit-metadata ring
-constexpr uint32_t kABytes = kTileM * kTileK * 2;
+constexpr int kMaxStages = 32;
+constexpr uint32_t kRowBytes = kTileK * 2;
+constexpr uint32_t kFullABytes = kTileM * kRowBytes;   // what one M = 128 MMA reads
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kMetaReaders = 6;   // 4 epilogue warps + the MMA thread + the TMA warp
 
 struct UnitMeta {
-    int tok[kTileM];    // candidate token ids (-1: padding)
-    int rows[kMaxN];    // bucket rows of this unit (n of them)
-    int n, npad, nvalid, pad;
+    int tok[kTileM];    // candidate token ids (-1: padding or invalid id)
+    int rows[kMaxN];    // bucket rows of this unit (n of them), then p.B up to npad
+    int n;              // rows in this unit; -1: end of stream
+    int npad, nvalid, p0, box;
+    int pad[3];
 };
 
 struct Params {
@@ -66,9 +78,12 @@ struct Params {
     float *out_max;
     int B, H, V, S, W, C;
     int chunk;      // positions per work item (<= 128)
-    int ordered;    // tmap_e is the cluster-ordered table in 64 x 128 tiles
+    int ordered;    // A comes from the cluster-ordered table (tile loads)
+    int nmax;       // bucket rows per unit (multiple of 16, <= 128)
     int num_kb;
     int stages;
+    uint32_t a_bytes, b_bytes;   // stage sizes
+    uint32_t tmem_cols;
 };
 
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int y0, int y1,
@@ -86,7 +101,7 @@ __device__ __forceinline__ void timeout(const Params &p)
     atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TIMEOUT);
 }
 
-// Rows of the bucket of cluster c in row order, block `blk` (kMaxN rows per block):
+// Rows of the bucket of cluster c in row order, block `blk` (nmax rows per block):
 // the warp writes them to `rows` and returns how many (all lanes).
 __device__ int bucket_rows(const Params &p, int c, int blk, int lane, int *rows)
 {
@@ -99,35 +114,182 @@ __device__ int bucket_rows(const Params &p, int c, int blk, int lane, int *rows)
         if (lane >= o) incl += y;
     }
     int pos = incl - cnt;
-    const int lo = blk * kMaxN, hi = lo + kMaxN;
+    const int lo = blk * p.nmax, hi = lo + p.nmax;
     for (uint32_t m = w; m; m &= m - 1u, ++pos)
         if (pos >= lo && pos < hi) rows[pos - lo] = lane * kWarp + __ffs(m) - 1;
     const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
-    return max(0, min(kMaxN, total - lo));
+    return max(0, min(p.nmax, total - lo));
+}
+
+// Metadata warp: publishes the units of this CTA's items (items blockIdx.x,
+// blockIdx.x + G, ...), then an end-of-stream entry.  False after a timed-out wait.
+__device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, uint32_t mempty0, int lane)
+{
+    const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
+    const int G = (int)gridDim.x;
+    int u = 0;
+    int it = blockIdx.x;
+    int2 item = it < n_items ? p.items[it] : make_int2(-1, 0);
+    for (; it < n_items; it += G) {
+        const int2 cur = item;
+        if (it + G < n_items) item = p.items[it + G];   // the next record, loaded early
+        int lo = 0, hi = 0;
+        if ((unsigned)cur.x < (unsigned)p.C && cur.y >= 0)
+            cluster_range(p.offsets, p.V, p.S, cur.x, &lo, &hi, nullptr);
+        const int p0 = cur.y > hi - lo ? hi : lo + cur.y;
+        const int nvalid = max(0, min(p.chunk, hi - p0));
+        if (nvalid == 0) continue;
+        for (int blk = 0;; ++blk) {
+            const int um = u % kMeta;
+            // a slot acquired for a block that turns out empty is reused by the next
+            // unit: its phase is unchanged until a unit is published in it
+            if (!mbar_wait(mempty0 + 8u * um, ((uint32_t)(u / kMeta) & 1u) ^ 1u, kWaitNs)) return false;
+            UnitMeta &m = meta[um];
+            const int n = bucket_rows(p, cur.x, blk, lane, m.rows);
+            if (n == 0) break;
+            const int npad = (n + 15) & ~15;
+            for (int r = n + lane; r < npad; r += kWarp) m.rows[r] = p.B;   // zero rows
+#pragma unroll
+            for (int j = 0; j < kTileM / kWarp; ++j) {
+                const int t = j * kWarp + lane;
+                int tok = -1;
+                if (t < nvalid) {
+                    tok = __ldg(p.ordering + p0 + t);
+                    if ((unsigned)tok >= (unsigned)p.V) {
+                        atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
+                        tok = -1;
+                    }
+                }
+                m.tok[t] = tok;
+            }
+            if (lane == 0) {
+                m.n = n;
+                m.npad = npad;
+                m.nvalid = nvalid;
+                m.p0 = p0;
+                m.box = nvalid <= 32 ? 32 : nvalid <= 64 ? 64 : kTileM;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                mbar_arrive(mfull0 + 8u * um);
+            }
+            ++u;
+            if (n < p.nmax) break;   // the bucket ended in this block
+        }
+    }
+    // end of stream
+    const int um = u % kMeta;
+    int ok = 1;
+    if (lane == 0) {
+        ok = mbar_wait(mempty0 + 8u * um, ((uint32_t)(u / kMeta) & 1u) ^ 1u, kWaitNs);
+        if (ok) {
+            meta[um].n = -1;
+            __threadfence_block();
+            mbar_arrive(mfull0 + 8u * um);
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// TMA warp: one stage of loads per (unit, k-block).  False after a timed-out wait;
+// then the stages it filled last are waited for (bounded), so that no copy is
+// still landing in shared memory when the CTA exits.
+__device__ void drain_loads(const Params &p, uint32_t full0, uint32_t issued, int lane)
+{
+    if (lane != 0) return;
+    const uint32_t S = (uint32_t)p.stages;
+    for (uint32_t q = issued > S ? issued - S : 0u; q < issued; ++q)
+        mbar_wait(full0 + 8u * (q % S), (q / S) & 1u, kWaitNs);
+}
+
+__device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtensorMap *tmap_e,
+                            const CUtensorMap *tmap_e64, const CUtensorMap *tmap_e32,
+                            const CUtensorMap *tmap_h, uint8_t *a_smem, uint8_t *b_smem, uint32_t full0,
+                            uint32_t empty0, uint32_t mfull0, uint32_t mempty0, int lane)
+{
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    for (int u = 0;; ++u) {
+        const int um = u % kMeta;
+        if (!mbar_wait(mfull0 + 8u * um, (uint32_t)(u / kMeta) & 1u, kWaitNs)) {
+            drain_loads(p, full0, issued, lane);
+            return false;
+        }
+        const UnitMeta &m = meta[um];
+        const int n = m.n;
+        if (n < 0) return true;
+        const int npad = m.npad, nvalid = m.nvalid, p0 = m.p0, box = m.box;
+        // lane j gathers candidate rows 4j..4j+3 (token-order table) and bucket rows
+        // 4j..4j+3 while 4j < npad
+        const int y0 = m.tok[4 * lane] >= 0 ? m.tok[4 * lane] : p.V;
+        const int y1 = m.tok[4 * lane + 1] >= 0 ? m.tok[4 * lane + 1] : p.V;
+        const int y2 = m.tok[4 * lane + 2] >= 0 ? m.tok[4 * lane + 2] : p.V;
+        const int y3 = m.tok[4 * lane + 3] >= 0 ? m.tok[4 * lane + 3] : p.V;
+        const bool has_b = 4 * lane < npad;
+        const int z0 = has_b ? m.rows[4 * lane] : 0, z1 = has_b ? m.rows[4 * lane + 1] : 0;
+        const int z2 = has_b ? m.rows[4 * lane + 2] : 0, z3 = has_b ? m.rows[4 * lane + 3] : 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mempty0 + 8u * um);   // the entry is in registers now
+        const bool has_a = 4 * lane < nvalid;
+        const CUtensorMap *amap = box == 32 ? tmap_e32 : box == 64 ? tmap_e64 : tmap_e;
+        const uint32_t a_tx =
+            p.ordered ? (uint32_t)box * kRowBytes : (uint32_t)((nvalid + 3) / 4) * 4 * kRowBytes;
+        const uint32_t tx = a_tx + (uint32_t)npad * kRowBytes;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            int wok = 1;
+            if (lane == 0) {
+                wok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitNs);
+                if (wok) mbar_arrive_expect_tx(full0 + 8u * stage, tx);
+            }
+            if (!__shfl_sync(0xffffffffu, wok, 0)) {
+                drain_loads(p, full0, issued, lane);
+                return false;
+            }
+            ++issued;
+            const uint32_t bar = full0 + 8u * stage;
+            const uint32_t a_dst = smem_u32(a_smem + (size_t)stage * p.a_bytes);
+            if (p.ordered) {
+                if (lane == 0) tma_load_2d(a_dst, amap, kb * kTileK, p0, bar);
+            } else if (has_a) {
+                tma_gather4(a_dst + (uint32_t)lane * 4 * kRowBytes, tmap_e, kb * kTileK, y0, y1, y2, y3, bar);
+            }
+            if (has_b)
+                tma_gather4(smem_u32(b_smem + (size_t)stage * p.b_bytes) + (uint32_t)lane * 4 * kRowBytes,
+                            tmap_h, kb * kTileK, z0, z1, z2, z3, bar);
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
 }
 
 template <bool SCATTER>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_h,
+    k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_e64,
+                const __grid_constant__ CUtensorMap tmap_e32, const __grid_constant__ CUtensorMap tmap_h,
                 const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int S = p.stages;
-    constexpr uint32_t kBBytes = kMaxN * kTileK * 2;
     uint8_t *a_smem = smem;
-    uint8_t *b_smem = smem + (size_t)S * kABytes;
-    UnitMeta *meta = reinterpret_cast<UnitMeta *>(b_smem + (size_t)S * kBBytes);
+    uint8_t *b_smem = smem + (size_t)S * p.a_bytes;
+    // an M = 128 MMA reads kFullABytes from a stage's base: slack after the B stages
+    // keeps the last stage's read inside the allocation when a_bytes is smaller
+    uint8_t *tail = b_smem + (size_t)S * p.b_bytes + (kFullABytes - p.a_bytes);
+    UnitMeta *meta = reinterpret_cast<UnitMeta *>(tail);
     unsigned long long *best = reinterpret_cast<unsigned long long *>(meta + kMeta);
     uint64_t *bars = reinterpret_cast<uint64_t *>(best + p.B);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 4 + 2 * kMeta);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5 + 2 * kMeta);
     __shared__ int s_last;
 
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x & (kWarp - 1);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8u * S;
     const uint32_t tfull0 = empty0 + 8u * S, tempty0 = tfull0 + 16u;
     const uint32_t mfull0 = tempty0 + 16u, mempty0 = mfull0 + 8u * kMeta;
-    constexpr uint32_t kTmemCols = 2 * kMaxN;
+    const uint32_t drain_bar = mempty0 + 8u * kMeta;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -140,145 +302,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int m = 0; m < kMeta; ++m) {
             mbar_init(mfull0 + 8u * m, 1);
-            mbar_init(mempty0 + 8u * m, 5);   // 4 epilogue warps + the MMA thread
+            mbar_init(mempty0 + 8u * m, kMetaReaders);
         }
+        mbar_init(drain_bar, 1);
         fence_barrier_init();
     }
     if (!SCATTER)
         for (int b = threadIdx.x; b < p.B; b += kThreads) best[b] = 0ull;
-    if (warp == 0) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    if (warp == 0) tmem_alloc(smem_u32(tmem_holder), p.tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     // the work items and buckets come from the top-K kernel before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
-    const int G = (int)gridDim.x;
-    const int nblk_max = (p.B + kMaxN - 1) / kMaxN;
+    const uint32_t acc_cols = p.tmem_cols / 2;
 
     if (warp == 4) {
-        // ------------------------------------------------------------- producer
-        int stage = 0, u = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int it = blockIdx.x; it < n_items && ok; it += G) {
-            const int2 item = p.items[it];
-            int lo = 0, hi = 0;
-            if ((unsigned)item.x < (unsigned)p.C && item.y >= 0)
-                cluster_range(p.offsets, p.V, p.S, item.x, &lo, &hi, nullptr);
-            const int p0 = item.y > hi - lo ? hi : lo + item.y;
-            const int nvalid = max(0, min(min(p.chunk, kTileM), hi - p0));
-            if (nvalid == 0) continue;
-            for (int blk = 0; blk < nblk_max && ok; ++blk, ++u) {
-                const int um = u % kMeta;
-                const uint32_t mpar = (uint32_t)(u / kMeta) & 1u;
-                if (!mbar_wait(mempty0 + 8u * um, mpar ^ 1u, kWaitNs)) {
-                    ok = false;
-                    break;
-                }
-                UnitMeta &m = meta[um];
-                const int n = bucket_rows(p, item.x, blk, lane, m.rows);
-                if (n == 0) {
-                    // no rows in this block (the bucket is smaller): publish an empty unit
-                    // so the ring stays in step, then stop this item
-                    if (lane == 0) {
-                        m.n = 0;
-                        m.npad = 0;
-                        m.nvalid = 0;
-                        __threadfence_block();
-                        mbar_arrive(mfull0 + 8u * um);
-                    }
-                    __syncwarp();
-                    ++u;
-                    break;
-                }
-                const int npad = (n + 15) & ~15;
-                for (int r = n + lane; r < npad; r += kWarp) m.rows[r] = p.B;   // zero rows
-#pragma unroll
-                for (int j = 0; j < kTileM / kWarp; ++j) {
-                    const int t = j * kWarp + lane;
-                    int tok = -1;
-                    if (t < nvalid) {
-                        tok = __ldg(p.ordering + p0 + t);
-                        if ((unsigned)tok >= (unsigned)p.V) {
-                            atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
-                            tok = -1;
-                        }
-                    }
-                    m.tok[t] = tok;
-                }
-                if (lane == 0) {
-                    m.n = n;
-                    m.npad = npad;
-                    m.nvalid = nvalid;
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence_block();
-                    mbar_arrive(mfull0 + 8u * um);
-                }
-                // the k-blocks: lane j gathers candidate rows 4j..4j+3 and, while j < npad/4,
-                // bucket rows 4j..4j+3 (out-of-range coordinates for padding)
-                const int y0 = m.tok[4 * lane] >= 0 ? m.tok[4 * lane] : p.V;
-                const int y1 = m.tok[4 * lane + 1] >= 0 ? m.tok[4 * lane + 1] : p.V;
-                const int y2 = m.tok[4 * lane + 2] >= 0 ? m.tok[4 * lane + 2] : p.V;
-                const int y3 = m.tok[4 * lane + 3] >= 0 ? m.tok[4 * lane + 3] : p.V;
-                const bool has_b = 4 * lane < npad;
-                const int z0 = has_b ? m.rows[4 * lane] : 0, z1 = has_b ? m.rows[4 * lane + 1] : 0;
-                const int z2 = has_b ? m.rows[4 * lane + 2] : 0, z3 = has_b ? m.rows[4 * lane + 3] : 0;
-                // candidate groups of four that are all padding are not fetched at all: their
-                // tile rows keep stale data, and the epilogue ignores those rows (token -1)
-                const bool has_a = 4 * lane < nvalid;
-                const uint32_t na = (uint32_t)(nvalid + 3) / 4;
-                const uint32_t tx = (p.ordered ? kABytes : na * 4 * 128) + (uint32_t)npad * kTileK * 2;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    int wok = 1;
-                    if (lane == 0) {
-                        wok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitNs);
-                        if (wok) mbar_arrive_expect_tx(full0 + 8u * stage, tx);
-                    }
-                    if (!__shfl_sync(0xffffffffu, wok, 0)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t bar = full0 + 8u * stage;
-                    if (p.ordered) {
-                        if (lane == 0)
-                            tma_load_2d(smem_u32(a_smem + (size_t)stage * kABytes), &tmap_e, kb * kTileK, p0, bar);
-                    } else if (has_a)
-                        tma_gather4(smem_u32(a_smem + (size_t)stage * kABytes + (size_t)lane * 4 * 128),
-                                    &tmap_e, kb * kTileK, y0, y1, y2, y3, bar);
-                    if (has_b)
-                        tma_gather4(smem_u32(b_smem + (size_t)stage * kBBytes + (size_t)lane * 4 * 128),
-                                    &tmap_h, kb * kTileK, z0, z1, z2, z3, bar);
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (n < kMaxN) {
-                    ++u;
-                    break;  // the bucket fits this block: no further row block
-                }
-            }
-        }
-        // end of stream: an empty unit with n = -1
-        if (ok) {
-            const int um = u % kMeta;
-            const uint32_t mpar = (uint32_t)(u / kMeta) & 1u;
-            if (lane == 0) {
-                if (mbar_wait(mempty0 + 8u * um, mpar ^ 1u, kWaitNs)) {
-                    meta[um].n = -1;
-                    __threadfence_block();
-                    mbar_arrive(mfull0 + 8u * um);
-                } else {
-                    ok = false;
-                }
-            }
-        }
-        if (!ok && lane == 0) timeout(p);
+        if (!publish_units(p, meta, mfull0, mempty0, lane) && lane == 0) timeout(p);
+    } else if (warp == 6) {
+        if (!issue_loads(p, meta, &tmap_e, &tmap_e64, &tmap_e32, &tmap_h, a_smem, b_smem, full0, empty0, mfull0,
+                         mempty0, lane) &&
+            lane == 0)
+            timeout(p);
     } else if (warp == 5) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -294,14 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n < 0) break;
                 const int npad = meta[um].npad;
                 mbar_arrive(mempty0 + 8u * um);   // done with this entry's metadata
-                if (n == 0) continue;
                 if (!mbar_wait(tempty0 + 8u * acc, acc_phase ^ 1u, kWaitNs)) {
                     timeout(p);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(kTileM, npad);
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kMaxN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)acc * acc_cols;
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(full0 + 8u * stage, phase, kWaitNs)) {
@@ -309,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sw128_kmajor_desc(smem_u32(a_smem + (size_t)stage * kABytes));
-                    const uint64_t bd = sw128_kmajor_desc(smem_u32(b_smem + (size_t)stage * kBBytes));
+                    const uint64_t ad = sw128_kmajor_desc(smem_u32(a_smem + (size_t)stage * p.a_bytes));
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(b_smem + (size_t)stage * p.b_bytes));
 #pragma unroll
                     for (int k = 0; k < kTileK / 16; ++k)
                         mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
@@ -328,6 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
+            // every MMA issued has completed before the accumulators are freed
+            mma_commit(drain_bar);
+            mbar_wait(drain_bar, 0u, kWaitNs);
         }
     } else {
         // ------------------------------------------------------------- epilogue
@@ -342,46 +390,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             const UnitMeta &m = meta[um];
             const int n = m.n;
             if (n < 0) break;
-            if (n > 0) {
-                if (!mbar_wait(tfull0 + 8u * acc, acc_phase, kWaitNs)) {
-                    if (lane == 0) timeout(p);
-                    break;
-                }
-                tc_fence_after();
-                const int t = warp * kWarp + lane;
-                const int tok = m.tok[t];
-                const uint32_t trow = tmem_base + ((uint32_t)(warp * kWarp) << 16) + (uint32_t)(acc * kMaxN);
-                for (int c0 = 0; c0 < m.npad; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_load_16(trow + (uint32_t)c0, r);
-                    tmem_wait_load();
+            if (!mbar_wait(tfull0 + 8u * acc, acc_phase, kWaitNs)) {
+                if (lane == 0) timeout(p);
+                break;
+            }
+            tc_fence_after();
+            const int t = warp * kWarp + lane;
+            const int tok = m.tok[t];
+            const uint32_t trow = tmem_base + ((uint32_t)(warp * kWarp) << 16) + (uint32_t)acc * acc_cols;
+            for (int c0 = 0; c0 < m.npad; c0 += 16) {
+                uint32_t r[16];
+                tmem_load_16(trow + (uint32_t)c0, r);
+                tmem_wait_load();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = c0 + j;
-                        if (col >= n) break;
-                        const float v = __uint_as_float(r[j]);
-                        const int row = m.rows[col];
-                        if (SCATTER) {
-                            if (tok >= 0) p.out_logits[(size_t)row * p.V + tok] = v;
-                        } else {
-                            unsigned long long key = tok >= 0 ? argmax_key(v, tok) : 0ull;
+                for (int j = 0; j < 16; ++j) {
+                    const int col = c0 + j;
+                    if (col >= n) break;
+                    const float v = __uint_as_float(r[j]);
+                    const int row = m.rows[col];
+                    if (SCATTER) {
+                        if (tok >= 0) p.out_logits[(size_t)row * p.V + tok] = v;
+                    } else {
+                        unsigned long long key = tok >= 0 ? argmax_key(v, tok) : 0ull;
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) {
-                                const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-                                key = other > key ? other : key;
-                            }
-                            if (lane == 0 && key) atomicMax(best + row, key);
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+                            key = other > key ? other : key;
                         }
+                        if (lane == 0 && key) atomicMax(best + row, key);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
             }
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(mempty0 + 8u * um);
+            if (lane == 0) {
+                mbar_arrive(tempty0 + 8u * acc);
+                mbar_arrive(mempty0 + 8u * um);
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
         }
     }
 
@@ -389,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, p.tmem_cols);
     }
     if (SCATTER) return;
     for (int b = threadIdx.x; b < p.B; b += kThreads) {
@@ -443,13 +490,13 @@ bool encode_rows(CUtensorMap *map, const void *base, long long inner, long long 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-size_t gather_tc_smem_bytes(int B, int stages)
+size_t smem_bytes(const Params &p, int stages)
 {
-    return 1024 + (size_t)stages * (kABytes + (size_t)kMaxN * kTileK * 2) + kMeta * sizeof(UnitMeta) +
-           (size_t)B * 8 + (size_t)(2 * stages + 4 + 2 * kMeta) * 8 + 16;
+    return 1024 + (size_t)stages * (p.a_bytes + p.b_bytes) + (kFullABytes - p.a_bytes) +
+           kMeta * sizeof(UnitMeta) + (size_t)p.B * 8 + (size_t)(2 * stages + 5 + 2 * kMeta) * 8 + 16;
 }
+
+}  // namespace
 
 cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s)
 {
@@ -471,27 +518,46 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     p.W = g.W;
     p.C = g.C;
     p.chunk = g.chunk;
-    if (p.chunk > kTileM) return cudaErrorInvalidValue;
+    if (p.chunk < 1 || p.chunk > kTileM) return cudaErrorInvalidValue;
+    p.ordered = g.embed_ordered != nullptr;
+    p.nmax = std::min(kMaxN, (g.B + 15) & ~15);
     p.num_kb = (g.H + kTileK - 1) / kTileK;
-    int stages = 6;
-    while (stages > 2 && gather_tc_smem_bytes(g.B, stages) > 220 * 1024) --stages;
+    // the A stage holds the largest box a unit can load: 32, 64 or 128 rows
+    const int a_rows = p.chunk <= 32 ? 32 : p.chunk <= 64 ? 64 : kTileM;
+    p.a_bytes = (uint32_t)a_rows * kRowBytes;
+    p.b_bytes = (uint32_t)p.nmax * kRowBytes;
+    uint32_t cols = 32;
+    while (cols < 2u * (uint32_t)p.nmax) cols <<= 1;
+    p.tmem_cols = cols;
+    int stages = kMaxStages;
+    while (stages > 2 && smem_bytes(p, stages) > 220 * 1024) --stages;
     p.stages = stages;
     alignas(64) CUtensorMap map_e;
+    alignas(64) CUtensorMap map_e64;
+    alignas(64) CUtensorMap map_e32;
     alignas(64) CUtensorMap map_h;
-    p.ordered = g.embed_ordered != nullptr;
-    if (p.ordered ? !encode_rows(&map_e, g.embed_ordered, g.H, g.V, g.ld, kTileM)
-                  : !encode_rows(&map_e, g.embed, g.H, g.V, g.ld, 1))
-        return cudaErrorInvalidValue;
+    if (p.ordered) {
+        if (!encode_rows(&map_e, g.embed_ordered, g.H, g.V, g.ld, kTileM) ||
+            !encode_rows(&map_e64, g.embed_ordered, g.H, g.V, g.ld, 64) ||
+            !encode_rows(&map_e32, g.embed_ordered, g.H, g.V, g.ld, 32))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!encode_rows(&map_e, g.embed, g.H, g.V, g.ld, 1)) return cudaErrorInvalidValue;
+        map_e64 = map_e;
+        map_e32 = map_e;
+    }
     if (!encode_rows(&map_h, g.hidden, g.H, g.B, g.H, 1)) return cudaErrorInvalidValue;
-    const size_t smem = gather_tc_smem_bytes(g.B, stages);
+    const size_t smem = smem_bytes(p, stages);
     if (scatter) {
         cudaError_t e = allow_smem((const void *)k_gather_tc<true>, smem);
         if (e != cudaSuccess) return e;
-        return launch_dependent(k_gather_tc<true>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_h, p);
+        return launch_dependent(k_gather_tc<true>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_e64,
+                                map_e32, map_h, p);
     }
     cudaError_t e = allow_smem((const void *)k_gather_tc<false>, smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_gather_tc<false>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_h, p);
+    return launch_dependent(k_gather_tc<false>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_e64,
+                            map_e32, map_h, p);
 }
 
 }  // namespace mtp

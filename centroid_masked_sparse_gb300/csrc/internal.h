@@ -55,6 +55,8 @@ cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s
 constexpr int kTcGatherChunk = 128;
 // Expected rows per selected cluster (B*K/C) from which the tensor-core gather is used.
 constexpr int kTcGatherMinReuse = 4;
+// With the cluster-ordered table: (row, cluster) pairs per SM from which it is used.
+constexpr int kTcOrderedMinPairsPerSm = 2;
 cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s);
 // out[p, :H] = embed[ordering[p], :H] (the cluster-ordered embedding copy, score.cu).
 cudaError_t launch_reorder_rows(const uint16_t *embed, long long ld, const int32_t *ordering, int V, int H,

@@ -1,6 +1,8 @@
 // C ABI of the centroid-masked sparse LM head: argument checks, workspace
 // layout and the launch sequence of each call.  Declarations and the contract
 // of every entry point are in include/mtp_head.h.
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 #include <unordered_map>
 
@@ -264,6 +266,31 @@ int choose_chunk(const mtp_head_desc *d, int B)
     return ch;
 }
 
+// Which gather a call runs.  The tensor-core gather takes calls whose buckets are
+// large (many rows per selected cluster), and every call with the cluster-ordered
+// table once there are enough selected clusters to occupy the SMs: there its A
+// operand is a plain tile load and the kernel issues few instructions per byte.
+// Its chunk is the largest of 128, 64, 32 positions that still gives about two
+// work items per SM.  Everything else runs the CUDA-core gather.
+bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
+{
+    const long long pairs = (long long)B * d->top_k;
+    if (pairs >= (long long)kTcGatherMinReuse * d->num_centroids) {
+        *chunk = kTcGatherChunk;
+        return true;
+    }
+    if (d->embed_ordered && pairs >= (long long)kTcOrderedMinPairsPerSm * sm_count()) {
+        const double avg = (double)d->vocab_size / d->num_centroids;
+        const double clusters = (double)std::min<long long>(pairs, d->num_centroids);
+        int ch = kTcGatherChunk;
+        while (ch > 32 && clusters * std::ceil(avg / ch) < 2.0 * sm_count()) ch /= 2;
+        *chunk = ch;
+        return true;
+    }
+    *chunk = choose_chunk(d, B);
+    return false;
+}
+
 mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t *out_tokens,
                       float *out_max, float *out_logits, void *workspace, size_t ws_bytes,
                       cudaStream_t s)
@@ -279,9 +306,8 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
         st = cuda_status(launch_fill_neg_inf(out_logits, (size_t)B * d->vocab_size, s));
         if (st != MTP_OK) return st;
     }
-    // large buckets (many rows per selected cluster) go to the tensor-core gather
-    const bool tc_gather = (long long)B * d->top_k >= (long long)kTcGatherMinReuse * d->num_centroids;
-    const int chunk = tc_gather ? kTcGatherChunk : choose_chunk(d, B);
+    int chunk = 0;
+    const bool tc_gather = tc_gather_plan(d, B, &chunk);
     st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s);
     if (st != MTP_OK) return st;
 

@@ -104,9 +104,12 @@ typedef enum mtp_status {
  *                    ordered-position order, row p = embed_w row token_ordering[p] (see
  *                    mtp_reorder_embeddings).  When set, the masked calls read every
  *                    selected cluster's candidate rows as one contiguous block instead of
- *                    gathering them row by row; results are identical either way.  NULL:
- *                    gather from embed_w (the page's layout).  It must match embed_w and
- *                    token_ordering; the library does not check that. */
+ *                    gathering them row by row, which lets more calls run the tensor-core
+ *                    gather; token ids are the same either way and logits agree within
+ *                    fp32 summation-order rounding (bit for bit when the same gather
+ *                    kernel runs).  NULL: gather from embed_w (the page's layout).  It
+ *                    must match embed_w and token_ordering; the library does not check
+ *                    that. */
 typedef struct mtp_head_desc {
     int32_t vocab_size;
     int32_t hidden_size;

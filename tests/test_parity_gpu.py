@@ -537,7 +537,7 @@ def _same_outputs(m, dh, h):
 ])
 def test_ordered_table_parity(build_lib, H, B, sizes):
     """With the ordered copy attached, every finish matches the oracle and is bit-identical
-    to the token-order path (same rows, same arithmetic)."""
+    to the token-order path: at these sizes both run the same gather kernel."""
     m = build_lib
     if sizes == "ragged":
         sz = [0] * 5 + [1, 2, 3] + [700, 1] + [37] * 20 + [0, 19]
@@ -557,11 +557,13 @@ def test_ordered_table_parity(build_lib, H, B, sizes):
         dh.drop_ordered_table()
 
 
-@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64)])
+@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64), ("uniform", 8)])
 def test_ordered_table_full_size(build_lib, name, B):
+    """Full-size tables with the ordered copy: the call may now run the other gather
+    kernel (the tensor cores sum in another order), so token ids must match exactly and
+    logits within the fp32 tolerance, against the oracle and the token-order path."""
     m = build_lib
     oh, dh = device_head(m, name)
-    t = helpers.tables(name)
     hidden, ref, _ = helpers.clean_batch(name, oh, B)
     h = helpers.bf16_tensor(hidden)
     base = _same_outputs(m, dh, h)
@@ -569,7 +571,13 @@ def test_ordered_table_full_size(build_lib, name, B):
     try:
         got = _same_outputs(m, dh, h)
         np.testing.assert_array_equal(got[0].cpu().numpy(), ref["tokens"])
-        for a, b in zip(base, got):
-            assert torch.equal(a, b)
+        np.testing.assert_array_equal(got[0].cpu().numpy(), base[0].cpu().numpy())
+        helpers.assert_close(got[1].cpu().numpy(), ref["max_logit"], f"ordered {name} max")
+        sc = got[2].cpu().numpy()
+        sref = oracle.masked_scatter_logits(oh, hidden[:8]) if B > 8 else None
+        if sref is not None:
+            helpers.assert_close(sc[:8], sref, f"ordered {name} scatter")
+        helpers.assert_close(sc, base[2].cpu().numpy(), f"ordered {name} scatter vs token order")
+        assert np.array_equal(np.isfinite(sc), np.isfinite(base[2].cpu().numpy()))
     finally:
         dh.drop_ordered_table()
