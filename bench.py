@@ -4,7 +4,9 @@ Default workload: Gemma-scale uniform clusters, V=262144 as 2048 clusters of
 128 tokens, H=1536, K=32 (4096 candidates a row), batch 64, sparse-argmax
 finish (mtp_masked_topk_tokens).  A step is one call of the whole head on one
 batch of synthetic hidden states, with the tables already resident in HBM.
-L2 is flushed (a 256 MB write) before every timed call, outside the events.
+L2 is flushed before every timed call, outside the events: a 256 MB write, then a
+512 MB read, so the written lines are evicted (and written back) before the
+call starts instead of inside it.
 
 Printed (rank 0, one JSON line): draft tokens/s over all ranks, µs per call,
 the gather-score kernel's roofline against the measured HBM copy bandwidth,
@@ -36,6 +38,7 @@ sys.path.insert(0, ROOT)
 METRIC = "masked-head draft tokens/s"
 UNIT = "tokens/s"
 FLUSH_BYTES = 256 << 20
+EVICT_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -191,6 +194,13 @@ class Timer:
     def __init__(self, torch, m, device):
         self.torch, self.m, self.device = torch, m, device
         self.flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.evict = torch.ones(EVICT_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush_l2(self):
+        """Write 256 MB (the flush), then read 512 MB: L2 ends up holding clean lines of
+        a buffer the call never touches, so no write-back of the flush lands in the call."""
+        self.flush.zero_()
+        self.evict.sum()
 
     def events(self, n):
         torch = self.torch
@@ -204,7 +214,7 @@ class Timer:
         records around each launch on the call's stream)."""
         torch, m = self.torch, self.m
         for i in range(warmup):
-            self.flush.zero_()
+            self.flush_l2()
             fn(i)
         names = ([kernel] if kernel else []) + [k for k in extra_kernels if k != kernel]
         call_ev = self.events(2 * steps)
@@ -214,7 +224,7 @@ class Timer:
         torch.cuda.synchronize()
         t0 = time.time()
         for i in range(steps):
-            self.flush.zero_()
+            self.flush_l2()
             for k in names:
                 m.mtp_profile_events(k, kev[k][2 * i], kev[k][2 * i + 1])
             call_ev[2 * i].record()
@@ -361,8 +371,7 @@ def gpu_main(args):
     t = synth.make_tables(name)
     dh = m.MaskedHead.from_host(t.centroid_w, t.embed_w, t.token_ordering, t.cluster_offsets,
                                 w.top_k, device=device)
-    if args.ordered:
-        dh.use_ordered_table()
+    dh_packed = dh.use_packed_table() if args.layout == "packed" else None
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
@@ -389,10 +398,12 @@ def gpu_main(args):
     value = ws * B / (call_ms * 1e-3)
     kern_s = res["kernel_ms"] * 1e-3
     achieved = res["bytes"]["gather"] / kern_s / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_gather_score", "achieved": round(achieved, 1),
+    plan = m.mtp_gather_plan(dh, B)
+    kfile, kname = ("gather_tc", "k_gather_tc") if plan == "tensor_core" else ("score", "k_gather_score")
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": hbm, "peak_source": f"{hbm_src} HBM copy GB/s", "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
-                "traffic": profiled_traffic("score", name, B),
+                "traffic": profiled_traffic(kfile, name, B),
                 "algorithmic_bytes": int(res["bytes"]["gather"]),
                 "kernel_us": round(res["kernel_ms"] * 1e3, 2)}
     call_gbs = res["bytes"]["call"] / (res["call_ms"] * 1e-3) / 1e9
@@ -401,9 +412,11 @@ def gpu_main(args):
            "us_per_call": round(call_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": {"workload": workload_label(w, B), "finish": "sparse argmax",
-                      "embedding_layout": "cluster-ordered copy" if args.ordered else "token order",
+                      "embedding_layout": ("packed tiles (built once at load, outside the timing)"
+                                           if args.layout == "packed" else "token order"),
                       "batch_per_gpu": B, "parallelism": "replicas" if ws > 1 else "single",
-                      "l2": "flushed before every timed call (256 MB write, outside the events)"},
+                      "l2": "flushed before every timed call, outside the events: 256 MB written, "
+                            "then 512 MB read so the written lines are evicted before the call"},
            "call_roofline": {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
                              "frac": round(call_gbs / hbm, 4),
                              "algorithmic_bytes": int(res["bytes"]["call"]),
@@ -425,7 +438,8 @@ def gpu_main(args):
                                row0=40000 + b)
             ach = r["bytes"]["gather"] / (r["kernel_ms"] * 1e-3) / 1e9
             cg = r["bytes"]["call"] / (r["call_ms"] * 1e-3) / 1e9
-            sweep[str(b)] = {"us_per_call": round(r["call_ms"] * 1e3, 2),
+            sweep[str(b)] = {"gather_kernel": m.mtp_gather_plan(dh, b),
+                             "us_per_call": round(r["call_ms"] * 1e3, 2),
                              "tokens_per_s": round(b / (r["call_ms"] * 1e-3), 1),
                              "gather_us": round(r["kernel_ms"] * 1e3, 2),
                              "gather_gbs": round(ach, 1), "gather_frac": round(ach / hbm, 4),
@@ -434,6 +448,15 @@ def gpu_main(args):
                              "kernels_us": r["kernels_us"], "max_call_us": r["max_call_us"],
                              "device_error": r["device_error"]}
         out["sweep"] = sweep
+        if args.layout == "packed":
+            # the same workload on the token-order table alone (no packed copy)
+            dh.drop_packed_table()
+            r = measure_masked(ctx, t, dh, name, B, max(20, args.steps // 4), args.warmup, row0=60000)
+            out["token_order_layout"] = {"us_per_call": round(r["call_ms"] * 1e3, 2),
+                                         "tokens_per_s": round(B / (r["call_ms"] * 1e-3), 1),
+                                         "gather_us": round(r["kernel_ms"] * 1e3, 2),
+                                         "kernels_us": r["kernels_us"]}
+            dh.use_packed_table(dh_packed)
         if not args.no_extra:
             out["other_workloads"] = other_workloads(ctx, args, hbm)
         out["cpu_baseline"] = cpu_baseline(t, name, B, budget_s=args.cpu_seconds)
@@ -452,19 +475,19 @@ def other_workloads(ctx, args, hbm):
     cases = (("scatter", True, False), ("variable", False, False), ("shared", False, False),
              ("shared", True, False), ("uniform", False, True), ("variable", False, True),
              ("shared", False, True), ("shared", True, True))
-    for name, scatter, ordered in cases:
+    for name, scatter, packed in cases:
         w = synth.WORKLOADS[name]
         t = synth.make_tables(name)
         dh = m.MaskedHead.from_host(t.centroid_w, t.embed_w, t.token_ordering, t.cluster_offsets,
                                     w.top_k, device=ctx["device"])
-        if ordered:
-            dh.use_ordered_table()
+        if packed:
+            dh.use_packed_table()
         r = measure_masked(ctx, t, dh, name, w.batch, steps, args.warmup, scatter=scatter)
         cg = r["bytes"]["call"] / (r["call_ms"] * 1e-3) / 1e9
         ga = r["bytes"]["gather"] / (r["kernel_ms"] * 1e-3) / 1e9
         key = f"{name}_{'scatter' if scatter else 'argmax'}_b{w.batch}"
-        if ordered:
-            key += "_ordered_table"
+        if packed:
+            key += "_packed_table"
         res[key] = {"workload": workload_label(w, w.batch),
                     "us_per_call": round(r["call_ms"] * 1e3, 2),
                     "tokens_per_s": round(w.batch / (r["call_ms"] * 1e-3), 1),
@@ -517,7 +540,8 @@ def reference_main(args):
            "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": workload_label(w, B), "finish": "sparse argmax",
-                      "embedding_layout": "cluster-ordered copy" if args.ordered else "token order",
+                      "embedding_layout": ("packed tiles (built once at load, outside the timing)"
+                                           if args.layout == "packed" else "token order"),
                       "batch_per_gpu": B},
            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads,
                             "kind": "oracle",
@@ -539,8 +563,9 @@ def parse():
     ap.add_argument("--quick", action="store_true", help="headline line only")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ordered", action="store_true",
-                    help="attach the cluster-ordered embedding copy (built once, outside the timing)")
+    ap.add_argument("--layout", default="packed", choices=["packed", "token"],
+                    help="embedding table the calls read: the packed tile copy (built once, outside "
+                         "the timing) or the token-order table alone")
     ap.add_argument("--finish", default="argmax", choices=["argmax", "scatter", "dense"],
                     help="profiling aid: time only this finish on the workload's tables")
     a = ap.parse_args()

@@ -22,7 +22,7 @@ from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_M
 
 __all__ = ["MaskedHead", "MtpError", "mtp_workspace_bytes", "mtp_centroid_scores",
            "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_dense_lm_head",
-           "mtp_read_device_error", "mtp_profile_events", "mtp_reorder_embeddings",
+           "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
            "MTP_DEVERR_TOKEN_RANGE",
            "MTP_DEVERR_OFFSETS", "lib"]
 
@@ -53,7 +53,7 @@ class MaskedHead:
     """
 
     def __init__(self, centroid_w, embed_w, token_ordering, top_k, cluster_offsets=None,
-                 vocab_size=None, embed_ordered=None):
+                 vocab_size=None, embed_packed=None):
         torch = _torch()
         if centroid_w is not None:
             assert centroid_w.dtype == torch.bfloat16 and centroid_w.is_contiguous()
@@ -78,30 +78,28 @@ class MaskedHead:
             embed_w=embed_w.data_ptr(), ld_embed=int(embed_w.stride(0)),
             token_ordering=None if token_ordering is None else token_ordering.data_ptr(),
             cluster_offsets=None if cluster_offsets is None else cluster_offsets.data_ptr(),
-            embed_ordered=None)
-        self.embed_ordered = None
+            embed_packed=None)
+        self.embed_packed = None
         self._ws = None
-        if embed_ordered is not None:
-            self.use_ordered_table(embed_ordered)
+        if embed_packed is not None:
+            self.use_packed_table(embed_packed)
 
-    def use_ordered_table(self, embed_ordered=None, stream=None):
-        """Attach a cluster-ordered embedding table (built with mtp_reorder_embeddings
-        when not given); the masked calls then read contiguous cluster blocks."""
+    def use_packed_table(self, packed=None, stream=None):
+        """Attach the packed embedding table (built here with mtp_pack_embeddings when
+        not given); calls then read candidate rows as contiguous tensor-core tiles."""
         torch = _torch()
-        if embed_ordered is None:
-            embed_ordered = torch.empty_strided(
-                (self.vocab_size, self.hidden_size), (int(self.embed_w.stride(0)), 1),
-                dtype=torch.bfloat16, device=self.device)
-            mtp_reorder_embeddings(self, embed_ordered, stream=stream)
-        assert embed_ordered.dtype == torch.bfloat16 and embed_ordered.stride(1) == 1
-        assert embed_ordered.stride(0) == self.embed_w.stride(0)
-        self.embed_ordered = embed_ordered
-        self.desc.embed_ordered = embed_ordered.data_ptr()
-        return embed_ordered
+        if packed is None:
+            n = mtp_packed_embeddings_bytes(self)
+            packed = torch.empty(n, dtype=torch.uint8, device=self.device)
+            mtp_pack_embeddings(self, packed, stream=stream)
+        assert packed.dtype == torch.uint8 and packed.is_contiguous()
+        self.embed_packed = packed
+        self.desc.embed_packed = packed.data_ptr()
+        return packed
 
-    def drop_ordered_table(self):
-        self.embed_ordered = None
-        self.desc.embed_ordered = None
+    def drop_packed_table(self):
+        self.embed_packed = None
+        self.desc.embed_packed = None
 
     @classmethod
     def from_host(cls, centroid_w, embed_w, token_ordering, cluster_offsets, top_k,
@@ -210,11 +208,23 @@ def mtp_dense_lm_head(head, hidden, out_logits=None, out_tokens=None, out_max=No
     return out_logits, out_tokens, out_max
 
 
-def mtp_reorder_embeddings(head, out, workspace=None, stream=None):
-    """Row p of `out` = embedding row token_ordering[p] (the cluster-ordered table)."""
-    check(lib().mtp_reorder_embeddings(ctypes.byref(head.desc), _ptr(out), _ptr(workspace),
-                                       _stream_ptr(stream, head.device)), "mtp_reorder_embeddings")
+def mtp_packed_embeddings_bytes(head) -> int:
+    return int(lib().mtp_packed_embeddings_bytes(ctypes.byref(head.desc)))
+
+
+def mtp_pack_embeddings(head, out, workspace=None, stream=None):
+    """Fill `out` (uint8, mtp_packed_embeddings_bytes) with the packed embedding table."""
+    check(lib().mtp_pack_embeddings(ctypes.byref(head.desc), _ptr(out), out.numel(), _ptr(workspace),
+                                    _stream_ptr(stream, head.device)), "mtp_pack_embeddings")
     return out
+
+
+def mtp_gather_plan(head, batch: int) -> str:
+    """'tensor_core' or 'cuda_core': the gather kernel a masked call of this batch runs."""
+    r = int(lib().mtp_gather_plan(ctypes.byref(head.desc), int(batch)))
+    if r < 0:
+        check(r, "mtp_gather_plan")
+    return "tensor_core" if r == 1 else "cuda_core"
 
 
 def mtp_read_device_error(workspace, stream=None) -> int:

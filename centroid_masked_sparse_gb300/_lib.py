@@ -41,7 +41,7 @@ class MtpHeadDesc(ctypes.Structure):
         ("ld_embed", ctypes.c_int64),
         ("token_ordering", ctypes.c_void_p),
         ("cluster_offsets", ctypes.c_void_p),
-        ("embed_ordered", ctypes.c_void_p),
+        ("embed_packed", ctypes.c_void_p),
     ]
 
 
@@ -54,7 +54,9 @@ SIGNATURES = {
     "mtp_masked_scatter_logits": (_i32, [_DP, _p, _i32, _p, _p, _sz, _p]),
     "mtp_dense_lm_head": (_i32, [_DP, _p, _i32, _p, _p, _p, _p, _sz, _p]),
     "mtp_masked_topk_tokens_noalloc": (_i32, [_DP, _p, _i32, _p, _p, _p]),
-    "mtp_reorder_embeddings": (_i32, [_DP, _p, _p, _p]),
+    "mtp_packed_embeddings_bytes": (ctypes.c_size_t, [_DP]),
+    "mtp_pack_embeddings": (_i32, [_DP, _p, ctypes.c_size_t, _p, _p]),
+    "mtp_gather_plan": (_i32, [_DP, _i32]),
     "mtp_read_device_error": (_i32, [_p, ctypes.POINTER(ctypes.c_uint32), _p]),
     "mtp_status_string": (ctypes.c_char_p, [_i32]),
     "mtp_version": (_i32, []),

@@ -186,7 +186,7 @@ struct TopkParams {
 struct GatherParams {
     const uint16_t *hidden;         // [B, H]
     const uint16_t *embed;          // [>=V, ld]
-    const uint16_t *embed_ordered;  // [V, ld]: row p = embed row ordering[p], or null
+    const uint8_t *packed;          // packed embedding table (tensor-core gather), or null
     long long ld;
     const int32_t *ordering;        // [V]
     const int32_t *offsets;         // [C+1] or null

@@ -11,15 +11,18 @@
 // lanes past the chunk ignored), the bucket's hidden rows its N side (padded to
 // a multiple of 16), K = H in 64-element blocks.  Operands reach shared memory
 // by TMA in the 128-byte-swizzled layout the MMA descriptors expect:
-//   * with the cluster-ordered copy of the embedding table the chunk's candidate
-//     rows are consecutive, and the A tile is one plain tile load of 32, 64 or
-//     128 rows (the smallest box that holds the chunk);
+//   * with the packed embedding table (below) the chunk's candidate rows are one
+//     or two contiguous, pre-swizzled runs of a 16 KB block per k-block, fetched
+//     with plain bulk copies: few large copies are what streams HBM fastest;
 //   * with the token-order table they are gathered four rows per instruction
 //     (tile::gather4), skipping groups that are all padding;
-//   * the bucket's hidden rows are always gathered (tile::gather4); padding rows
-//     use an out-of-range row, which TMA fills with zeros without reading memory.
-// Tile rows that no load wrote hold stale data; they only feed TMEM lanes and
-// columns the epilogue ignores.
+//   * the bucket's hidden rows are always gathered (tile::gather4), only the
+//     groups of four that hold real rows (a padding row inside such a group uses
+//     an out-of-range row, which TMA fills with zeros without reading memory).
+// Each gather4 costs the TMA unit far more time than its 512 bytes suggest, so
+// the count of gathers per k-block, not bytes, sets this kernel's pace once
+// buckets are large; tile rows that no load wrote hold stale data, which only
+// feeds TMEM lanes and columns the epilogue ignores.
 //
 // Warp roles per CTA (one CTA per SM, 224 threads):
 //   warp 4   metadata: walks this CTA's items and publishes each unit's token
@@ -32,6 +35,13 @@
 //   warps 0-3 epilogue: tcgen05.ld of the unit's logits (thread = candidate),
 //            then the scatter store or the per-row argmax fold.
 // Every mbarrier wait is bounded and records MTP_DEVERR_TIMEOUT if it gives up.
+//
+// The packed table (its layout is specified with mtp_pack_embeddings in the C
+// header) stores each cluster's rows in ordered-position order, padded to 32
+// rows, as 16 KB blocks of 128 padded rows x 64 elements in the 128-byte
+// swizzle.  A run of rows starting at a multiple of 8 rows, copied to a
+// 1024-byte-aligned stage, is already the MMA's K-major operand (the swizzle
+// depends on the row modulo 8 only).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -56,12 +66,17 @@ constexpr uint32_t kRowBytes = kTileK * 2;
 constexpr uint32_t kFullABytes = kTileM * kRowBytes;   // what one M = 128 MMA reads
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kMetaReaders = 6;   // 4 epilogue warps + the MMA thread + the TMA warp
+constexpr int kPackRows = 32;          // clusters are padded to multiples of this
+constexpr int kPackSuper = 128;        // rows per packed block
+constexpr uint32_t kPackBlock = kPackSuper * kRowBytes;  // 16384 bytes
 
 struct UnitMeta {
     int tok[kTileM];    // candidate token ids (-1: padding or invalid id)
     int rows[kMaxN];    // bucket rows of this unit (n of them), then p.B up to npad
     int n;              // rows in this unit; -1: end of stream
-    int npad, nvalid, p0, box;
+    int npad, nvalid;
+    int p0;             // token-order table: first ordered position; packed: first group
+    int box;            // token-order table: unused; packed: groups of 32 rows
     int pad[3];
 };
 
@@ -77,8 +92,9 @@ struct Params {
     int32_t *out_tokens;
     float *out_max;
     int B, H, V, S, W, C;
-    int chunk;      // positions per work item (<= 128)
-    int ordered;    // A comes from the cluster-ordered table (tile loads)
+    int chunk;      // positions per work item (<= 128; a multiple of 32 when packed)
+    const uint8_t *packed;    // packed table blocks, or null (token-order gathers)
+    const int32_t *poff;      // its padded cluster offsets [C+1]
     int nmax;       // bucket rows per unit (multiple of 16, <= 128)
     int num_kb;
     int stages;
@@ -127,6 +143,7 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
 {
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
     const int G = (int)gridDim.x;
+    const long long packed_groups = p.packed ? __ldg(p.poff + p.C) / kPackRows : 0;
     int u = 0;
     int it = blockIdx.x;
     int2 item = it < n_items ? p.items[it] : make_int2(-1, 0);
@@ -139,6 +156,14 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
         const int p0 = cur.y > hi - lo ? hi : lo + cur.y;
         const int nvalid = max(0, min(p.chunk, hi - p0));
         if (nvalid == 0) continue;
+        // packed table: the chunk starts at padded position poff[c] + y, a group boundary;
+        // a chunk reaching past the table's last group (tables packed from other
+        // offsets) is skipped and flagged instead of read
+        const int g0 = p.packed ? (__ldg(p.poff + cur.x) + cur.y) / kPackRows : 0;
+        if (p.packed && (long long)g0 + (nvalid + kPackRows - 1) / kPackRows > packed_groups) {
+            if (lane == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
+            continue;
+        }
         for (int blk = 0;; ++blk) {
             const int um = u % kMeta;
             // a slot acquired for a block that turns out empty is reused by the next
@@ -166,8 +191,8 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                 m.n = n;
                 m.npad = npad;
                 m.nvalid = nvalid;
-                m.p0 = p0;
-                m.box = nvalid <= 32 ? 32 : nvalid <= 64 ? 64 : kTileM;
+                m.p0 = p.packed ? g0 : p0;
+                m.box = (nvalid + kPackRows - 1) / kPackRows;
             }
             __syncwarp();
             if (lane == 0) {
@@ -204,7 +229,6 @@ __device__ void drain_loads(const Params &p, uint32_t full0, uint32_t issued, in
 }
 
 __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtensorMap *tmap_e,
-                            const CUtensorMap *tmap_e64, const CUtensorMap *tmap_e32,
                             const CUtensorMap *tmap_h, uint8_t *a_smem, uint8_t *b_smem, uint32_t full0,
                             uint32_t empty0, uint32_t mfull0, uint32_t mempty0, int lane)
 {
@@ -219,23 +243,34 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
         const UnitMeta &m = meta[um];
         const int n = m.n;
         if (n < 0) return true;
-        const int npad = m.npad, nvalid = m.nvalid, p0 = m.p0, box = m.box;
+        const int nvalid = m.nvalid, g0 = m.p0, groups = m.box;
         // lane j gathers candidate rows 4j..4j+3 (token-order table) and bucket rows
-        // 4j..4j+3 while 4j < npad
+        // 4j..4j+3 while 4j < n
         const int y0 = m.tok[4 * lane] >= 0 ? m.tok[4 * lane] : p.V;
         const int y1 = m.tok[4 * lane + 1] >= 0 ? m.tok[4 * lane + 1] : p.V;
         const int y2 = m.tok[4 * lane + 2] >= 0 ? m.tok[4 * lane + 2] : p.V;
         const int y3 = m.tok[4 * lane + 3] >= 0 ? m.tok[4 * lane + 3] : p.V;
-        const bool has_b = 4 * lane < npad;
+        const bool has_b = 4 * lane < n;
         const int z0 = has_b ? m.rows[4 * lane] : 0, z1 = has_b ? m.rows[4 * lane + 1] : 0;
         const int z2 = has_b ? m.rows[4 * lane + 2] : 0, z3 = has_b ? m.rows[4 * lane + 3] : 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(mempty0 + 8u * um);   // the entry is in registers now
         const bool has_a = 4 * lane < nvalid;
-        const CUtensorMap *amap = box == 32 ? tmap_e32 : box == 64 ? tmap_e64 : tmap_e;
-        const uint32_t a_tx =
-            p.ordered ? (uint32_t)box * kRowBytes : (uint32_t)((nvalid + 3) / 4) * 4 * kRowBytes;
-        const uint32_t tx = a_tx + (uint32_t)npad * kRowBytes;
+        const uint32_t a_tx = p.packed ? (uint32_t)groups * kPackRows * kRowBytes
+                                       : (uint32_t)((nvalid + 3) / 4) * 4 * kRowBytes;
+        // packed: rows [pp0, pp0 + groups*32) of the padded table, pp0 = 32*g0; the run
+        // is in block pp0/128 from row pp0%128 on, and continues at row 0 of the next
+        // block if it crosses the block's end (lane 0 copies the first part, lane 1 the rest)
+        const int prow0 = g0 * kPackRows, nrows = groups * kPackRows;
+        const int blk0 = prow0 / kPackSuper, r0 = prow0 % kPackSuper;
+        const int first = min(nrows, kPackSuper - r0);
+        const bool has_pk = lane == 0 || (lane == 1 && nrows > first);
+        const uint32_t pk_bytes = (uint32_t)(lane == 0 ? first : nrows - first) * kRowBytes;
+        const uint32_t pk_dst_off = lane == 0 ? 0u : (uint32_t)first * kRowBytes;
+        const uint8_t *pk_src = p.packed ? p.packed + (size_t)(blk0 + lane) * p.num_kb * kPackBlock +
+                                               (lane == 0 ? (size_t)r0 * kRowBytes : 0)
+                                         : nullptr;
+        const uint32_t tx = a_tx + (uint32_t)((n + 3) / 4) * 4 * kRowBytes;
         for (int kb = 0; kb < p.num_kb; ++kb) {
             int wok = 1;
             if (lane == 0) {
@@ -249,8 +284,9 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
             ++issued;
             const uint32_t bar = full0 + 8u * stage;
             const uint32_t a_dst = smem_u32(a_smem + (size_t)stage * p.a_bytes);
-            if (p.ordered) {
-                if (lane == 0) tma_load_2d(a_dst, amap, kb * kTileK, p0, bar);
+            if (p.packed) {
+                if (has_pk)
+                    bulk_copy_g2s(a_dst + pk_dst_off, pk_src + (size_t)kb * kPackBlock, pk_bytes, bar);
             } else if (has_a) {
                 tma_gather4(a_dst + (uint32_t)lane * 4 * kRowBytes, tmap_e, kb * kTileK, y0, y1, y2, y3, bar);
             }
@@ -267,8 +303,7 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
 
 template <bool SCATTER>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_e64,
-                const __grid_constant__ CUtensorMap tmap_e32, const __grid_constant__ CUtensorMap tmap_h,
+    k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_h,
                 const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -321,8 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 4) {
         if (!publish_units(p, meta, mfull0, mempty0, lane) && lane == 0) timeout(p);
     } else if (warp == 6) {
-        if (!issue_loads(p, meta, &tmap_e, &tmap_e64, &tmap_e32, &tmap_h, a_smem, b_smem, full0, empty0, mfull0,
-                         mempty0, lane) &&
+        if (!issue_loads(p, meta, &tmap_e, &tmap_h, a_smem, b_smem, full0, empty0, mfull0, mempty0, lane) &&
             lane == 0)
             timeout(p);
     } else if (warp == 5) {
@@ -519,10 +553,15 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     p.C = g.C;
     p.chunk = g.chunk;
     if (p.chunk < 1 || p.chunk > kTileM) return cudaErrorInvalidValue;
-    p.ordered = g.embed_ordered != nullptr;
-    p.nmax = std::min(kMaxN, (g.B + 15) & ~15);
     p.num_kb = (g.H + kTileK - 1) / kTileK;
-    // the A stage holds the largest box a unit can load: 32, 64 or 128 rows
+    if (g.packed) {
+        if (p.chunk % kPackRows != 0) return cudaErrorInvalidValue;
+        p.packed = g.packed;
+        p.poff = reinterpret_cast<const int32_t *>(
+            g.packed + packed_poff_offset(g.V, g.H, g.C, g.offsets != nullptr));
+    }
+    p.nmax = std::min(kMaxN, (g.B + 15) & ~15);
+    // the A stage holds the chunk: 32, 64 or 128 rows
     const int a_rows = p.chunk <= 32 ? 32 : p.chunk <= 64 ? 64 : kTileM;
     p.a_bytes = (uint32_t)a_rows * kRowBytes;
     p.b_bytes = (uint32_t)p.nmax * kRowBytes;
@@ -533,31 +572,164 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     while (stages > 2 && smem_bytes(p, stages) > 220 * 1024) --stages;
     p.stages = stages;
     alignas(64) CUtensorMap map_e;
-    alignas(64) CUtensorMap map_e64;
-    alignas(64) CUtensorMap map_e32;
     alignas(64) CUtensorMap map_h;
-    if (p.ordered) {
-        if (!encode_rows(&map_e, g.embed_ordered, g.H, g.V, g.ld, kTileM) ||
-            !encode_rows(&map_e64, g.embed_ordered, g.H, g.V, g.ld, 64) ||
-            !encode_rows(&map_e32, g.embed_ordered, g.H, g.V, g.ld, 32))
-            return cudaErrorInvalidValue;
-    } else {
-        if (!encode_rows(&map_e, g.embed, g.H, g.V, g.ld, 1)) return cudaErrorInvalidValue;
-        map_e64 = map_e;
-        map_e32 = map_e;
-    }
+    // the token-order map is encoded either way (unused with the packed table)
+    if (!encode_rows(&map_e, g.embed, g.H, g.V, g.ld, 1)) return cudaErrorInvalidValue;
     if (!encode_rows(&map_h, g.hidden, g.H, g.B, g.H, 1)) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes(p, stages);
     if (scatter) {
         cudaError_t e = allow_smem((const void *)k_gather_tc<true>, smem);
         if (e != cudaSuccess) return e;
-        return launch_dependent(k_gather_tc<true>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_e64,
-                                map_e32, map_h, p);
+        return launch_dependent(k_gather_tc<true>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_h, p);
     }
     cudaError_t e = allow_smem((const void *)k_gather_tc<false>, smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_gather_tc<false>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_e64,
-                            map_e32, map_h, p);
+    return launch_dependent(k_gather_tc<false>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_h, p);
+}
+
+// ---------------------------------------------------------------------------
+// Packing the embedding table
+// ---------------------------------------------------------------------------
+namespace {
+
+size_t packed_groups_bound(int V, int C, bool explicit_offsets)
+{
+    if (!explicit_offsets) {
+        const long long S = V / C;
+        return (size_t)C * (size_t)((S + kPackRows - 1) / kPackRows);
+    }
+    return (size_t)(((long long)V + (long long)(kPackRows - 1) * C + kPackRows - 1) / kPackRows);
+}
+
+// Padded cluster offsets, one CTA: poff[c] = sum over c' < c of roundup(size(c'), 32).
+// Offsets whose padded total exceeds the buffer's bound (overlapping clusters) are
+// an error: every cluster is then recorded as empty, so no later read or write
+// leaves the buffer.
+__global__ void __launch_bounds__(1024) k_pack_offsets(const int32_t *offsets, int V, int S, int C,
+                                                       long long bound_rows, int32_t *poff, uint32_t *ctrl)
+{
+    __shared__ long long warp_tot[32];
+    const int per = (C + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int c0 = min(C, (int)threadIdx.x * per), c1 = min(C, c0 + per);
+    long long local = 0;
+    for (int c = c0; c < c1; ++c) {
+        int lo = 0, hi = 0;
+        cluster_range(offsets, V, S, c, &lo, &hi, ctrl ? ctrl + kCtrlError : nullptr);
+        local += (hi - lo + kPackRows - 1) / kPackRows * kPackRows;
+    }
+    // exclusive scan of `local` over the block
+    const int lane = threadIdx.x & (kWarp - 1), w = threadIdx.x / kWarp;
+    const int nw = (int)blockDim.x / kWarp;
+    long long incl = local;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == kWarp - 1) warp_tot[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        long long t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) warp_tot[lane] = t;   // inclusive over warps
+    }
+    __syncthreads();
+    const bool bad = warp_tot[nw - 1] > bound_rows;
+    if (bad && threadIdx.x == 0 && ctrl) atomicOr(ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
+    long long run = bad ? 0 : incl - local + (w > 0 ? warp_tot[w - 1] : 0);
+    for (int c = c0; c < c1; ++c) {
+        poff[c] = (int32_t)run;
+        if (bad) continue;
+        int lo = 0, hi = 0;
+        cluster_range(offsets, V, S, c, &lo, &hi, nullptr);
+        run += (hi - lo + kPackRows - 1) / kPackRows * kPackRows;
+    }
+    if (threadIdx.x == blockDim.x - 1) poff[C] = bad ? 0 : (int32_t)warp_tot[nw - 1];
+}
+
+// One CTA of 256 threads per 32-row group g and k-block kb (4 KB of the 16 KB
+// block of super-group g/4): thread = (row, piece).
+__global__ void __launch_bounds__(256) k_pack_tiles(const uint16_t *__restrict__ embed, long long ld,
+                                                    const int32_t *__restrict__ ordering,
+                                                    const int32_t *__restrict__ offsets, int V, int H, int S, int C,
+                                                    int num_kb, const int32_t *__restrict__ poff,
+                                                    uint8_t *__restrict__ packed, uint32_t *ctrl)
+{
+    __shared__ int row_tok[kPackRows];
+    const int r = threadIdx.x >> 3, j = threadIdx.x & 7;
+    const long long groups = __ldg(poff + C) / kPackRows;
+    const long long total = groups * num_kb;
+    for (long long blk = blockIdx.x; blk < total; blk += gridDim.x) {
+        const long long g = blk / num_kb;
+        const int kb = (int)(blk - g * num_kb);
+        __syncthreads();   // the previous block's row_tok is consumed
+        if (j == 0) {
+            // the cluster holding padded position 32g + r: the last c with poff[c] <= pp
+            const int pp = (int)(g * kPackRows) + r;
+            int a = 0, b = C;   // poff[a] <= pp < poff[b] holds for the answer a
+            while (b - a > 1) {
+                const int mid = (a + b) >> 1;
+                if (__ldg(poff + mid) <= pp) a = mid;
+                else b = mid;
+            }
+            int lo = 0, hi = 0;
+            cluster_range(offsets, V, S, a, &lo, &hi, nullptr);
+            const int local = pp - __ldg(poff + a);
+            int tok = -1;
+            if (local < hi - lo) {
+                tok = __ldg(ordering + lo + local);
+                if ((unsigned)tok >= (unsigned)V) {
+                    if (ctrl) atomicOr(ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
+                    tok = -1;
+                }
+            }
+            row_tok[r] = tok;
+        }
+        __syncthreads();
+        const int tok = row_tok[r];
+        const int k0 = kb * kTileK + j * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (tok >= 0 && k0 < H) v = ld_stream16(embed + (long long)tok * ld + k0);
+        const size_t sub = ((size_t)(g / 4) * num_kb + kb) * kPackBlock + (size_t)(g % 4) * kPackRows * kRowBytes;
+        uint8_t *dst = packed + sub + (size_t)r * kRowBytes + (size_t)((j ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4 *>(dst) = v;
+    }
+}
+
+}  // namespace
+
+size_t packed_poff_offset(int V, int H, int C, bool explicit_offsets)
+{
+    const size_t num_kb = (size_t)((H + kTileK - 1) / kTileK);
+    const size_t supers = (packed_groups_bound(V, C, explicit_offsets) + 3) / 4;
+    return supers * num_kb * kPackBlock;   // a multiple of 16 KB: poff stays 256-byte aligned
+}
+
+size_t packed_table_bytes(int V, int H, int C, bool explicit_offsets)
+{
+    return packed_poff_offset(V, H, C, explicit_offsets) + (size_t)(C + 1) * sizeof(int32_t);
+}
+
+cudaError_t launch_pack_embeddings(const uint16_t *embed, long long ld, const int32_t *ordering,
+                                   const int32_t *offsets, int V, int H, int C, uint8_t *packed, uint32_t *ctrl,
+                                   cudaStream_t s)
+{
+    const int S = offsets ? 0 : V / C;
+    int32_t *poff = reinterpret_cast<int32_t *>(packed + packed_poff_offset(V, H, C, offsets != nullptr));
+    const long long bound_rows = (long long)packed_groups_bound(V, C, offsets != nullptr) * kPackRows;
+    k_pack_offsets<<<1, 1024, 0, s>>>(offsets, V, S, C, bound_rows, poff, ctrl);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int num_kb = (H + kTileK - 1) / kTileK;
+    const long long total = (long long)packed_groups_bound(V, C, offsets != nullptr) * num_kb;
+    const long long grid = std::min<long long>(total, (long long)sm_count() * 8);
+    k_pack_tiles<<<(int)std::max<long long>(1, grid), 256, 0, s>>>(embed, ld, ordering, offsets, V, H, S, C,
+                                                                     num_kb, poff, packed, ctrl);
+    return cudaGetLastError();
 }
 
 }  // namespace mtp

@@ -50,17 +50,20 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
 void gather_geometry(GatherParams &p);
 size_t gather_smem_bytes(const GatherParams &p);
 cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s);
-// Tensor-core variant of the gather for large buckets (gather_tc.cu); p.chunk <= 128.
+// Tensor-core variant of the gather (gather_tc.cu); p.chunk <= 128, a multiple of 32
+// when p.packed is set.
 cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s);
 constexpr int kTcGatherChunk = 128;
 // Expected rows per selected cluster (B*K/C) from which the tensor-core gather is used.
 constexpr int kTcGatherMinReuse = 4;
-// With the cluster-ordered table: (row, cluster) pairs per SM from which it is used.
-constexpr int kTcOrderedMinPairsPerSm = 2;
 cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s);
-// out[p, :H] = embed[ordering[p], :H] (the cluster-ordered embedding copy, score.cu).
-cudaError_t launch_reorder_rows(const uint16_t *embed, long long ld, const int32_t *ordering, int V, int H,
-                                uint16_t *out, uint32_t *ctrl, cudaStream_t s);
+// The packed embedding table of the tensor-core gather (gather_tc.cu): byte size for
+// the shapes (an upper bound with explicit offsets) and the kernels that fill it.
+size_t packed_table_bytes(int V, int H, int C, bool explicit_offsets);
+size_t packed_poff_offset(int V, int H, int C, bool explicit_offsets);
+cudaError_t launch_pack_embeddings(const uint16_t *embed, long long ld, const int32_t *ordering,
+                                   const int32_t *offsets, int V, int H, int C, uint8_t *packed,
+                                   uint32_t *ctrl, cudaStream_t s);
 
 // Tensor-core skinny GEMM out[n, m] = sum_k table[m, k] * hidden[n, k] (gemm_tc.cu).
 struct TcGemmArgs {

@@ -2,7 +2,6 @@
 // layout and the launch sequence of each call.  Declarations and the contract
 // of every entry point are in include/mtp_head.h.
 #include <algorithm>
-#include <cmath>
 #include <mutex>
 #include <unordered_map>
 
@@ -144,7 +143,7 @@ mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool o
     if (embed) {
         if (d->ld_embed < d->hidden_size) return MTP_ERR_SHAPE;
         if (d->ld_embed % 8 != 0 || !aligned16(d->embed_w)) return MTP_ERR_ALIGN;
-        if (!aligned16(d->embed_ordered)) return MTP_ERR_ALIGN;
+        if (((uintptr_t)d->embed_packed & 255u) != 0) return MTP_ERR_ALIGN;
     }
     if (centroids) {
         if (d->num_centroids < 1 || d->top_k < 1 || d->top_k > d->num_centroids) return MTP_ERR_SHAPE;
@@ -267,24 +266,30 @@ int choose_chunk(const mtp_head_desc *d, int B)
 }
 
 // Which gather a call runs.  The tensor-core gather takes calls whose buckets are
-// large (many rows per selected cluster), and every call with the cluster-ordered
-// table once there are enough selected clusters to occupy the SMs: there its A
-// operand is a plain tile load and the kernel issues few instructions per byte.
-// Its chunk is the largest of 128, 64, 32 positions that still gives about two
-// work items per SM.  Everything else runs the CUDA-core gather.
+// large (B*K >= 4C), where one candidate tile serves a whole bucket.  With the
+// packed embedding table it also takes calls over uniform clusters (a multiple
+// of 32 positions: no padding in the table) with at least C (row, cluster)
+// pairs: there its 16 KB block copies stream HBM faster than the CUDA-core
+// gather's row copies (measured at B*K = C: ~10% less gather time).  Smaller
+// calls keep more SMs busy with the CUDA-core gather's finer work items, and
+// ragged clusters would read the packed table's padding.  Its chunk is the
+// largest of 128, 64, 32 positions that still gives about two work items per SM.
 bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
 {
     const long long pairs = (long long)B * d->top_k;
-    if (pairs >= (long long)kTcGatherMinReuse * d->num_centroids) {
-        *chunk = kTcGatherChunk;
-        return true;
-    }
-    if (d->embed_ordered && pairs >= (long long)kTcOrderedMinPairsPerSm * sm_count()) {
+    const bool large = pairs >= (long long)kTcGatherMinReuse * d->num_centroids;
+    const bool packed_uniform = d->embed_packed && !d->cluster_offsets &&
+                                (d->vocab_size / d->num_centroids) % 32 == 0 && pairs >= d->num_centroids;
+    if (d->embed_packed && (large || packed_uniform)) {
         const double avg = (double)d->vocab_size / d->num_centroids;
         const double clusters = (double)std::min<long long>(pairs, d->num_centroids);
         int ch = kTcGatherChunk;
-        while (ch > 32 && clusters * std::ceil(avg / ch) < 2.0 * sm_count()) ch /= 2;
+        while (ch > 32 && clusters * (double)((long long)(avg + ch - 1) / ch) < 2.0 * sm_count()) ch /= 2;
         *chunk = ch;
+        return true;
+    }
+    if (large) {
+        *chunk = kTcGatherChunk;
         return true;
     }
     *chunk = choose_chunk(d, B);
@@ -314,7 +319,7 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     GatherParams gp{};
     gp.hidden = (const uint16_t *)hidden;
     gp.embed = (const uint16_t *)d->embed_w;
-    gp.embed_ordered = (const uint16_t *)d->embed_ordered;
+    gp.packed = tc_gather ? (const uint8_t *)d->embed_packed : nullptr;
     gp.ld = d->ld_embed;
     gp.ordering = d->token_ordering;
     gp.offsets = d->cluster_offsets;
@@ -441,21 +446,48 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
     return cuda_status(launch_tc_gemm(g, s));
 }
 
-mtp_status mtp_reorder_embeddings(const mtp_head_desc *desc, void *embed_ordered_out, void *workspace,
-                                  void *stream)
+size_t mtp_packed_embeddings_bytes(const mtp_head_desc *desc)
+{
+    if (check_desc(desc, false, true, false) != MTP_OK) return 0;
+    if (desc->num_centroids < 1 || desc->num_centroids > MTP_MAX_CENTROIDS) return 0;
+    if (!desc->cluster_offsets && desc->vocab_size % desc->num_centroids != 0) return 0;
+    return packed_table_bytes(desc->vocab_size, desc->hidden_size, desc->num_centroids,
+                              desc->cluster_offsets != nullptr);
+}
+
+mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, size_t packed_bytes, void *workspace,
+                               void *stream)
 {
     mtp_status st = check_desc(desc, false, true, false);
     if (st != MTP_OK) return st;
-    if (!desc->token_ordering || !embed_ordered_out) return MTP_ERR_NULL;
-    if (!aligned16(embed_ordered_out) || !aligned16(workspace)) return MTP_ERR_ALIGN;
-    const char *src = (const char *)desc->embed_w, *dst = (const char *)embed_ordered_out;
-    const size_t bytes = (size_t)desc->vocab_size * desc->ld_embed * 2;
-    if (src < dst + bytes && dst < src + bytes) return MTP_ERR_SHAPE;   // overlapping tables
+    if (!desc->token_ordering || !packed) return MTP_ERR_NULL;
+    if (desc->num_centroids < 1) return MTP_ERR_SHAPE;
+    if (desc->num_centroids > MTP_MAX_CENTROIDS) return MTP_ERR_UNSUPPORTED;
+    if (!desc->cluster_offsets && desc->vocab_size % desc->num_centroids != 0) return MTP_ERR_SHAPE;
+    if (((uintptr_t)packed & 255u) != 0 || !aligned16(workspace)) return MTP_ERR_ALIGN;
+    const size_t need = packed_table_bytes(desc->vocab_size, desc->hidden_size, desc->num_centroids,
+                                           desc->cluster_offsets != nullptr);
+    if (packed_bytes < need) return MTP_ERR_WORKSPACE;
+    const char *src = (const char *)desc->embed_w, *dst = (const char *)packed;
+    const size_t src_bytes = (size_t)desc->vocab_size * desc->ld_embed * 2;
+    if (src < dst + need && dst < src + src_bytes) return MTP_ERR_SHAPE;   // overlapping tables
     st = use_device(desc->device);
     if (st != MTP_OK) return st;
-    return cuda_status(launch_reorder_rows((const uint16_t *)desc->embed_w, desc->ld_embed, desc->token_ordering,
-                                           desc->vocab_size, desc->hidden_size, (uint16_t *)embed_ordered_out,
-                                           (uint32_t *)workspace, (cudaStream_t)stream));
+    return cuda_status(launch_pack_embeddings((const uint16_t *)desc->embed_w, desc->ld_embed,
+                                              desc->token_ordering, desc->cluster_offsets, desc->vocab_size,
+                                              desc->hidden_size, desc->num_centroids, (uint8_t *)packed,
+                                              (uint32_t *)workspace, (cudaStream_t)stream));
+}
+
+int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch)
+{
+    mtp_status st = check_desc(desc, true, true, true);
+    if (st != MTP_OK) return st;
+    st = check_batch(batch);
+    if (st != MTP_OK) return st;
+    if (batch == 0) return 0;
+    int chunk = 0;
+    return tc_gather_plan(desc, batch, &chunk) ? 1 : 0;
 }
 
 mtp_status mtp_read_device_error(const void *workspace, uint32_t *host_word, void *stream)

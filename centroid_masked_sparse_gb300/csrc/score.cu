@@ -41,8 +41,6 @@
 // CTA to finish (a ticket, never a wait) turns the per-row keys into token
 // ids.  Every mbarrier wait gives up after a wall-clock limit and records
 // MTP_DEVERR_TIMEOUT rather than hanging.
-#include <algorithm>
-
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -239,14 +237,10 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
                         sm.meta[slot].tok = tok;
                         sm.meta[slot].use = huse - 1u;
                         if (tok >= 0) {
-                            // the same row either way: by token id, or by position in the
-                            // cluster-ordered copy (consecutive positions, consecutive rows)
-                            const uint16_t *src = p.embed_ordered
-                                                      ? p.embed_ordered + (long long)(cur.p0 + q) * p.ld
-                                                      : p.embed + (long long)tok * p.ld;
                             mbar_arrive_expect_tx(sm.full0 + 8u * slot, rb);
-                            bulk_copy_g2s_hint(smem_u32(sm.ring + (size_t)slot * rb), src, rb,
-                                               sm.full0 + 8u * slot, pol);
+                            bulk_copy_g2s_hint(smem_u32(sm.ring + (size_t)slot * rb),
+                                               p.embed + (long long)tok * p.ld, rb, sm.full0 + 8u * slot,
+                                               pol);
                         } else {
                             mbar_arrive(sm.full0 + 8u * slot);
                         }
@@ -543,37 +537,6 @@ __global__ void __launch_bounds__(256) k_fill_neg_inf(float *out, size_t n)
         o4[i] = v;
     if (blockIdx.x == 0 && threadIdx.x < (n & 3))
         out[n4 * 4 + threadIdx.x] = ninf;
-}
-
-// out[p, :H] = embed[ordering[p], :H] for p < V: one warp per row, 16-byte lanes.
-__global__ void __launch_bounds__(256) k_reorder_rows(const uint16_t *__restrict__ embed, long long ld,
-                                                      const int32_t *__restrict__ ordering, int V, int H,
-                                                      uint16_t *__restrict__ out, uint32_t *ctrl)
-{
-    const int lane = threadIdx.x & (kWarp - 1);
-    const int hv = H >> 3;
-    const long long warps = (long long)gridDim.x * (blockDim.x / kWarp);
-    for (long long p = (long long)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; p < V; p += warps) {
-        const int tok = __ldg(ordering + p);
-        if ((unsigned)tok >= (unsigned)V) {
-            if (lane == 0 && ctrl) atomicOr(ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
-            continue;
-        }
-        const uint16_t *src = embed + (long long)tok * ld;
-        uint16_t *dst = out + p * ld;
-        for (int i = lane; i < hv; i += kWarp)
-            *reinterpret_cast<uint4 *>(dst + i * 8) = ld_stream16(src + i * 8);
-    }
-}
-
-cudaError_t launch_reorder_rows(const uint16_t *embed, long long ld, const int32_t *ordering, int V, int H,
-                                uint16_t *out, uint32_t *ctrl, cudaStream_t s)
-{
-    const int per_sm = blocks_per_sm((const void *)k_reorder_rows, 256, 0);
-    const long long need = ((long long)V + 7) / 8;
-    const long long grid = std::min<long long>(need, (long long)sm_count() * (per_sm > 0 ? per_sm : 1));
-    k_reorder_rows<<<(int)grid, 256, 0, s>>>(embed, ld, ordering, V, H, out, ctrl);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s)

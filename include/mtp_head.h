@@ -100,16 +100,16 @@ typedef enum mtp_status {
  *   cluster_offsets  int32 [C+1] ascending, off[0] = 0, off[C] = V: centroid c owns
  *                    positions [off[c], off[c+1]); empty clusters are allowed.  NULL
  *                    means uniform clusters of V/C positions (the page's layout).
- *   embed_ordered    optional bf16 [V, ld_embed], 16-byte aligned: the embedding rows in
- *                    ordered-position order, row p = embed_w row token_ordering[p] (see
- *                    mtp_reorder_embeddings).  When set, the masked calls read every
- *                    selected cluster's candidate rows as one contiguous block instead of
- *                    gathering them row by row, which lets more calls run the tensor-core
- *                    gather; token ids are the same either way and logits agree within
- *                    fp32 summation-order rounding (bit for bit when the same gather
- *                    kernel runs).  NULL: gather from embed_w (the page's layout).  It
- *                    must match embed_w and token_ordering; the library does not check
- *                    that. */
+ *   embed_packed     optional packed copy of the embedding table built by
+ *                    mtp_pack_embeddings (layout below), 256-byte aligned.  When set,
+ *                    the masked calls that run the tensor-core gather read each chunk's
+ *                    candidate rows as contiguous 4 KB blocks instead of gathering
+ *                    them row by row, and the library routes more calls there.  Token
+ *                    ids are the same either way; logits agree within fp32 rounding
+ *                    of the summation order (bit for bit when the same gather kernel
+ *                    runs).  NULL: gather from embed_w (the page's layout).  It must
+ *                    have been packed from this descriptor's tables; the library does
+ *                    not check that. */
 typedef struct mtp_head_desc {
     int32_t vocab_size;
     int32_t hidden_size;
@@ -122,7 +122,7 @@ typedef struct mtp_head_desc {
     int64_t ld_embed;
     const int32_t *token_ordering;
     const int32_t *cluster_offsets;
-    const void *embed_ordered;
+    const void *embed_packed;
 } mtp_head_desc;
 
 /* Bytes of device workspace that the masked calls and the dense head's argmax
@@ -196,18 +196,45 @@ MTP_API mtp_status mtp_masked_topk_tokens_noalloc(const mtp_head_desc *desc, con
                                                   int32_t batch, int32_t *out_tokens,
                                                   float *out_max, void *stream);
 
-/* Build the cluster-ordered embedding table: row p of embed_ordered_out = row
- * token_ordering[p] of desc->embed_w, for p < V (first H elements of each row;
- * the row stride of the output is desc->ld_embed).  A one-time layout step
- * (V * H * 2 bytes read and written); the result may then be passed as
- * desc->embed_ordered.  The page gathers from the token-order table on every
- * call; the ordered copy turns that gather into contiguous reads per cluster.
- *   embed_ordered_out  bf16 [V, ld_embed] device buffer, 16-byte aligned, not
- *                      overlapping embed_w
- * Token ids outside [0, V) are skipped (their rows are left unwritten) and set
- * MTP_DEVERR_TOKEN_RANGE in *workspace's error word if workspace is non-NULL. */
-MTP_API mtp_status mtp_reorder_embeddings(const mtp_head_desc *desc, void *embed_ordered_out,
-                                          void *workspace, void *stream);
+/* The packed embedding table: the rows of each cluster in ordered-position
+ * order, cut into the operand tiles of the tensor-core gather.  This is a
+ * layout of this library (the page gathers from the token-order table on every
+ * call); building it is a one-time step, like loading the weights.
+ *
+ * Layout, with KB = ceil(H / 64) k-blocks of 64 elements:
+ *   - cluster c is padded to P(c) = roundup(size(c), 32) positions; padded
+ *     cluster offsets poff[c] = P(0) + ... + P(c-1); padded position q of
+ *     cluster c (q < size(c)) is the embedding row of token_ordering[off[c] + q];
+ *   - padded positions 128s .. 128s+127 (super-group s) and k-block kb form one
+ *     16384-byte block at byte offset (s * KB + kb) * 16384: its row r (0..127)
+ *     holds elements kb*64 .. kb*64+63 of padded position 128s + r (zeros for
+ *     padding rows and for elements at or beyond H), with the 16-byte piece j
+ *     (elements j*8 .. j*8+7) stored at r*128 + ((j XOR (r mod 8)) * 16), the
+ *     128-byte swizzle the tensor cores read;
+ *   - after the blocks (SG = ceil(groups / 4) super-groups, groups the bound
+ *     below): int32 poff[0..C].
+ * mtp_packed_embeddings_bytes gives the size for the descriptor's shapes: with
+ * uniform clusters exactly C * ceil(S/32) groups of 32, with explicit cluster
+ * offsets the upper bound ceil((V + 31 C) / 32) groups; 0 for an invalid
+ * descriptor. */
+MTP_API size_t mtp_packed_embeddings_bytes(const mtp_head_desc *desc);
+
+/* Fill `packed` (packed_bytes >= mtp_packed_embeddings_bytes(desc), 256-byte
+ * aligned, not overlapping the tables) from desc->embed_w, token_ordering and
+ * cluster_offsets.  Reads V*H*2 bytes and writes the packed size; asynchronous on
+ * `stream`.  Token ids outside [0, V) become zero rows and, like invalid cluster
+ * offsets (clusters then count as empty), set MTP_DEVERR_TOKEN_RANGE /
+ * MTP_DEVERR_OFFSETS in *workspace's error word when workspace is non-NULL
+ * (16-byte aligned, at least 64 bytes; the word is not cleared first). */
+MTP_API mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, size_t packed_bytes,
+                                       void *workspace, void *stream);
+
+/* Which gather kernel a masked call with this descriptor and batch runs: 1 for
+ * the tensor-core gather (large buckets, or the packed table over uniform
+ * clusters with at least C row-cluster pairs), 0 for the CUDA-core gather, a
+ * negative mtp_status for an invalid descriptor or batch.  Host-only; for
+ * profiling and benchmarks (the calls choose by themselves). */
+MTP_API int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch);
 
 /* Enqueue an asynchronous copy of the workspace's device error word (a set of
  * MTP_DEVERR_* bits, reset by each masked call) into *host_word; the value is

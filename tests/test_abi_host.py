@@ -121,22 +121,56 @@ def test_dense_and_scores_reject_bad_arguments(L):
     assert L.mtp_profile_events(0, None, None) == 0
 
 
-def test_ordered_table_checks(L):
-    # the optional cluster-ordered table must be 16-byte aligned like the embedding table
+def test_packed_table_sizes_and_checks(L):
+    # uniform clusters of 128: no padding, exactly V*H*2 bytes of blocks + poff[C+1]
     d = _desc()
-    d.embed_ordered = 0xA004
+    assert L.mtp_packed_embeddings_bytes(ctypes.byref(d)) == 262144 * 1536 * 2 + 2049 * 4
+    # explicit offsets: bound with 31 padding rows per cluster
+    d = _desc(offsets=0x5000)
+    groups = (262144 + 31 * 2048 + 31) // 32
+    assert L.mtp_packed_embeddings_bytes(ctypes.byref(d)) == (groups + 3) // 4 * 24 * 16384 + 2049 * 4
+    # a K tail (H = 72: two k-blocks) and clusters of 40 (two groups of 32 each): 16 groups
+    # make 4 blocks of 128 rows per k-block
+    d = _desc(V=40 * 8, H=72, C=8, K=2)
+    assert L.mtp_packed_embeddings_bytes(ctypes.byref(d)) == 4 * 2 * 16384 + 9 * 4
+    d = _desc(V=40 * 9, H=72, C=9, K=2)   # 18 groups -> 5 super-groups
+    assert L.mtp_packed_embeddings_bytes(ctypes.byref(d)) == 5 * 2 * 16384 + 10 * 4
+    assert L.mtp_packed_embeddings_bytes(ctypes.byref(_desc(H=12))) == 0
+    assert L.mtp_packed_embeddings_bytes(None) == 0
+    # the packed table must be 256-byte aligned when attached
+    d = _desc()
+    d.embed_packed = 0xA010
     out = ctypes.c_void_p(0x8000)
     assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 1 << 30, None) == -3
-    # building it: null, misaligned and overlapping tables are refused before any launch
-    d = _desc(V=1024, H=64, ew=0x100000)
-    assert L.mtp_reorder_embeddings(ctypes.byref(d), None, None, None) == -1
-    assert L.mtp_reorder_embeddings(None, ctypes.c_void_p(0x800000), None, None) == -1
-    assert L.mtp_reorder_embeddings(ctypes.byref(_desc(V=1024, H=64, ordering=None)),
-                                    ctypes.c_void_p(0x800000), None, None) == -1
-    assert L.mtp_reorder_embeddings(ctypes.byref(d), ctypes.c_void_p(0x800008), None, None) == -3
-    assert L.mtp_reorder_embeddings(ctypes.byref(d), ctypes.c_void_p(0x800000),
-                                    ctypes.c_void_p(0x9004), None) == -3
-    # [V, H] bf16 at 0x100000 spans 128 KiB: an output inside that range overlaps it
-    assert L.mtp_reorder_embeddings(ctypes.byref(d), ctypes.c_void_p(0x110000), None, None) == -2
-    assert L.mtp_reorder_embeddings(ctypes.byref(_desc(V=1024, H=12, ew=0x100000)),
-                                    ctypes.c_void_p(0x800000), None, None) == -2
+    # building it: null, misaligned, small and overlapping buffers are refused before any launch
+    d = _desc(V=1024, H=64, C=16, ew=0x100000)
+    need = L.mtp_packed_embeddings_bytes(ctypes.byref(d))
+    big = ctypes.c_void_p(0x4000000)
+    assert L.mtp_pack_embeddings(ctypes.byref(d), None, need, None, None) == -1
+    assert L.mtp_pack_embeddings(None, big, need, None, None) == -1
+    assert L.mtp_pack_embeddings(ctypes.byref(_desc(V=1024, H=64, C=16, ordering=None)), big, need,
+                                 None, None) == -1
+    assert L.mtp_pack_embeddings(ctypes.byref(d), ctypes.c_void_p(0x4000010), need, None, None) == -3
+    assert L.mtp_pack_embeddings(ctypes.byref(d), big, need, ctypes.c_void_p(0x9004), None) == -3
+    assert L.mtp_pack_embeddings(ctypes.byref(d), big, need - 1, None, None) == -4
+    # [V, H] bf16 at 0x100000 spans 128 KiB: a packed buffer starting inside it overlaps
+    assert L.mtp_pack_embeddings(ctypes.byref(d), ctypes.c_void_p(0x110000), need, None, None) == -2
+    assert L.mtp_pack_embeddings(ctypes.byref(_desc(V=1000, H=64, C=16, ew=0x100000)), big, need,
+                                 None, None) == -2
+
+
+def test_gather_plan(L):
+    d = _desc()
+    assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0      # B*K = C: CUDA-core gather
+    assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1     # B*K = 4C: large buckets
+    assert L.mtp_gather_plan(ctypes.byref(d), 0) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), -1) == -2
+    assert L.mtp_gather_plan(ctypes.byref(d), 2000) == -6
+    assert L.mtp_gather_plan(ctypes.byref(_desc(K=0)), 8) == -2
+    d.embed_packed = 0xA000                                  # packed table, uniform clusters
+    assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 0
+    d = _desc(offsets=0x5000)                                # ragged clusters: only large buckets
+    d.embed_packed = 0xA000
+    assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1

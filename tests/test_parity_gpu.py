@@ -321,11 +321,12 @@ def test_padded_table_and_identity_ordering(build_lib):
     _full_check(m, oh, dh, hidden, "padded")
 
 
+@pytest.mark.parametrize("packed", [False, True])
 @pytest.mark.parametrize("B,K", [(12, 3), (32, 8)])
-def test_integer_inputs_bit_exact_with_ties(build_lib, B, K):
+def test_integer_inputs_bit_exact_with_ties(build_lib, B, K, packed):
     """Small-integer inputs make every sum exact in fp32 and fp64: logits must be
     bit-identical, and forced ties exercise both tie-break rules.  B*K >= 4C sends
-    the second case through the tensor-core gather."""
+    the second case through the tensor-core gather; with the packed table both do."""
     m = build_lib
     g = np.random.default_rng(11)
     V, C, H = 512, 16, 64
@@ -342,6 +343,8 @@ def test_integer_inputs_bit_exact_with_ties(build_lib, B, K):
     oh = oracle.Head(cwb, ewb, perm, None, K)
     dh = m.MaskedHead(helpers.bf16_tensor(cwb), helpers.bf16_tensor(ewb),
                       torch.from_numpy(perm).cuda(), K)
+    if packed:
+        dh.use_packed_table()
     h = helpers.bf16_tensor(hb)
     scores, topk = m.mtp_centroid_scores(dh, h)
     tok, mx = m.mtp_masked_topk_tokens(dh, h)
@@ -492,35 +495,87 @@ def test_empty_batch_is_noop(build_lib):
 
 
 # ---------------------------------------------------------------------------
-# the cluster-ordered copy of the embedding table
+# the packed embedding table (tensor-core gather operand tiles)
 
 
-def test_reorder_embeddings_is_the_ordering_gather(build_lib):
-    """Row p of the ordered copy is embedding row token_ordering[p] (first H columns;
-    the row stride is the table's, padding columns are not written)."""
+def _unpack(packed, V, H, C, sizes):
+    """The packed layout read back with numpy: (padded table [poff[C], H], poff [C+1])."""
+    KB = (H + 63) // 64
+    if sizes is None:
+        groups = C * ((V // C + 31) // 32)
+    else:
+        groups = (V + 31 * C + 31) // 32
+    SG = (groups + 3) // 4
+    off = SG * KB * 16384
+    buf = packed.cpu().numpy()
+    poff = buf[off:off + 4 * (C + 1)].view(np.int32)
+    blocks = buf[:off].reshape(SG, KB, 128, 8, 16)
+    r = np.arange(128)[:, None]
+    j = np.arange(8)[None, :]
+    un = blocks[:, :, r, j ^ (r & 7)]                        # undo the 128-byte swizzle
+    rows = un.reshape(SG, KB, 128, 128).view(np.uint16)      # [SG, KB, 128, 64]
+    table = rows.transpose(0, 2, 1, 3).reshape(SG * 128, KB * 64)[:int(poff[-1])]
+    assert not table[:, H:].any(), "elements past H must be zero"
+    return table[:, :H], poff
+
+
+@pytest.mark.parametrize("H,sizes", [(264, "ragged"), (128, None)])
+def test_pack_embeddings_layout(build_lib, H, sizes):
     m = build_lib
-    t, oh, dh = _custom(m, 4096, 128, 64, 5, seed=31, pad_rows=64, pad_cols=8)
-    ordered = dh.use_ordered_table()
-    torch.cuda.synchronize()
-    got = ordered.view(torch.int16).cpu().numpy().view(np.uint16)
-    np.testing.assert_array_equal(got[:, :128], t.embed_w[t.token_ordering])
+    if sizes == "ragged":
+        sz = [0] * 5 + [1, 2, 3] + [700, 1] + [37] * 20 + [0, 19]
+        t, oh, dh = _custom(m, int(sum(sz)), H, len(sz), 6, seed=77, sizes=sz, pad_cols=8)
+        sizes = np.array(sz)
+    else:
+        t, oh, dh = _custom(m, 4096, H, 64, 5, seed=21)
+        sizes = None
+    V, C = oh.V, t.centroid_w.shape[0]
+    ws = dh.workspace(1)
+    ws.zero_()
+    n = m.mtp_packed_embeddings_bytes(dh)
+    packed = torch.full((n,), 0xAB, dtype=torch.uint8, device="cuda")
+    m.mtp_pack_embeddings(dh, packed, workspace=ws)
+    assert m.mtp_read_device_error(ws) == 0
+    table, poff = _unpack(packed, V, H, C, sizes)
+    off = t.cluster_offsets if t.cluster_offsets is not None else np.arange(C + 1) * (V // C)
+    size = np.diff(off)
+    np.testing.assert_array_equal(poff, np.concatenate([[0], np.cumsum((size + 31) // 32 * 32)]))
+    ew = t.embed_w[:, :H]
+    for c in range(C):
+        blk = table[poff[c]:poff[c + 1]]
+        np.testing.assert_array_equal(blk[:size[c]], ew[t.token_ordering[off[c]:off[c + 1]]])
+        assert not blk[size[c]:].any(), f"cluster {c}: padding rows must be zero"
 
 
-def test_reorder_embeddings_flags_bad_token_ids(build_lib):
+def test_pack_embeddings_flags_bad_inputs(build_lib):
     m = build_lib
     t, oh, dh = _custom(m, 1024, 64, 16, 4, seed=5)
     bad = t.token_ordering.copy()
     bad[10] = 1024 + 7
     dbad = m.MaskedHead(dh.centroid_w, dh.embed_w, torch.from_numpy(bad).cuda(), 4, vocab_size=1024)
     ws = dbad.workspace(1)
-    ws[:64].zero_()
-    out = torch.zeros(1024, 64, dtype=torch.bfloat16, device="cuda")
-    m.mtp_reorder_embeddings(dbad, out, workspace=ws)
+    ws.zero_()
+    packed = dbad.use_packed_table()
+    m.mtp_pack_embeddings(dbad, packed, workspace=ws)
     assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_TOKEN_RANGE
-    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    table, _ = _unpack(packed, 1024, 64, 16, None)
     keep = np.arange(1024) != 10
-    np.testing.assert_array_equal(got[keep], t.embed_w[bad[keep]])
-    assert not got[10].any()   # the bad row is left as it was
+    np.testing.assert_array_equal(table[keep], t.embed_w[bad[keep]])
+    assert not table[10].any()   # the bad id becomes a zero row
+    # overlapping clusters (each in range on its own) whose padded sizes overflow the
+    # table's bound: flagged, every cluster recorded as empty, and later calls read nothing
+    off = np.array([0, 1024] * 8 + [1024], dtype=np.int32)
+    dov = m.MaskedHead(dh.centroid_w, dh.embed_w, dh.token_ordering, 4, torch.from_numpy(off).cuda(),
+                       vocab_size=1024)
+    ws2 = dov.workspace(64)
+    ws2.zero_()
+    p2 = torch.empty(m.mtp_packed_embeddings_bytes(dov), dtype=torch.uint8, device="cuda")
+    m.mtp_pack_embeddings(dov, p2, workspace=ws2)
+    assert m.mtp_read_device_error(ws2) & m.MTP_DEVERR_OFFSETS
+    dov.use_packed_table(p2)
+    h = helpers.bf16_tensor(synth.random_hidden(64, 64, 3))
+    m.mtp_masked_topk_tokens(dov, h, workspace=ws2)
+    assert m.mtp_read_device_error(ws2) & m.MTP_DEVERR_OFFSETS
 
 
 def _same_outputs(m, dh, h):
@@ -531,13 +586,14 @@ def _same_outputs(m, dh, h):
 
 
 @pytest.mark.parametrize("H,B,sizes", [
-    (264, 7, None),                # CUDA-core gather
-    (264, 64, None),               # tensor-core gather (B*K >= 4C), K tail
-    (64, 41, "ragged"),            # empty and oversized clusters, last cluster at the table's end
+    (264, 7, None),                # few pairs: the CUDA-core gather either way
+    (264, 64, None),               # large buckets: the tensor-core gather either way, K tail
+    (264, 4, None),                # B*K = C: packed -> tensor cores, token order -> CUDA cores
+    (64, 41, "ragged"),            # empty and oversized clusters, padding groups, table end
 ])
-def test_ordered_table_parity(build_lib, H, B, sizes):
-    """With the ordered copy attached, every finish matches the oracle and is bit-identical
-    to the token-order path: at these sizes both run the same gather kernel."""
+def test_packed_table_parity(build_lib, H, B, sizes):
+    """With the packed table attached every finish matches the oracle; where both
+    layouts run the same gather kernel the outputs are bit-identical."""
     m = build_lib
     if sizes == "ragged":
         sz = [0] * 5 + [1, 2, 3] + [700, 1] + [37] * 20 + [0, 19]
@@ -547,37 +603,39 @@ def test_ordered_table_parity(build_lib, H, B, sizes):
     hidden = synth.random_hidden(B, H, H + 6)
     h = helpers.bf16_tensor(hidden)
     base = _same_outputs(m, dh, h)
-    dh.use_ordered_table()
+    dh.use_packed_table()
     try:
-        _full_check(m, oh, dh, hidden, f"ordered H={H} B={B}")
+        _full_check(m, oh, dh, hidden, f"packed H={H} B={B}")
         got = _same_outputs(m, dh, h)
-        for a, b in zip(base, got):
-            assert torch.equal(a, b)
+        same_kernel = B * 8 >= 4 * 32 or B * 8 < 32
+        if same_kernel and sizes is None:
+            for a, b in zip(base, got):
+                assert torch.equal(a, b)
+        else:
+            np.testing.assert_array_equal(got[0].cpu().numpy(), base[0].cpu().numpy())
+            helpers.assert_close(got[2].cpu().numpy(), base[2].cpu().numpy(), "packed vs token order")
     finally:
-        dh.drop_ordered_table()
+        dh.drop_packed_table()
 
 
-@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64), ("uniform", 8)])
-def test_ordered_table_full_size(build_lib, name, B):
-    """Full-size tables with the ordered copy: the call may now run the other gather
-    kernel (the tensor cores sum in another order), so token ids must match exactly and
-    logits within the fp32 tolerance, against the oracle and the token-order path."""
+@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64), ("uniform", 8), ("variable", 64)])
+def test_packed_table_full_size(build_lib, name, B):
+    """Full-size tables with the packed table: token ids match the oracle and the
+    token-order path exactly, logits within the fp32 tolerance (the packed call may run
+    the tensor-core gather where the token-order call runs the CUDA-core one)."""
     m = build_lib
     oh, dh = device_head(m, name)
     hidden, ref, _ = helpers.clean_batch(name, oh, B)
     h = helpers.bf16_tensor(hidden)
     base = _same_outputs(m, dh, h)
-    dh.use_ordered_table()
+    dh.use_packed_table()
     try:
         got = _same_outputs(m, dh, h)
         np.testing.assert_array_equal(got[0].cpu().numpy(), ref["tokens"])
         np.testing.assert_array_equal(got[0].cpu().numpy(), base[0].cpu().numpy())
-        helpers.assert_close(got[1].cpu().numpy(), ref["max_logit"], f"ordered {name} max")
+        helpers.assert_close(got[1].cpu().numpy(), ref["max_logit"], f"packed {name} max")
         sc = got[2].cpu().numpy()
-        sref = oracle.masked_scatter_logits(oh, hidden[:8]) if B > 8 else None
-        if sref is not None:
-            helpers.assert_close(sc[:8], sref, f"ordered {name} scatter")
-        helpers.assert_close(sc, base[2].cpu().numpy(), f"ordered {name} scatter vs token order")
-        assert np.array_equal(np.isfinite(sc), np.isfinite(base[2].cpu().numpy()))
+        helpers.assert_close(sc[:4], oracle.masked_scatter_logits(oh, hidden[:4]), f"packed {name} scatter")
+        helpers.assert_close(sc, base[2].cpu().numpy(), f"packed {name} scatter vs token order")
     finally:
-        dh.drop_ordered_table()
+        dh.drop_packed_table()
