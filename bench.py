@@ -144,6 +144,16 @@ def barrier(ws):
         dist.barrier()
 
 
+def rank_row0(rank):
+    """First hidden-row index of a rank's batches: every replica draws its own rows."""
+    return rank * 100000
+
+
+def job_tokens_per_s(ws, batch_per_rank, slowest_call_ms):
+    """Whole-job rate: the rows all ranks processed per call, over the slowest rank's time."""
+    return ws * batch_per_rank / (slowest_call_ms * 1e-3)
+
+
 def max_over_ranks(x, ws, device=None):
     """The maximum of a float over all ranks (the slowest rank sets the time)."""
     if ws <= 1:
@@ -392,10 +402,10 @@ def gpu_main(args):
                               "kernels_us": r["kernels_us"], "device_error": r["device_error"]}))
         return
     sampler = ClockSampler(uuid) if rank == 0 else None
-    res = measure_masked(ctx, t, dh, name, B, args.steps, args.warmup, row0=rank * 100000)
+    res = measure_masked(ctx, t, dh, name, B, args.steps, args.warmup, row0=rank_row0(rank))
     clocks = sampler.stop(res["t0"], res["t1"]) if sampler else None
     call_ms = max_over_ranks(res["call_ms"], ws, device)
-    value = ws * B / (call_ms * 1e-3)
+    value = job_tokens_per_s(ws, B, call_ms)
     kern_s = res["kernel_ms"] * 1e-3
     achieved = res["bytes"]["gather"] / kern_s / 1e9
     plan = m.mtp_gather_plan(dh, B)

@@ -1,0 +1,79 @@
+"""The multi-replica path of bench.py on CPU: two gloo ranks on 127.0.0.1.
+
+Rows are independent, so N GPUs run N replicas with no collective on the data
+path; what the ranks share is the timing: a barrier on both sides of the timed
+loop, the slowest rank's time (all-reduce max) and the whole-job rate.  The
+reference arm runs on rank 0 only.  No GPU is used."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method="env://", rank=rank, world_size=ws)
+    try:
+        got_ws, got_rank, _ = bench.dist_setup()
+        bench.barrier(got_ws)
+        # each rank's call time differs; the job is as slow as its slowest rank
+        call_ms = 0.1 + 0.05 * rank
+        slowest = bench.max_over_ranks(call_ms, got_ws)
+        value = bench.job_tokens_per_s(got_ws, 64, slowest)
+        bench.barrier(got_ws)
+        q.put((got_rank, got_ws, slowest, value, bench.rank_row0(got_rank)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_share_barrier_and_slowest_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert [r[0] for r in res] == [0, 1] and all(r[1] == 2 for r in res)
+    # both ranks see the slowest time (0.15 ms) and the same whole-job rate: 2 x 64 rows / 0.15 ms
+    for r in res:
+        assert r[2] == pytest.approx(0.15)
+        assert r[3] == pytest.approx(2 * 64 / 0.15e-3)
+    # the replicas draw disjoint hidden rows
+    assert res[0][4] != res[1][4]
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+           "--steps", "2", "--warmup", "3"]
+    r1 = subprocess.run(cmd, env=env, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    env.update(RANK="0", LOCAL_RANK="0")
+    r0 = subprocess.run(cmd, env=env, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r0.returncode == 0, r0.stderr[-2000:]
+    line = json.loads(r0.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
