@@ -295,6 +295,30 @@ def measure_masked(ctx, t, dh, name, B, steps, warmup, scatter=False, rot=4, row
                 max_call_us=round(float(np.max(call)) * 1e3, 2), device_error=dev_err)
 
 
+def measure_graph(ctx, t, dh, name, B, steps, warmup, rot=4, row0=0):
+    """µs per call replaying a CUDA graph of the call (the batch copied into the graph's
+    static input inside the timed region), on a side stream: the legacy stream cannot be
+    captured."""
+    torch, m, synth, timer = ctx["torch"], ctx["m"], ctx["synth"], ctx["timer"]
+    hb = make_batches(synth, t, name, B, rot, row0)
+    hs = [torch.from_numpy(h.view(np.int16)).to(ctx["device"]).view(torch.bfloat16) for h in hb]
+    gs = torch.cuda.Stream(device=ctx["device"])
+    gs.wait_stream(torch.cuda.current_stream(ctx["device"]))
+    with torch.cuda.stream(gs):
+        g = m.CapturedCalls(dh, sizes=(B,))
+        try:
+            call, _, _, _ = timer.run(lambda i: g(hs[i % rot]), steps, warmup, ws=ctx["ws"])
+            # replay alone: the producer of the hidden states wrote them into the static input
+            g.hidden[:B].copy_(hs[0])
+            bare, _, _, _ = timer.run(lambda i: g.replay(B), steps, warmup, ws=ctx["ws"])
+            err = m.mtp_read_device_error(g.ws, stream=gs)
+        finally:
+            gs.synchronize()
+            g.close()
+    torch.cuda.current_stream(ctx["device"]).wait_stream(gs)
+    return float(np.mean(call)), float(np.mean(bare)), err
+
+
 def measure_dense(ctx, t, dh, B, steps, warmup):
     torch, m, synth, timer = ctx["torch"], ctx["m"], ctx["synth"], ctx["timer"]
     h = torch.from_numpy(synth.hidden_batch("scatter", B).view(np.int16)).to(ctx["device"]).view(
@@ -448,8 +472,12 @@ def gpu_main(args):
                                row0=40000 + b)
             ach = r["bytes"]["gather"] / (r["kernel_ms"] * 1e-3) / 1e9
             cg = r["bytes"]["call"] / (r["call_ms"] * 1e-3) / 1e9
+            g_ms, g_bare_ms, g_err = measure_graph(ctx, t, dh, name, b, max(20, args.steps // 4),
+                                                   args.warmup, row0=40000 + b)
             sweep[str(b)] = {"gather_kernel": m.mtp_gather_plan(dh, b),
                              "us_per_call": round(r["call_ms"] * 1e3, 2),
+                             "graph_us_per_call": round(g_ms * 1e3, 2),
+                             "graph_replay_only_us": round(g_bare_ms * 1e3, 2), "graph_device_error": g_err,
                              "tokens_per_s": round(b / (r["call_ms"] * 1e-3), 1),
                              "gather_us": round(r["kernel_ms"] * 1e3, 2),
                              "gather_gbs": round(ach, 1), "gather_frac": round(ach / hbm, 4),

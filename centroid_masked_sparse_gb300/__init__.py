@@ -20,7 +20,7 @@ import ctypes
 from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_MAX_BATCH,
                    MtpError, MtpHeadDesc, check, lib)
 
-__all__ = ["MaskedHead", "MtpError", "mtp_workspace_bytes", "mtp_centroid_scores",
+__all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "mtp_workspace_bytes", "mtp_centroid_scores",
            "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_dense_lm_head",
            "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
            "MTP_DEVERR_TOKEN_RANGE",
@@ -225,6 +225,98 @@ def mtp_gather_plan(head, batch: int) -> str:
     if r < 0:
         check(r, "mtp_gather_plan")
     return "tensor_core" if r == 1 else "cuda_core"
+
+
+MTP_FINISH_ARGMAX, MTP_FINISH_SCATTER = 0, 1
+
+
+class CapturedCalls:
+    """The sparse argmax (or scatter) recorded as one CUDA graph per batch size.
+
+    Like the fixed-size graphs the proposer keeps for get_top_tokens: each call copies
+    the batch into a static input (zero-initialised, so padding rows are finite),
+    replays the graph of the smallest captured size >= B and returns views of the
+    first B outputs.  Batches above the largest size run the eager call.  Outputs
+    are overwritten by the next call; all graphs share one workspace and run on the
+    stream they were captured on (the current stream at construction by default).
+    """
+
+    def __init__(self, head, sizes=(1, 2, 4, 8, 16, 32, 64), finish="argmax", stream=None):
+        torch = _torch()
+        self.head, self.finish = head, finish
+        self.sizes = sorted(int(b) for b in sizes)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(head.device)
+        if self.stream.cuda_stream == 0:
+            raise ValueError("graph capture needs a created stream, not the legacy default stream")
+        top = self.sizes[-1]
+        dev = head.device
+        self.hidden = torch.zeros(top, head.hidden_size, dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(mtp_workspace_bytes(head, top), dtype=torch.uint8, device=dev)
+        if finish == "argmax":
+            self.out0 = torch.empty(top, dtype=torch.int32, device=dev)
+            self.out1 = torch.empty(top, dtype=torch.float32, device=dev)
+            code = MTP_FINISH_ARGMAX
+        elif finish == "scatter":
+            self.out0 = torch.empty(top, head.vocab_size, dtype=torch.float32, device=dev)
+            self.out1 = None
+            code = MTP_FINISH_SCATTER
+        else:
+            raise ValueError(finish)
+        self.graphs = {}
+        try:
+            for b in self.sizes:
+                h = ctypes.c_void_p()
+                check(lib().mtp_graph_capture(ctypes.byref(head.desc), code, _ptr(self.hidden), b,
+                                              _ptr(self.out0), _ptr(self.out1), _ptr(self.ws),
+                                              self.ws.numel(), ctypes.c_void_p(self.stream.cuda_stream),
+                                              ctypes.byref(h)), "mtp_graph_capture")
+                self.graphs[b] = h
+        except Exception:
+            self.close()
+            raise
+
+    def size_for(self, batch):
+        for b in self.sizes:
+            if b >= batch:
+                return b
+        return None
+
+    def replay(self, batch):
+        """Replay for a batch already written into self.hidden[:batch] (no copy)."""
+        size = self.size_for(batch)
+        if size is None:
+            raise ValueError(f"batch {batch} is above the largest captured size {self.sizes[-1]}")
+        check(lib().mtp_graph_launch(self.graphs[size], ctypes.c_void_p(self.stream.cuda_stream)),
+              "mtp_graph_launch")
+        if self.finish == "argmax":
+            return self.out0[:batch], self.out1[:batch]
+        return self.out0[:batch]
+
+    def __call__(self, hidden):
+        B = _hidden_ok(self.head, hidden)
+        size = self.size_for(B)
+        with _torch().cuda.stream(self.stream):
+            if size is None:   # above the largest graph: the eager call
+                if self.finish == "argmax":
+                    return mtp_masked_topk_tokens(self.head, hidden)
+                return mtp_masked_scatter_logits(self.head, hidden)
+            self.hidden[:B].copy_(hidden)
+            check(lib().mtp_graph_launch(self.graphs[size], ctypes.c_void_p(self.stream.cuda_stream)),
+                  "mtp_graph_launch")
+        if self.finish == "argmax":
+            return self.out0[:B], self.out1[:B]
+        return self.out0[:B]
+
+    def close(self):
+        for h in self.graphs.values():
+            lib().mtp_graph_destroy(h)
+        self.graphs = {}
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
 
 
 def mtp_read_device_error(workspace, stream=None) -> int:

@@ -179,13 +179,18 @@ int proj_rows_per_group(int B, int H)
 struct Prof {
     int id;
     cudaStream_t s;
-    Prof(int id_, cudaStream_t s_) : id(id_), s(s_)
+    bool on;
+    Prof(int id_, cudaStream_t s_) : id(id_), s(s_), on(false)
     {
-        if (g_prof[id][0]) cudaEventRecord((cudaEvent_t)g_prof[id][0], s);
+        if (!g_prof[id][0] && !g_prof[id][1]) return;
+        // never record the profiling events into a graph being captured
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        on = cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
+        if (on && g_prof[id][0]) cudaEventRecord((cudaEvent_t)g_prof[id][0], s);
     }
     ~Prof()
     {
-        if (g_prof[id][1]) cudaEventRecord((cudaEvent_t)g_prof[id][1], s);
+        if (on && g_prof[id][1]) cudaEventRecord((cudaEvent_t)g_prof[id][1], s);
     }
 };
 

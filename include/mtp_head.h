@@ -229,6 +229,39 @@ MTP_API size_t mtp_packed_embeddings_bytes(const mtp_head_desc *desc);
 MTP_API mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, size_t packed_bytes,
                                        void *workspace, void *stream);
 
+/* CUDA graphs of the masked calls.  Gemma4Proposer._setup_centroids_cuda_graphs
+ * ("Add Gemma4 MTP speculative decoding with centroids masking", vLLM
+ * spec_decode/gemma4.py) records get_top_tokens at fixed batch sizes so that a
+ * draft step replays one graph instead of launching its kernels one by one.
+ * mtp_graph_capture does the same for one call with fixed buffers: it runs the
+ * call once eagerly on `stream` (argument checks, one-time per-device setup),
+ * then records it (cudaStreamBeginCapture in thread-local mode) and instantiates
+ * the graph.  Every pointer (desc tables, hidden, outputs, workspace) is baked
+ * in: a replay reads the buffers' contents at replay time, so the caller copies
+ * each new batch into `hidden` before mtp_graph_launch.  The descriptor struct
+ * itself is not kept.
+ *   finish   MTP_FINISH_ARGMAX: out0 = int32 out_tokens [batch], out1 = float
+ *            out_max [batch] or NULL (mtp_masked_topk_tokens);
+ *            MTP_FINISH_SCATTER: out0 = float out_logits [batch, V], out1 unused
+ *            (mtp_masked_scatter_logits)
+ *   stream   a created stream (capture is impossible on the legacy stream: NULL
+ *            returns MTP_ERR_NULL)
+ *   graph    receives an opaque handle owned by the caller (mtp_graph_destroy)
+ * Replays of one graph on several streams at once race on its workspace.  The
+ * eager call's statuses apply; a failed capture returns MTP_ERR_CUDA and leaves
+ * *graph NULL. */
+#define MTP_FINISH_ARGMAX 0
+#define MTP_FINISH_SCATTER 1
+typedef struct mtp_graph mtp_graph;
+MTP_API mtp_status mtp_graph_capture(const mtp_head_desc *desc, int32_t finish, const void *hidden,
+                                     int32_t batch, void *out0, void *out1, void *workspace,
+                                     size_t workspace_bytes, void *stream, mtp_graph **graph);
+/* Enqueue one replay of the recorded call on `stream` (any stream of the graph's device). */
+MTP_API mtp_status mtp_graph_launch(const mtp_graph *graph, void *stream);
+/* Free the graph (NULL is a no-op).  The caller must not destroy a graph whose
+ * replay is still in flight. */
+MTP_API mtp_status mtp_graph_destroy(mtp_graph *graph);
+
 /* Which gather kernel a masked call with this descriptor and batch runs: 1 for
  * the tensor-core gather (large buckets, or the packed table over uniform
  * clusters with at least C row-cluster pairs), 0 for the CUDA-core gather, a

@@ -174,3 +174,23 @@ def test_gather_plan(L):
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1
+
+
+def test_graph_capture_rejects_bad_arguments(L):
+    d = _desc()
+    g = ctypes.c_void_p(0x1234)
+    out = ctypes.c_void_p(0x8000)
+    assert L.mtp_graph_capture(ctypes.byref(d), 0, FAKE, 4, out, None, WS, 1 << 30, None,
+                               ctypes.byref(g)) == -1          # the legacy stream cannot be captured
+    assert g.value is None                                    # *graph is cleared on every failure
+    st = ctypes.c_void_p(0x77)
+    assert L.mtp_graph_capture(ctypes.byref(d), 2, FAKE, 4, out, None, WS, 1 << 30, st,
+                               ctypes.byref(g)) == -2          # unknown finish
+    assert L.mtp_graph_capture(ctypes.byref(d), 0, FAKE, 0, out, None, WS, 1 << 30, st,
+                               ctypes.byref(g)) == -2          # nothing to record
+    assert L.mtp_graph_capture(ctypes.byref(d), 0, FAKE, 4, out, None, WS, 1 << 30, st, None) == -1
+    # the eager call's own checks come first (misaligned hidden states)
+    assert L.mtp_graph_capture(ctypes.byref(d), 0, ctypes.c_void_p(0x7002), 4, out, None, WS,
+                               1 << 30, st, ctypes.byref(g)) == -3
+    assert L.mtp_graph_launch(None, None) == -1
+    assert L.mtp_graph_destroy(None) == 0

@@ -639,3 +639,70 @@ def test_packed_table_full_size(build_lib, name, B):
         helpers.assert_close(sc, base[2].cpu().numpy(), f"packed {name} scatter vs token order")
     finally:
         dh.drop_packed_table()
+
+
+# ---------------------------------------------------------------------------
+# CUDA graphs of the calls (fixed sizes, pad-up replay)
+
+
+def test_captured_calls_match_eager_calls(build_lib):
+    """Replays at padded sizes give the eager call's outputs bit for bit (each row's
+    result does not depend on the other rows), a replay reads the current contents of
+    the static input, and batches above the largest size fall back to the eager call."""
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = m.CapturedCalls(dh, sizes=(1, 2, 4, 8, 16, 32, 64))
+        try:
+            for B in (1, 3, 5, 8, 17, 64, 70):
+                hidden = synth.hidden_batch("uniform", B, row0=9000 + 100 * B)
+                h = helpers.bf16_tensor(hidden)
+                tok, mx = g(h)
+                tok, mx = tok.clone(), mx.clone()
+                etok, emx = m.mtp_masked_topk_tokens(dh, h)
+                s.synchronize()
+                assert torch.equal(tok, etok) and torch.equal(mx, emx), f"B={B}"
+                if B in (5, 64):
+                    ref = oracle.masked_topk_tokens(oh, hidden)
+                    clear = (ref["score_margin"] > helpers.MARGIN) & (ref["logit_margin"] > helpers.MARGIN)
+                    np.testing.assert_array_equal(tok.cpu().numpy()[clear], ref["tokens"][clear])
+            assert m.mtp_read_device_error(g.ws, stream=s) == 0
+        finally:
+            g.close()
+
+
+def test_captured_scatter_and_packed_graphs(build_lib):
+    m = build_lib
+    # scatter finish on the tiny head
+    oh, dh = device_head(m, "tiny")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = m.CapturedCalls(dh, sizes=(1, 2), finish="scatter")
+        try:
+            hidden = synth.hidden_batch("tiny", 2, row0=77)
+            out = g(helpers.bf16_tensor(hidden)).clone()
+            s.synchronize()
+            helpers.assert_close(out.cpu().numpy(), oracle.masked_scatter_logits(oh, hidden), "graph scatter")
+        finally:
+            g.close()
+    # the packed table's tensor-core gather inside a graph (B*K = C on uniform clusters)
+    oh, dh = device_head(m, "uniform")
+    packed = dh.use_packed_table()
+    try:
+        with torch.cuda.stream(s):
+            g = m.CapturedCalls(dh, sizes=(64,))
+            try:
+                assert m.mtp_gather_plan(dh, 64) == "tensor_core"
+                hidden = synth.hidden_batch("uniform", 64, row0=4242)
+                h = helpers.bf16_tensor(hidden)
+                tok, mx = g(h)
+                tok, mx = tok.clone(), mx.clone()
+                etok, emx = m.mtp_masked_topk_tokens(dh, h)
+                s.synchronize()
+                assert torch.equal(tok, etok) and torch.equal(mx, emx)
+            finally:
+                g.close()
+    finally:
+        dh.drop_packed_table()
+        del packed
