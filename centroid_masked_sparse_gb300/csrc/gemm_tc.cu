@@ -93,6 +93,9 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
     return v;
 }
 
+// Columns of the partial tile that one reduction step loads at once (from every rank).
+constexpr int kRedCols = 4;
+
 __device__ __forceinline__ void report_timeout(const TcParams &p)
 {
     if (p.err) atomicOr(p.err, MTP_DEVERR_TIMEOUT);
@@ -234,7 +237,8 @@ __global__ void __launch_bounds__(kTcThreads)
             const uint32_t trow = tmem_base + ((uint32_t)(warp * kWarp) << 16) + (uint32_t)(acc * p.n_pad);
             float *outp = p.out ? p.out + (size_t)sp * p.split_stride : nullptr;
             // cluster mode: the stage ring is idle now (every MMA of this CTA's only
-            // unit has completed), so it holds the partial tile as red[n][128]
+            // unit has completed), so it holds the partial tile as red[n][128]: a warp
+            // reads one column of it as one contiguous 128-byte line
             float *red = reinterpret_cast<float *>(smem);
             const int m_local = warp * kWarp + lane;
             for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
@@ -280,7 +284,9 @@ __global__ void __launch_bounds__(kTcThreads)
     if (p.cluster_reduce) {
         // split-K: the cluster's CTAs hold the partial tiles of one output tile.  Each
         // rank sums a slice of the columns over all ranks, in rank order (deterministic),
-        // and stores it; the loads of one column are independent, so they overlap.
+        // and stores it; it loads kRedCols columns from every rank at once (all loads
+        // independent, each warp-wide load one 128-byte line), so the remote latency is
+        // paid once per group of columns, not once per column.
         cluster_sync_all();
         uint32_t rank;
         asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
@@ -296,17 +302,24 @@ __global__ void __launch_bounds__(kTcThreads)
 #pragma unroll
             for (int r = 0; r < 8; ++r) base[r] = r < p.splits ? dsmem_addr(red0, (uint32_t)r) : 0u;
             if (m < p.M) {
-                for (int j = j0; j < j1; ++j) {
-                    const int n = nb * p.n_pad + j;
-                    if (n >= p.N) break;
-                    const uint32_t off = (uint32_t)((j * kTileM + m_local) * 4);
-                    float part[8];
+                for (int j = j0; j < j1; j += kRedCols) {
+                    float part[kRedCols][8];
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) part[r] = r < p.splits ? ld_dsmem_f32(base[r] + off) : 0.f;
-                    float v = 0.f;
+                    for (int q = 0; q < kRedCols; ++q) {
+                        const uint32_t off = (uint32_t)(((j + q) * kTileM + m_local) * 4);
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) v += part[r];
-                    p.out[(size_t)n * p.ldo + m] = v;
+                        for (int r = 0; r < 8; ++r)
+                            part[q][r] = (r < p.splits && j + q < j1) ? ld_dsmem_f32(base[r] + off) : 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < kRedCols; ++q) {
+                        const int n = nb * p.n_pad + j + q;
+                        if (j + q >= j1 || n >= p.N) break;
+                        float v = 0.f;
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) v += part[q][r];   // rank order: deterministic
+                        p.out[(size_t)n * p.ldo + m] = v;
+                    }
                 }
             }
         }

@@ -136,8 +136,10 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     }
     const float span = vmax - vmin;
     const float scale = (span > 0.f && span < __int_as_float(0x7f800000)) ? 255.5f / span : 0.f;
+    // the scores are read from global memory once: later passes take them back from the
+    // order-preserving keys in shared memory
     for (int c = tid; c < p.C; c += kTopkThreads)
-        atomicAdd(&hist[value_bucket(row[c], vmin, scale)], 1u);
+        atomicAdd(&hist[value_bucket(ord_value(keys[c]), vmin, scale)], 1u);
     __syncthreads();
     if (tid < kWarp) {
         uint32_t loc[8], sum = 0u;
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     const int ncand = (int)s_above;
     if (ncand <= kCandCap) {
         for (int c = tid; c < p.C; c += kTopkThreads) {
-            if (value_bucket(row[c], vmin, scale) >= kbucket) {
+            if (value_bucket(ord_value(keys[c]), vmin, scale) >= kbucket) {
                 const int pos = atomicAdd(&s_ncand, 1);
                 s_cand[pos] = select_key(keys[c], c);
             }
