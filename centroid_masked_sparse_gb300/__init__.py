@@ -21,7 +21,7 @@ from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_M
                    MtpError, MtpHeadDesc, check, lib)
 
 __all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "mtp_workspace_bytes", "mtp_centroid_scores",
-           "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_dense_lm_head",
+           "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_select_and_score", "mtp_dense_lm_head",
            "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
            "MTP_DEVERR_TOKEN_RANGE",
            "MTP_DEVERR_OFFSETS", "lib"]
@@ -184,6 +184,23 @@ def mtp_masked_scatter_logits(head, hidden, out=None, workspace=None, stream=Non
                                           _stream_ptr(stream, head.device)),
           "mtp_masked_scatter_logits")
     return out
+
+
+def mtp_select_and_score(head, hidden, out_logits=None, out_ids=None, with_ids=True, workspace=None,
+                         stream=None):
+    """(logits fp32 [B, K*S], token ids int32 [B, K*S] or None): _select_and_score's pair."""
+    torch = _torch()
+    B = _hidden_ok(head, hidden)
+    width = head.top_k * (head.vocab_size // max(1, head.num_centroids))
+    if out_logits is None:
+        out_logits = torch.empty(B, width, dtype=torch.float32, device=head.device)
+    if with_ids and out_ids is None:
+        out_ids = torch.empty(B, width, dtype=torch.int32, device=head.device)
+    ws = workspace if workspace is not None else head.workspace(B)
+    check(lib().mtp_select_and_score(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_logits),
+                                     _ptr(out_ids), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream_ptr(stream, head.device)), "mtp_select_and_score")
+    return out_logits, out_ids
 
 
 def mtp_dense_lm_head(head, hidden, out_logits=None, out_tokens=None, out_max=None,

@@ -57,6 +57,7 @@ SIGNATURES = {
     "mtp_packed_embeddings_bytes": (ctypes.c_size_t, [_DP]),
     "mtp_pack_embeddings": (_i32, [_DP, _p, ctypes.c_size_t, _p, _p]),
     "mtp_gather_plan": (_i32, [_DP, _i32]),
+    "mtp_select_and_score": (_i32, [_DP, _p, _i32, _p, _p, _p, ctypes.c_size_t, _p]),
     "mtp_graph_capture": (_i32, [_DP, _i32, _p, _i32, _p, _p, _p, ctypes.c_size_t, _p,
                                  ctypes.POINTER(ctypes.c_void_p)]),
     "mtp_graph_launch": (_i32, [_p, _p]),

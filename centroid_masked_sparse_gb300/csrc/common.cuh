@@ -198,6 +198,13 @@ struct GatherParams {
     float *out_logits;              // [B, V] (scatter finish)
     int32_t *out_tokens;            // [B] (argmax finish)
     float *out_max;                 // [B] or null
+    // the sparse pair (scatter instantiation): out_logits / out_ids are [B, sparse_width]
+    // with sparse_width = K * S, entry (row, rank k of the cluster in the row's top-K,
+    // position i in the cluster) at row * sparse_width + k * S + i; 0 = full-vocab scatter
+    int sparse_width;
+    int32_t *out_ids;               // [B, sparse_width] or null
+    const int32_t *topk;            // [B, K] the rows' selections (ranks for the sparse pair)
+    int K;
     int B, H, V, S, W, C;
     int chunk;                      // ordered positions per work item
     int ring;                       // embedding-row slots per CTA

@@ -77,7 +77,9 @@ struct UnitMeta {
     int npad, nvalid;
     int p0;             // token-order table: first ordered position; packed: first group
     int box;            // token-order table: unused; packed: groups of 32 rows
-    int pad[3];
+    int local0;         // position of the chunk's first candidate inside its cluster
+    int pad[2];
+    int ranks[kMaxN];   // sparse pair: rank of the cluster in each row's top-K
 };
 
 struct Params {
@@ -91,6 +93,10 @@ struct Params {
     float *out_logits;
     int32_t *out_tokens;
     float *out_max;
+    int sparse_width;         // sparse pair: row stride K*S of out_logits / out_ids; 0 otherwise
+    int32_t *out_ids;
+    const int32_t *topk;      // [B, K]
+    int K;
     int B, H, V, S, W, C;
     int chunk;      // positions per work item (<= 128; a multiple of 32 when packed)
     const uint8_t *packed;    // packed table blocks, or null (token-order gathers)
@@ -187,10 +193,25 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                 }
                 m.tok[t] = tok;
             }
+            if (p.sparse_width) {
+                // the sparse pair's column block of each row: the cluster's rank in its top-K
+                __syncwarp();   // every lane's row entries are written
+                for (int r = 0; r < n; ++r) {
+                    const int32_t *sel = p.topk + (size_t)m.rows[r] * p.K;
+                    int rank = -1;
+                    for (int k0 = 0; k0 < p.K && rank < 0; k0 += kWarp) {
+                        const bool hit = k0 + lane < p.K && __ldcg(sel + k0 + lane) == cur.x;
+                        const unsigned bal = __ballot_sync(0xffffffffu, hit);
+                        if (bal) rank = k0 + __ffs(bal) - 1;
+                    }
+                    if (lane == 0) m.ranks[r] = rank;
+                }
+            }
             if (lane == 0) {
                 m.n = n;
                 m.npad = npad;
                 m.nvalid = nvalid;
+                m.local0 = p0 - lo;
                 m.p0 = p.packed ? g0 : p0;
                 m.box = (nvalid + kPackRows - 1) / kPackRows;
             }
@@ -443,7 +464,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float v = __uint_as_float(r[j]);
                     const int row = m.rows[col];
                     if (SCATTER) {
-                        if (tok >= 0) p.out_logits[(size_t)row * p.V + tok] = v;
+                        if (tok >= 0) {
+                            if (p.sparse_width) {
+                                const int rank = m.ranks[col];
+                                if (rank >= 0) {
+                                    const size_t o = (size_t)row * p.sparse_width + (size_t)rank * p.S +
+                                                     (size_t)(m.local0 + t);
+                                    p.out_logits[o] = v;
+                                    if (p.out_ids) p.out_ids[o] = tok;
+                                }
+                            } else {
+                                p.out_logits[(size_t)row * p.V + tok] = v;
+                            }
+                        }
                     } else {
                         unsigned long long key = tok >= 0 ? argmax_key(v, tok) : 0ull;
 #pragma unroll
@@ -545,6 +578,10 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     p.out_logits = g.out_logits;
     p.out_tokens = g.out_tokens;
     p.out_max = g.out_max;
+    p.sparse_width = g.sparse_width;
+    p.out_ids = g.out_ids;
+    p.topk = g.topk;
+    p.K = g.K;
     p.B = g.B;
     p.H = g.H;
     p.V = g.V;

@@ -301,9 +301,12 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
     return false;
 }
 
+// The masked calls.  Finishes: the sparse argmax (out_tokens), the full-vocabulary
+// scatter (out_logits [B, V]) or, with `sparse`, the sparse pair (out_logits and
+// out_ids [B, K*S], every entry written, so no -inf fill).
 mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t *out_tokens,
-                      float *out_max, float *out_logits, void *workspace, size_t ws_bytes,
-                      cudaStream_t s)
+                      float *out_max, float *out_logits, int32_t *out_ids, bool sparse, void *workspace,
+                      size_t ws_bytes, cudaStream_t s)
 {
     const Layout L = layout_for(d, B);
     if (!workspace || ws_bytes < L.total) return MTP_ERR_WORKSPACE;
@@ -311,7 +314,7 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     mtp_status st = use_device(d->device);
     if (st != MTP_OK) return st;
     char *ws = (char *)workspace;
-    if (out_logits) {
+    if (out_logits && !sparse) {
         Prof pr(MTP_KERNEL_FILL, s);
         st = cuda_status(launch_fill_neg_inf(out_logits, (size_t)B * d->vocab_size, s));
         if (st != MTP_OK) return st;
@@ -336,6 +339,10 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     gp.out_logits = out_logits;
     gp.out_tokens = out_tokens;
     gp.out_max = out_max;
+    gp.topk = (const int32_t *)(ws + L.topk);
+    gp.K = d->top_k;
+    gp.sparse_width = sparse ? d->top_k * (d->vocab_size / d->num_centroids) : 0;
+    gp.out_ids = sparse ? out_ids : nullptr;
     gp.B = B;
     gp.H = d->hidden_size;
     gp.V = d->vocab_size;
@@ -386,7 +393,7 @@ mtp_status mtp_masked_topk_tokens(const mtp_head_desc *desc, const void *hidden,
     if (batch == 0) return MTP_OK;
     if (!hidden || !out_tokens) return MTP_ERR_NULL;
     if (!aligned16(hidden)) return MTP_ERR_ALIGN;
-    return run_masked(desc, hidden, batch, out_tokens, out_max, nullptr, workspace, workspace_bytes,
+    return run_masked(desc, hidden, batch, out_tokens, out_max, nullptr, nullptr, false, workspace, workspace_bytes,
                       (cudaStream_t)stream);
 }
 
@@ -400,7 +407,21 @@ mtp_status mtp_masked_scatter_logits(const mtp_head_desc *desc, const void *hidd
     if (batch == 0) return MTP_OK;
     if (!hidden || !out_logits) return MTP_ERR_NULL;
     if (!aligned16(hidden) || !aligned16(out_logits)) return MTP_ERR_ALIGN;
-    return run_masked(desc, hidden, batch, nullptr, nullptr, out_logits, workspace, workspace_bytes,
+    return run_masked(desc, hidden, batch, nullptr, nullptr, out_logits, nullptr, false, workspace, workspace_bytes,
+                      (cudaStream_t)stream);
+}
+
+mtp_status mtp_select_and_score(const mtp_head_desc *desc, const void *hidden, int32_t batch, float *out_logits,
+                                int32_t *out_ids, void *workspace, size_t workspace_bytes, void *stream)
+{
+    mtp_status st = check_desc(desc, true, true, true);
+    if (st != MTP_OK) return st;
+    if ((st = check_batch(batch)) != MTP_OK) return st;
+    if (desc->cluster_offsets) return MTP_ERR_UNSUPPORTED;   // the pair's width K*S needs uniform clusters
+    if (batch == 0) return MTP_OK;
+    if (!hidden || !out_logits) return MTP_ERR_NULL;
+    if (!aligned16(hidden)) return MTP_ERR_ALIGN;
+    return run_masked(desc, hidden, batch, nullptr, nullptr, out_logits, out_ids, true, workspace, workspace_bytes,
                       (cudaStream_t)stream);
 }
 

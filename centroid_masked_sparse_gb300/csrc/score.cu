@@ -77,10 +77,12 @@ __device__ __forceinline__ void record_timeout(const GatherParams &p, uint32_t s
 struct SlotMeta {
     int tok;      // token id, -1: skipped (invalid id), kTokDone: end of stream
     uint32_t use; // h-buffer use number: buffer use % 4, phase parity (use / 4) & 1
+    int pos;      // position of the token inside its cluster (the sparse pair's column)
 };
 
 struct HMeta {
     int rows[kMaxRowGroup];
+    int ranks[kMaxRowGroup];   // rank of the item's cluster in each row's top-K (sparse pair)
     int gr;       // rows in this group
     int left;     // slots of this item not yet consumed
 };
@@ -92,6 +94,7 @@ struct Smem {
     HMeta *hmeta;
     unsigned long long *best;
     int *prow;   // the producer's row list of the current item [B]
+    int *prank;  // rank of the item's cluster in each of those rows' top-K [B] (sparse pair)
 };
 
 __device__ __forceinline__ Smem carve(uint8_t *base, const GatherParams &p)
@@ -109,6 +112,7 @@ __device__ __forceinline__ Smem carve(uint8_t *base, const GatherParams &p)
     s.hmeta = reinterpret_cast<HMeta *>(s.meta + p.ring);
     s.best = reinterpret_cast<unsigned long long *>(s.hmeta + kHBuffers);
     s.prow = reinterpret_cast<int *>(s.best + p.B);
+    s.prank = s.prow + p.B;
     return s;
 }
 
@@ -116,6 +120,7 @@ __device__ __forceinline__ Smem carve(uint8_t *base, const GatherParams &p)
 struct ItemMeta {
     int valid;      // a real item (index below the item count)
     int c, p0, nvalid;
+    int off;        // p0 minus the cluster's first position
     int tok0, tok1; // token ids at positions p0 + lane and p0 + 32 + lane (-1 beyond nvalid)
     uint32_t mask;  // row-mask word `lane` of the cluster (lane < W)
 };
@@ -129,6 +134,7 @@ __device__ __forceinline__ void load_item(const GatherParams &p, int2 item, bool
     m.valid = valid;
     m.c = -1;
     m.p0 = 0;
+    m.off = 0;
     m.nvalid = 0;
     m.tok0 = -1;
     m.tok1 = -1;
@@ -141,6 +147,7 @@ __device__ __forceinline__ void load_item(const GatherParams &p, int2 item, bool
     const int nvalid = max(0, min(p.chunk, hi - p0));
     m.c = item.x;
     m.p0 = p0;
+    m.off = p0 - lo;
     m.nvalid = nvalid;
     if (nvalid == 0) return;
     if (lane < nvalid) m.tok0 = __ldg(p.ordering + p0 + lane);
@@ -188,6 +195,20 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
         for (uint32_t mm = cur.mask; mm; mm &= mm - 1u) sm.prow[pos++] = lane * kWarp + __ffs(mm) - 1;
         const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
         __syncwarp();
+        if (p.sparse_width) {
+            // the sparse pair's column block of each row: the cluster's rank in its top-K
+            for (int r = 0; r < total; ++r) {
+                const int32_t *sel = p.topk + (size_t)sm.prow[r] * p.K;
+                int rank = -1;
+                for (int k0 = 0; k0 < p.K && rank < 0; k0 += kWarp) {
+                    const bool hit = k0 + lane < p.K && __ldcg(sel + k0 + lane) == cur.c;
+                    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+                    if (bal) rank = k0 + __ffs(bal) - 1;
+                }
+                if (lane == 0) sm.prank[r] = rank;
+            }
+            __syncwarp();
+        }
         for (int g0 = 0; g0 < total; g0 += p.row_group) {
             const int gr = min(p.row_group, total - g0);
             const int hb = (int)(huse % kHBuffers);
@@ -198,7 +219,10 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
                 if (!ok) record_timeout(p, kSiteProducerHEmpty, huse);
                 if (ok) {
                     HMeta &hm = sm.hmeta[hb];
-                    for (int r = 0; r < gr; ++r) hm.rows[r] = sm.prow[g0 + r];
+                    for (int r = 0; r < gr; ++r) {
+                        hm.rows[r] = sm.prow[g0 + r];
+                        if (p.sparse_width) hm.ranks[r] = sm.prank[g0 + r];
+                    }
                     hm.gr = gr;
                     hm.left = cur.nvalid;
                     __threadfence_block();
@@ -236,6 +260,7 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
                     if (lok) {
                         sm.meta[slot].tok = tok;
                         sm.meta[slot].use = huse - 1u;
+                        sm.meta[slot].pos = cur.off + q;
                         if (tok >= 0) {
                             mbar_arrive_expect_tx(sm.full0 + 8u * slot, rb);
                             bulk_copy_g2s_hint(smem_u32(sm.ring + (size_t)slot * rb),
@@ -356,7 +381,16 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
                 if (lane == r) {
                     const int row = hm.rows[r];
                     if (SCATTER) {
-                        p.out_logits[(size_t)row * p.V + m.tok] = acc;
+                        if (p.sparse_width) {
+                            const int rank = hm.ranks[r];
+                            if (rank >= 0) {
+                                const size_t o = (size_t)row * p.sparse_width + (size_t)rank * p.S + m.pos;
+                                p.out_logits[o] = acc;
+                                if (p.out_ids) p.out_ids[o] = m.tok;
+                            }
+                        } else {
+                            p.out_logits[(size_t)row * p.V + m.tok] = acc;
+                        }
                     } else {
                         const unsigned long long key = argmax_key(acc, m.tok);
                         best = key > best ? key : best;
@@ -491,7 +525,7 @@ size_t gather_smem_bytes(const GatherParams &p)
     const size_t rb = (size_t)p.H * 2;
     return (size_t)p.ring * rb + (size_t)kHBuffers * p.row_group * rb +
            (size_t)(2 * p.ring + 2 * kHBuffers) * 8 + (size_t)p.ring * sizeof(SlotMeta) +
-           kHBuffers * sizeof(HMeta) + (size_t)p.B * 12;
+           kHBuffers * sizeof(HMeta) + (size_t)p.B * 16;
 }
 
 // Geometry of the gather kernel for p.H and p.B: consumer warps, CTAs per SM,
@@ -509,7 +543,7 @@ void gather_geometry(GatherParams &p)
     if (rg > p.B) rg = p.B;
     p.row_group = rg;
     const size_t budget = (size_t)(212 * 1024) / (size_t)p.ctas_per_sm;
-    const size_t fixed = (size_t)kHBuffers * rg * rb + kHBuffers * (sizeof(HMeta) + 16) + (size_t)p.B * 12 + 64;
+    const size_t fixed = (size_t)kHBuffers * rg * rb + kHBuffers * (sizeof(HMeta) + 16) + (size_t)p.B * 16 + 64;
     long long r = fixed < budget ? (long long)((budget - fixed) / (rb + 16 + sizeof(SlotMeta))) : 0;
     const int nw = p.consumer_warps;
     if (r > 256) r = 256;

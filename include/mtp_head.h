@@ -159,6 +159,21 @@ MTP_API mtp_status mtp_masked_scatter_logits(const mtp_head_desc *desc, const vo
                                      int32_t batch, float *out_logits,
                                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* _select_and_score: steps 1-4 returned as the sparse pair, for consumers of the
+ * candidates themselves (tree drafting, sampling over the candidate set).  Uniform
+ * clusters only (cluster_offsets NULL; MTP_ERR_UNSUPPORTED otherwise): with
+ * S = V / C, row b holds K*S entries, the clusters in the row's selection order
+ * (score desc, index asc) and inside each cluster its positions in order:
+ *   out_logits  fp32 [batch, K*S] out: entry k*S + i is the logit of token
+ *               token_ordering[c_k * S + i], c_k the row's k-th selected centroid
+ *   out_ids     int32 [batch, K*S] out, or NULL: that token id
+ * Every entry is written (no fill); with an out-of-range token id in
+ * token_ordering the entries of that id are left unwritten and the device error
+ * word reports MTP_DEVERR_TOKEN_RANGE.  Workspace as for mtp_masked_topk_tokens. */
+MTP_API mtp_status mtp_select_and_score(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                                        float *out_logits, int32_t *out_ids, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
 /* Dense comparator: logit[b, t] = sum_k h[b, k] * E[t, k] for every t < V.
  *   out_logits  fp32 [batch, V] out (row stride V), or NULL
  *   out_tokens  int32 [batch] out, or NULL: dense argmax, lower id on ties

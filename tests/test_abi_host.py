@@ -194,3 +194,19 @@ def test_graph_capture_rejects_bad_arguments(L):
                                1 << 30, st, ctypes.byref(g)) == -3
     assert L.mtp_graph_launch(None, None) == -1
     assert L.mtp_graph_destroy(None) == 0
+
+
+def test_select_and_score_rejects_bad_arguments(L):
+    d = _desc()
+    out = ctypes.c_void_p(0x8000)
+    ids = ctypes.c_void_p(0x9000000)
+    # the pair's width K*S needs uniform clusters
+    assert L.mtp_select_and_score(ctypes.byref(_desc(offsets=0x5000)), FAKE, 4, out, ids, WS,
+                                  1 << 30, None) == -6
+    assert L.mtp_select_and_score(ctypes.byref(d), None, 4, out, ids, WS, 1 << 30, None) == -1
+    assert L.mtp_select_and_score(ctypes.byref(d), FAKE, 4, None, ids, WS, 1 << 30, None) == -1
+    assert L.mtp_select_and_score(ctypes.byref(d), ctypes.c_void_p(0x7002), 4, out, ids, WS,
+                                  1 << 30, None) == -3
+    assert L.mtp_select_and_score(ctypes.byref(d), FAKE, 4, out, ids, WS, 16, None) == -4
+    assert L.mtp_select_and_score(ctypes.byref(d), FAKE, -2, out, ids, WS, 1 << 30, None) == -2
+    assert L.mtp_select_and_score(ctypes.byref(d), None, 0, None, None, None, 0, None) == 0

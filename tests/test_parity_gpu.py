@@ -706,3 +706,54 @@ def test_captured_scatter_and_packed_graphs(build_lib):
     finally:
         dh.drop_packed_table()
         del packed
+
+
+# ---------------------------------------------------------------------------
+# the sparse pair of _select_and_score
+
+
+@pytest.mark.parametrize("name,B,packed,rows", [
+    ("tiny", 1, False, None),
+    ("uniform", 1, False, None),
+    ("uniform", 8, False, None),
+    ("uniform", 64, False, [0, 17, 40, 63]),
+    ("uniform", 64, True, [1, 30, 62]),        # packed table: the tensor-core gather
+    ("shared", 256, False, [0, 99, 255]),      # large buckets: the tensor-core gather (gather4)
+    ("shared", 256, True, [3, 128, 200]),
+])
+def test_select_and_score_pair(build_lib, name, B, packed, rows):
+    """Every row's K*S candidates in selection order with their token ids: ids exact where
+    the oracle's K/(K+1) margin is clear, logits within the fp32 tolerance."""
+    m = build_lib
+    oh, dh = device_head(m, name)
+    hidden, ref, _ = helpers.clean_batch(name, oh, B, need_logit_margin=False)
+    if packed:
+        dh.use_packed_table()
+    try:
+        logits, ids = m.mtp_select_and_score(dh, helpers.bf16_tensor(hidden))
+        torch.cuda.synchronize()
+    finally:
+        if packed:
+            dh.drop_packed_table()
+    logits, ids = logits.cpu().numpy(), ids.cpu().numpy()
+    assert logits.shape == (B, oh.K * (oh.V // oh.C)) and ids.shape == logits.shape
+    for b in (rows if rows is not None else range(B)):
+        rlog, rtok = oracle.select_and_score_row(oh, hidden, b)
+        np.testing.assert_array_equal(ids[b], rtok, err_msg=f"{name} row {b} ids")
+        helpers.assert_close(logits[b], rlog, f"{name} row {b} logits")
+    # every row's ids are the union of its selected clusters: a set of K*S distinct tokens
+    for b in range(B):
+        assert len(np.unique(ids[b])) == ids.shape[1]
+
+
+def test_select_and_score_matches_the_scatter(build_lib):
+    """The pair scattered into a -inf row is the full-vocabulary scatter finish."""
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    h = helpers.bf16_tensor(synth.hidden_batch("uniform", 16, row0=777))
+    logits, ids = m.mtp_select_and_score(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    torch.cuda.synchronize()
+    rebuilt = torch.full_like(sc, float("-inf"))
+    rebuilt.scatter_(1, ids.long(), logits)
+    assert torch.equal(rebuilt, sc)
