@@ -319,6 +319,23 @@ def measure_graph(ctx, t, dh, name, B, steps, warmup, rot=4, row0=0):
     return float(np.mean(call)), float(np.mean(bare)), err
 
 
+def measure_pair(ctx, t, dh, name, B, steps, warmup, rot=4, row0=0):
+    """µs per call of the sparse pair (mtp_select_and_score) and its gather kernel's µs."""
+    torch, m, synth, timer = ctx["torch"], ctx["m"], ctx["synth"], ctx["timer"]
+    hb = make_batches(synth, t, name, B, rot, row0)
+    hs = [torch.from_numpy(h.view(np.int16)).to(ctx["device"]).view(torch.bfloat16) for h in hb]
+    ws = dh.workspace(B)
+    width = t.workload.top_k * (t.workload.vocab // t.workload.centroids)
+    lg = torch.empty(B, width, dtype=torch.float32, device=ctx["device"])
+    ids = torch.empty(B, width, dtype=torch.int32, device=ctx["device"])
+    fn = lambda i: m.mtp_select_and_score(dh, hs[i % rot], out_logits=lg, out_ids=ids,  # noqa: E731
+                                          workspace=ws)
+    call, _, _, _ = timer.run(fn, steps, warmup, ws=ctx["ws"])
+    _, kern, _, _ = timer.run(fn, max(20, steps // 4), 2, kernel="gather_score", ws=ctx["ws"])
+    return dict(call_ms=float(np.mean(call)), kernel_ms=float(np.mean(kern)),
+                device_error=m.mtp_read_device_error(ws), out_bytes=B * width * 8)
+
+
 def measure_dense(ctx, t, dh, B, steps, warmup):
     torch, m, synth, timer = ctx["torch"], ctx["m"], ctx["synth"], ctx["timer"]
     h = torch.from_numpy(synth.hidden_batch("scatter", B).view(np.int16)).to(ctx["device"]).view(
@@ -511,8 +528,8 @@ def other_workloads(ctx, args, hbm):
     res = {}
     steps = max(10, args.steps // 8)
     cases = (("scatter", True, False), ("variable", False, False), ("shared", False, False),
-             ("shared", True, False), ("uniform", False, True), ("variable", False, True),
-             ("shared", False, True), ("shared", True, True))
+             ("shared", True, False), ("uniform", False, False), ("uniform", False, True),
+             ("variable", False, True), ("shared", False, True), ("shared", True, True))
     for name, scatter, packed in cases:
         w = synth.WORKLOADS[name]
         t = synth.make_tables(name)
@@ -535,6 +552,14 @@ def other_workloads(ctx, args, hbm):
                     "unique_clusters": r["bytes"]["unique_clusters"],
                     "kernels_us": r["kernels_us"], "max_call_us": r["max_call_us"],
                     "device_error": r["device_error"]}
+        if name == "uniform" and not scatter:
+            pr = measure_pair(ctx, t, dh, name, w.batch, steps, args.warmup)
+            res[f"uniform_pair_b{w.batch}" + ("_packed_table" if packed else "")] = {
+                "finish": "sparse pair (logits + token ids, [B, K*S])",
+                "us_per_call": round(pr["call_ms"] * 1e3, 2),
+                "tokens_per_s": round(w.batch / (pr["call_ms"] * 1e-3), 1),
+                "gather_us": round(pr["kernel_ms"] * 1e3, 2), "output_bytes": pr["out_bytes"],
+                "device_error": pr["device_error"]}
         if name == "scatter":
             d = measure_dense(ctx, t, dh, w.batch, steps, args.warmup)
             gbs = d["bytes"] / (d["kernel_ms"] * 1e-3) / 1e9

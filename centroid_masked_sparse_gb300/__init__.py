@@ -20,7 +20,7 @@ import ctypes
 from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_MAX_BATCH,
                    MtpError, MtpHeadDesc, check, lib)
 
-__all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "mtp_workspace_bytes", "mtp_centroid_scores",
+__all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "MTP_FINISH_PAIR", "mtp_workspace_bytes", "mtp_centroid_scores",
            "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_select_and_score", "mtp_dense_lm_head",
            "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
            "MTP_DEVERR_TOKEN_RANGE",
@@ -244,7 +244,7 @@ def mtp_gather_plan(head, batch: int) -> str:
     return "tensor_core" if r == 1 else "cuda_core"
 
 
-MTP_FINISH_ARGMAX, MTP_FINISH_SCATTER = 0, 1
+MTP_FINISH_ARGMAX, MTP_FINISH_SCATTER, MTP_FINISH_PAIR = 0, 1, 2
 
 
 class CapturedCalls:
@@ -277,6 +277,11 @@ class CapturedCalls:
             self.out0 = torch.empty(top, head.vocab_size, dtype=torch.float32, device=dev)
             self.out1 = None
             code = MTP_FINISH_SCATTER
+        elif finish == "pair":
+            width = head.top_k * (head.vocab_size // max(1, head.num_centroids))
+            self.out0 = torch.empty(top, width, dtype=torch.float32, device=dev)
+            self.out1 = torch.empty(top, width, dtype=torch.int32, device=dev)
+            code = MTP_FINISH_PAIR
         else:
             raise ValueError(finish)
         self.graphs = {}
@@ -305,7 +310,7 @@ class CapturedCalls:
             raise ValueError(f"batch {batch} is above the largest captured size {self.sizes[-1]}")
         check(lib().mtp_graph_launch(self.graphs[size], ctypes.c_void_p(self.stream.cuda_stream)),
               "mtp_graph_launch")
-        if self.finish == "argmax":
+        if self.finish in ("argmax", "pair"):
             return self.out0[:batch], self.out1[:batch]
         return self.out0[:batch]
 
@@ -316,11 +321,13 @@ class CapturedCalls:
             if size is None:   # above the largest graph: the eager call
                 if self.finish == "argmax":
                     return mtp_masked_topk_tokens(self.head, hidden)
+                if self.finish == "pair":
+                    return mtp_select_and_score(self.head, hidden)
                 return mtp_masked_scatter_logits(self.head, hidden)
             self.hidden[:B].copy_(hidden)
             check(lib().mtp_graph_launch(self.graphs[size], ctypes.c_void_p(self.stream.cuda_stream)),
                   "mtp_graph_launch")
-        if self.finish == "argmax":
+        if self.finish in ("argmax", "pair"):
             return self.out0[:B], self.out1[:B]
         return self.out0[:B]
 

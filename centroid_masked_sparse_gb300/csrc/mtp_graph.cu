@@ -21,7 +21,9 @@ mtp_status run_call(const mtp_head_desc *desc, int32_t finish, const void *hidde
 {
     if (finish == MTP_FINISH_ARGMAX)
         return mtp_masked_topk_tokens(desc, hidden, batch, (int32_t *)out0, (float *)out1, ws, ws_bytes, stream);
-    return mtp_masked_scatter_logits(desc, hidden, batch, (float *)out0, ws, ws_bytes, stream);
+    if (finish == MTP_FINISH_SCATTER)
+        return mtp_masked_scatter_logits(desc, hidden, batch, (float *)out0, ws, ws_bytes, stream);
+    return mtp_select_and_score(desc, hidden, batch, (float *)out0, (int32_t *)out1, ws, ws_bytes, stream);
 }
 
 }  // namespace
@@ -35,7 +37,8 @@ mtp_status mtp_graph_capture(const mtp_head_desc *desc, int32_t finish, const vo
     if (!graph) return MTP_ERR_NULL;
     *graph = nullptr;
     if (!stream) return MTP_ERR_NULL;
-    if (finish != MTP_FINISH_ARGMAX && finish != MTP_FINISH_SCATTER) return MTP_ERR_SHAPE;
+    if (finish != MTP_FINISH_ARGMAX && finish != MTP_FINISH_SCATTER && finish != MTP_FINISH_PAIR)
+        return MTP_ERR_SHAPE;
     if (batch < 1) return MTP_ERR_SHAPE;
     // eagerly once: validates everything and does the one-time per-device work
     // (kernel attributes, occupancy queries, tensor-map encoder lookup) outside the capture

@@ -258,7 +258,9 @@ MTP_API mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, 
  *   finish   MTP_FINISH_ARGMAX: out0 = int32 out_tokens [batch], out1 = float
  *            out_max [batch] or NULL (mtp_masked_topk_tokens);
  *            MTP_FINISH_SCATTER: out0 = float out_logits [batch, V], out1 unused
- *            (mtp_masked_scatter_logits)
+ *            (mtp_masked_scatter_logits);
+ *            MTP_FINISH_PAIR: out0 = float out_logits [batch, K*S], out1 = int32
+ *            out_ids [batch, K*S] or NULL (mtp_select_and_score)
  *   stream   a created stream (capture is impossible on the legacy stream: NULL
  *            returns MTP_ERR_NULL)
  *   graph    receives an opaque handle owned by the caller (mtp_graph_destroy)
@@ -267,6 +269,7 @@ MTP_API mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, 
  * *graph NULL. */
 #define MTP_FINISH_ARGMAX 0
 #define MTP_FINISH_SCATTER 1
+#define MTP_FINISH_PAIR 2
 typedef struct mtp_graph mtp_graph;
 MTP_API mtp_status mtp_graph_capture(const mtp_head_desc *desc, int32_t finish, const void *hidden,
                                      int32_t batch, void *out0, void *out1, void *workspace,

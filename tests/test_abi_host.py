@@ -184,7 +184,7 @@ def test_graph_capture_rejects_bad_arguments(L):
                                ctypes.byref(g)) == -1          # the legacy stream cannot be captured
     assert g.value is None                                    # *graph is cleared on every failure
     st = ctypes.c_void_p(0x77)
-    assert L.mtp_graph_capture(ctypes.byref(d), 2, FAKE, 4, out, None, WS, 1 << 30, st,
+    assert L.mtp_graph_capture(ctypes.byref(d), 3, FAKE, 4, out, None, WS, 1 << 30, st,
                                ctypes.byref(g)) == -2          # unknown finish
     assert L.mtp_graph_capture(ctypes.byref(d), 0, FAKE, 0, out, None, WS, 1 << 30, st,
                                ctypes.byref(g)) == -2          # nothing to record

@@ -757,3 +757,20 @@ def test_select_and_score_matches_the_scatter(build_lib):
     rebuilt = torch.full_like(sc, float("-inf"))
     rebuilt.scatter_(1, ids.long(), logits)
     assert torch.equal(rebuilt, sc)
+
+
+def test_captured_pair_graph(build_lib):
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = m.CapturedCalls(dh, sizes=(4, 8), finish="pair")
+        try:
+            h = helpers.bf16_tensor(synth.hidden_batch("uniform", 6, row0=31337))
+            lg, ids = g(h)
+            lg, ids = lg.clone(), ids.clone()
+            elg, eids = m.mtp_select_and_score(dh, h)
+            s.synchronize()
+            assert torch.equal(lg, elg) and torch.equal(ids, eids)
+        finally:
+            g.close()
