@@ -23,6 +23,7 @@ from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_M
 __all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "MTP_FINISH_PAIR", "mtp_workspace_bytes", "mtp_centroid_scores",
            "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_select_and_score", "mtp_dense_lm_head",
            "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
+           "mtp_masked_topk_keys", "mtp_decode_keys", "combine_keys", "sharded_topk_tokens",
            "MTP_DEVERR_TOKEN_RANGE",
            "MTP_DEVERR_OFFSETS", "lib"]
 
@@ -50,10 +51,12 @@ class MaskedHead:
     embed_w          bf16 [>= V, ld] with unit inner stride (row stride ld >= H)
     token_ordering   int32 [V]: ordered position -> token id
     cluster_offsets  int32 [C + 1] or None (uniform clusters of V / C)
+    cluster_range    (begin, end): the clusters this GPU owns when the head is sharded
+                     over GPUs by cluster, or None for all of them
     """
 
     def __init__(self, centroid_w, embed_w, token_ordering, top_k, cluster_offsets=None,
-                 vocab_size=None, embed_packed=None):
+                 vocab_size=None, embed_packed=None, cluster_range=None):
         torch = _torch()
         if centroid_w is not None:
             assert centroid_w.dtype == torch.bfloat16 and centroid_w.is_contiguous()
@@ -78,7 +81,10 @@ class MaskedHead:
             embed_w=embed_w.data_ptr(), ld_embed=int(embed_w.stride(0)),
             token_ordering=None if token_ordering is None else token_ordering.data_ptr(),
             cluster_offsets=None if cluster_offsets is None else cluster_offsets.data_ptr(),
-            embed_packed=None)
+            embed_packed=None,
+            cluster_begin=0 if cluster_range is None else int(cluster_range[0]),
+            cluster_end=0 if cluster_range is None else int(cluster_range[1]))
+        self.cluster_range = cluster_range
         self.embed_packed = None
         self._ws = None
         if embed_packed is not None:
@@ -341,6 +347,50 @@ class CapturedCalls:
             self.close()
         except Exception:  # noqa: BLE001 - interpreter shutdown
             pass
+
+
+def mtp_masked_topk_keys(head, hidden, out_keys=None, workspace=None, stream=None):
+    """int64 [B]: this shard's best candidate of each row as a max-combinable key."""
+    torch = _torch()
+    B = _hidden_ok(head, hidden)
+    if out_keys is None:
+        out_keys = torch.empty(B, dtype=torch.int64, device=head.device)
+    ws = workspace if workspace is not None else head.workspace(B)
+    check(lib().mtp_masked_topk_keys(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_keys), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream_ptr(stream, head.device)),
+          "mtp_masked_topk_keys")
+    return out_keys
+
+
+def mtp_decode_keys(keys, out_tokens=None, out_max=None, with_max=True, stream=None):
+    """(token ids int32 [B], max logit fp32 [B] or None) from combined keys."""
+    torch = _torch()
+    B = int(keys.shape[0])
+    assert keys.dtype == torch.int64 and keys.is_contiguous()
+    if out_tokens is None:
+        out_tokens = torch.empty(B, dtype=torch.int32, device=keys.device)
+    if with_max and out_max is None:
+        out_max = torch.empty(B, dtype=torch.float32, device=keys.device)
+    check(lib().mtp_decode_keys(_ptr(keys), B, _ptr(out_tokens), _ptr(out_max),
+                                _stream_ptr(stream, keys.device)), "mtp_decode_keys")
+    return out_tokens, out_max
+
+
+def combine_keys(keys, group=None):
+    """The shards' exchange step: an elementwise max of the int64 keys over the ranks of
+    `group` (in place).  Nothing to do without an initialised process group."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(keys, op=dist.ReduceOp.MAX, group=group)
+    return keys
+
+
+def sharded_topk_tokens(head, hidden, group=None, workspace=None, stream=None):
+    """The sparse argmax of a cluster-sharded head: each rank's keys over its clusters,
+    one max all-reduce of B x 8 bytes, then the decode (same result on every rank)."""
+    keys = mtp_masked_topk_keys(head, hidden, workspace=workspace, stream=stream)
+    combine_keys(keys, group)
+    return mtp_decode_keys(keys, stream=stream)
 
 
 def mtp_read_device_error(workspace, stream=None) -> int:

@@ -42,6 +42,8 @@ class MtpHeadDesc(ctypes.Structure):
         ("token_ordering", ctypes.c_void_p),
         ("cluster_offsets", ctypes.c_void_p),
         ("embed_packed", ctypes.c_void_p),
+        ("cluster_begin", ctypes.c_int32),
+        ("cluster_end", ctypes.c_int32),
     ]
 
 
@@ -58,6 +60,8 @@ SIGNATURES = {
     "mtp_pack_embeddings": (_i32, [_DP, _p, ctypes.c_size_t, _p, _p]),
     "mtp_gather_plan": (_i32, [_DP, _i32]),
     "mtp_select_and_score": (_i32, [_DP, _p, _i32, _p, _p, _p, ctypes.c_size_t, _p]),
+    "mtp_masked_topk_keys": (_i32, [_DP, _p, _i32, _p, _p, ctypes.c_size_t, _p]),
+    "mtp_decode_keys": (_i32, [_p, _i32, _p, _p, _p]),
     "mtp_graph_capture": (_i32, [_DP, _i32, _p, _i32, _p, _p, _p, ctypes.c_size_t, _p,
                                  ctypes.POINTER(ctypes.c_void_p)]),
     "mtp_graph_launch": (_i32, [_p, _p]),

@@ -181,12 +181,14 @@ struct TopkParams {
     int items_cap;           // capacity of items
     uint32_t *ctrl;
     int chunk;               // tokens per work item
+    int c_begin, c_end;      // clusters this shard gathers (bucketing skips the others)
 };
 
 struct GatherParams {
     const uint16_t *hidden;         // [B, H]
     const uint16_t *embed;          // [>=V, ld]
     const uint8_t *packed;          // packed embedding table (tensor-core gather), or null
+    int packed_clusters;            // clusters the packed table was sized for (its shard)
     long long ld;
     const int32_t *ordering;        // [V]
     const int32_t *offsets;         // [C+1] or null

@@ -595,7 +595,7 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
         if (p.chunk % kPackRows != 0) return cudaErrorInvalidValue;
         p.packed = g.packed;
         p.poff = reinterpret_cast<const int32_t *>(
-            g.packed + packed_poff_offset(g.V, g.H, g.C, g.offsets != nullptr));
+            g.packed + packed_poff_offset(g.V, g.H, g.C, g.packed_clusters, g.offsets != nullptr));
     }
     p.nmax = std::min(kMaxN, (g.B + 15) & ~15);
     // the A stage holds the chunk: 32, 64 or 128 rows
@@ -629,30 +629,31 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
 // ---------------------------------------------------------------------------
 namespace {
 
-size_t packed_groups_bound(int V, int C, bool explicit_offsets)
+// Groups of 32 rows a table of n clusters needs (exact for uniform clusters).
+size_t packed_groups_bound(int V, int C, int n, bool explicit_offsets)
 {
     if (!explicit_offsets) {
         const long long S = V / C;
-        return (size_t)C * (size_t)((S + kPackRows - 1) / kPackRows);
+        return (size_t)n * (size_t)((S + kPackRows - 1) / kPackRows);
     }
-    return (size_t)(((long long)V + (long long)(kPackRows - 1) * C + kPackRows - 1) / kPackRows);
+    return (size_t)(((long long)V + (long long)(kPackRows - 1) * n + kPackRows - 1) / kPackRows);
 }
 
 // Padded cluster offsets, one CTA: poff[c] = sum over c' < c of roundup(size(c'), 32).
 // Offsets whose padded total exceeds the buffer's bound (overlapping clusters) are
 // an error: every cluster is then recorded as empty, so no later read or write
 // leaves the buffer.
-__global__ void __launch_bounds__(1024) k_pack_offsets(const int32_t *offsets, int V, int S, int C,
-                                                       long long bound_rows, int32_t *poff, uint32_t *ctrl)
+__global__ void __launch_bounds__(1024) k_pack_offsets(const int32_t *offsets, int V, int S, int C, int c0,
+                                                       int c1, long long bound_rows, int32_t *poff, uint32_t *ctrl)
 {
     __shared__ long long warp_tot[32];
     const int per = (C + (int)blockDim.x - 1) / (int)blockDim.x;
-    const int c0 = min(C, (int)threadIdx.x * per), c1 = min(C, c0 + per);
+    const int cb = min(C, (int)threadIdx.x * per), ce = min(C, cb + per);
     long long local = 0;
-    for (int c = c0; c < c1; ++c) {
+    for (int c = cb; c < ce; ++c) {
         int lo = 0, hi = 0;
         cluster_range(offsets, V, S, c, &lo, &hi, ctrl ? ctrl + kCtrlError : nullptr);
-        local += (hi - lo + kPackRows - 1) / kPackRows * kPackRows;
+        if (c >= c0 && c < c1) local += (hi - lo + kPackRows - 1) / kPackRows * kPackRows;
     }
     // exclusive scan of `local` over the block
     const int lane = threadIdx.x & (kWarp - 1), w = threadIdx.x / kWarp;
@@ -678,9 +679,9 @@ __global__ void __launch_bounds__(1024) k_pack_offsets(const int32_t *offsets, i
     const bool bad = warp_tot[nw - 1] > bound_rows;
     if (bad && threadIdx.x == 0 && ctrl) atomicOr(ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
     long long run = bad ? 0 : incl - local + (w > 0 ? warp_tot[w - 1] : 0);
-    for (int c = c0; c < c1; ++c) {
+    for (int c = cb; c < ce; ++c) {
         poff[c] = (int32_t)run;
-        if (bad) continue;
+        if (bad || c < c0 || c >= c1) continue;   // other shards' clusters count as empty
         int lo = 0, hi = 0;
         cluster_range(offsets, V, S, c, &lo, &hi, nullptr);
         run += (hi - lo + kPackRows - 1) / kPackRows * kPackRows;
@@ -739,30 +740,31 @@ __global__ void __launch_bounds__(256) k_pack_tiles(const uint16_t *__restrict__
 
 }  // namespace
 
-size_t packed_poff_offset(int V, int H, int C, bool explicit_offsets)
+size_t packed_poff_offset(int V, int H, int C, int n, bool explicit_offsets)
 {
     const size_t num_kb = (size_t)((H + kTileK - 1) / kTileK);
-    const size_t supers = (packed_groups_bound(V, C, explicit_offsets) + 3) / 4;
+    const size_t supers = (packed_groups_bound(V, C, n, explicit_offsets) + 3) / 4;
     return supers * num_kb * kPackBlock;   // a multiple of 16 KB: poff stays 256-byte aligned
 }
 
-size_t packed_table_bytes(int V, int H, int C, bool explicit_offsets)
+size_t packed_table_bytes(int V, int H, int C, int n, bool explicit_offsets)
 {
-    return packed_poff_offset(V, H, C, explicit_offsets) + (size_t)(C + 1) * sizeof(int32_t);
+    return packed_poff_offset(V, H, C, n, explicit_offsets) + (size_t)(C + 1) * sizeof(int32_t);
 }
 
 cudaError_t launch_pack_embeddings(const uint16_t *embed, long long ld, const int32_t *ordering,
-                                   const int32_t *offsets, int V, int H, int C, uint8_t *packed, uint32_t *ctrl,
-                                   cudaStream_t s)
+                                   const int32_t *offsets, int V, int H, int C, int c0, int c1, uint8_t *packed,
+                                   uint32_t *ctrl, cudaStream_t s)
 {
     const int S = offsets ? 0 : V / C;
-    int32_t *poff = reinterpret_cast<int32_t *>(packed + packed_poff_offset(V, H, C, offsets != nullptr));
-    const long long bound_rows = (long long)packed_groups_bound(V, C, offsets != nullptr) * kPackRows;
-    k_pack_offsets<<<1, 1024, 0, s>>>(offsets, V, S, C, bound_rows, poff, ctrl);
+    const int n = c1 - c0;
+    int32_t *poff = reinterpret_cast<int32_t *>(packed + packed_poff_offset(V, H, C, n, offsets != nullptr));
+    const long long bound_rows = (long long)packed_groups_bound(V, C, n, offsets != nullptr) * kPackRows;
+    k_pack_offsets<<<1, 1024, 0, s>>>(offsets, V, S, C, c0, c1, bound_rows, poff, ctrl);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int num_kb = (H + kTileK - 1) / kTileK;
-    const long long total = (long long)packed_groups_bound(V, C, offsets != nullptr) * num_kb;
+    const long long total = (long long)packed_groups_bound(V, C, n, offsets != nullptr) * num_kb;
     const long long grid = std::min<long long>(total, (long long)sm_count() * 8);
     k_pack_tiles<<<(int)std::max<long long>(1, grid), 256, 0, s>>>(embed, ld, ordering, offsets, V, H, S, C,
                                                                      num_kb, poff, packed, ctrl);

@@ -59,11 +59,15 @@ constexpr int kTcGatherMinReuse = 4;
 cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s);
 // The packed embedding table of the tensor-core gather (gather_tc.cu): byte size for
 // the shapes (an upper bound with explicit offsets) and the kernels that fill it.
-size_t packed_table_bytes(int V, int H, int C, bool explicit_offsets);
-size_t packed_poff_offset(int V, int H, int C, bool explicit_offsets);
+// n = clusters the table holds (a shard's [c0, c1), or all C).
+size_t packed_table_bytes(int V, int H, int C, int n, bool explicit_offsets);
+size_t packed_poff_offset(int V, int H, int C, int n, bool explicit_offsets);
 cudaError_t launch_pack_embeddings(const uint16_t *embed, long long ld, const int32_t *ordering,
-                                   const int32_t *offsets, int V, int H, int C, uint8_t *packed,
+                                   const int32_t *offsets, int V, int H, int C, int c0, int c1, uint8_t *packed,
                                    uint32_t *ctrl, cudaStream_t s);
+// Argmax keys (u64, workspace) -> signed-comparable int64 keys, and back to token ids.
+cudaError_t launch_export_keys(const unsigned long long *keys, int B, int64_t *out, cudaStream_t s);
+cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, float *maxv, cudaStream_t s);
 
 // Tensor-core skinny GEMM out[n, m] = sum_k table[m, k] * hidden[n, k] (gemm_tc.cu).
 struct TcGemmArgs {

@@ -129,6 +129,24 @@ Layout layout_for(const mtp_head_desc *d, int B)
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// The clusters a descriptor owns: [cluster_begin, cluster_end), or all C for (0, 0).
+void cluster_span(const mtp_head_desc *d, int *c0, int *c1)
+{
+    if (d->cluster_begin == 0 && d->cluster_end == 0) {
+        *c0 = 0;
+        *c1 = d->num_centroids;
+    } else {
+        *c0 = d->cluster_begin;
+        *c1 = d->cluster_end;
+    }
+}
+
+bool span_ok(const mtp_head_desc *d)
+{
+    if (d->cluster_begin == 0 && d->cluster_end == 0) return true;
+    return d->cluster_begin >= 0 && d->cluster_begin <= d->cluster_end && d->cluster_end <= d->num_centroids;
+}
+
 // Checks of the descriptor.  `centroids`: the call reads the centroid table
 // (and needs C, K); `embed`: it reads the embedding table; `ordering`: it
 // reads token_ordering.
@@ -149,6 +167,7 @@ mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool o
         if (d->num_centroids < 1 || d->top_k < 1 || d->top_k > d->num_centroids) return MTP_ERR_SHAPE;
         if (d->num_centroids > MTP_MAX_CENTROIDS) return MTP_ERR_UNSUPPORTED;
         if (!aligned16(d->centroid_w)) return MTP_ERR_ALIGN;
+        if (!span_ok(d)) return MTP_ERR_SHAPE;
     }
     if (ordering && !d->cluster_offsets && d->vocab_size % d->num_centroids != 0) return MTP_ERR_SHAPE;
     return MTP_OK;
@@ -251,6 +270,7 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
         tp.items_cap = L->items_cap;
         tp.ctrl = (uint32_t *)ws;
         tp.chunk = chunk;
+        cluster_span(d, &tp.c_begin, &tp.c_end);
     }
     Prof pr(MTP_KERNEL_TOPK, s);
     return cuda_status(launch_topk(tp, s));
@@ -328,6 +348,11 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     gp.hidden = (const uint16_t *)hidden;
     gp.embed = (const uint16_t *)d->embed_w;
     gp.packed = tc_gather ? (const uint8_t *)d->embed_packed : nullptr;
+    {
+        int c0, c1;
+        cluster_span(d, &c0, &c1);
+        gp.packed_clusters = c1 - c0;
+    }
     gp.ld = d->ld_embed;
     gp.ordering = d->token_ordering;
     gp.offsets = d->cluster_offsets;
@@ -477,7 +502,10 @@ size_t mtp_packed_embeddings_bytes(const mtp_head_desc *desc)
     if (check_desc(desc, false, true, false) != MTP_OK) return 0;
     if (desc->num_centroids < 1 || desc->num_centroids > MTP_MAX_CENTROIDS) return 0;
     if (!desc->cluster_offsets && desc->vocab_size % desc->num_centroids != 0) return 0;
-    return packed_table_bytes(desc->vocab_size, desc->hidden_size, desc->num_centroids,
+    if (!span_ok(desc)) return 0;
+    int c0, c1;
+    cluster_span(desc, &c0, &c1);
+    return packed_table_bytes(desc->vocab_size, desc->hidden_size, desc->num_centroids, c1 - c0,
                               desc->cluster_offsets != nullptr);
 }
 
@@ -490,8 +518,11 @@ mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, size_t p
     if (desc->num_centroids < 1) return MTP_ERR_SHAPE;
     if (desc->num_centroids > MTP_MAX_CENTROIDS) return MTP_ERR_UNSUPPORTED;
     if (!desc->cluster_offsets && desc->vocab_size % desc->num_centroids != 0) return MTP_ERR_SHAPE;
+    if (!span_ok(desc)) return MTP_ERR_SHAPE;
     if (((uintptr_t)packed & 255u) != 0 || !aligned16(workspace)) return MTP_ERR_ALIGN;
-    const size_t need = packed_table_bytes(desc->vocab_size, desc->hidden_size, desc->num_centroids,
+    int c0, c1;
+    cluster_span(desc, &c0, &c1);
+    const size_t need = packed_table_bytes(desc->vocab_size, desc->hidden_size, desc->num_centroids, c1 - c0,
                                            desc->cluster_offsets != nullptr);
     if (packed_bytes < need) return MTP_ERR_WORKSPACE;
     const char *src = (const char *)desc->embed_w, *dst = (const char *)packed;
@@ -501,8 +532,38 @@ mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, size_t p
     if (st != MTP_OK) return st;
     return cuda_status(launch_pack_embeddings((const uint16_t *)desc->embed_w, desc->ld_embed,
                                               desc->token_ordering, desc->cluster_offsets, desc->vocab_size,
-                                              desc->hidden_size, desc->num_centroids, (uint8_t *)packed,
+                                              desc->hidden_size, desc->num_centroids, c0, c1, (uint8_t *)packed,
                                               (uint32_t *)workspace, (cudaStream_t)stream));
+}
+
+mtp_status mtp_masked_topk_keys(const mtp_head_desc *desc, const void *hidden, int32_t batch, int64_t *out_keys,
+                                void *workspace, size_t workspace_bytes, void *stream)
+{
+    mtp_status st = check_desc(desc, true, true, true);
+    if (st != MTP_OK) return st;
+    if ((st = check_batch(batch)) != MTP_OK) return st;
+    if (batch == 0) return MTP_OK;
+    if (!hidden || !out_keys) return MTP_ERR_NULL;
+    if (!aligned16(hidden)) return MTP_ERR_ALIGN;
+    if (!workspace || workspace_bytes < layout_for(desc, batch).total) return MTP_ERR_WORKSPACE;
+    // the call's decoded tokens go to the scores region, which nothing reads after the
+    // top-K; the keys it leaves in the workspace are exported
+    const Layout L = layout_for(desc, batch);
+    char *ws = (char *)workspace;
+    st = run_masked(desc, hidden, batch, (int32_t *)(ws + L.scores), nullptr, nullptr, nullptr, false, workspace,
+                    workspace_bytes, (cudaStream_t)stream);
+    if (st != MTP_OK) return st;
+    return cuda_status(launch_export_keys((const unsigned long long *)(ws + L.keys), batch, out_keys,
+                                          (cudaStream_t)stream));
+}
+
+mtp_status mtp_decode_keys(const int64_t *keys, int32_t batch, int32_t *out_tokens, float *out_max, void *stream)
+{
+    mtp_status st = check_batch(batch);
+    if (st != MTP_OK) return st;
+    if (batch == 0) return MTP_OK;
+    if (!keys || !out_tokens) return MTP_ERR_NULL;
+    return cuda_status(launch_decode_keys(keys, batch, out_tokens, out_max, (cudaStream_t)stream));
 }
 
 int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch)

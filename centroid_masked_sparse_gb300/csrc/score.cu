@@ -573,6 +573,37 @@ __global__ void __launch_bounds__(256) k_fill_neg_inf(float *out, size_t n)
         out[n4 * 4 + threadIdx.x] = ninf;
 }
 
+// Argmax keys as signed-comparable int64 (the sign bit flipped: unsigned order
+// becomes signed order, and the empty key 0 becomes INT64_MIN), and back.
+__global__ void k_export_keys(const unsigned long long *keys, int B, int64_t *out)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) out[b] = (int64_t)(__ldcg(keys + b) ^ 0x8000000000000000ull);
+}
+
+__global__ void k_decode_keys(const int64_t *keys, int B, int32_t *tokens, float *maxv)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    int32_t tok;
+    float v;
+    decode_argmax_key((unsigned long long)keys[b] ^ 0x8000000000000000ull, &tok, &v);
+    tokens[b] = tok;
+    if (maxv) maxv[b] = v;
+}
+
+cudaError_t launch_export_keys(const unsigned long long *keys, int B, int64_t *out, cudaStream_t s)
+{
+    k_export_keys<<<(B + 255) / 256, 256, 0, s>>>(keys, B, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, float *maxv, cudaStream_t s)
+{
+    k_decode_keys<<<(B + 255) / 256, 256, 0, s>>>(keys, B, tokens, maxv);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s)
 {
     const int per_sm = blocks_per_sm((const void *)k_fill_neg_inf, 256, 0);

@@ -72,6 +72,7 @@ __device__ __forceinline__ unsigned long long select_key(uint32_t ord, int c)
 // Bucketing of one selection (row b picked centroid c): see the file comment.
 __device__ __forceinline__ void bucket_selection(const TopkParams &p, int b, int c)
 {
+    if (c < p.c_begin || c >= p.c_end) return;   // another shard's cluster
     atomicOr(&p.rowmask[(size_t)c * p.W + (b >> 5)], 1u << (b & 31));
     if (atomicAdd(&p.ccount[c], 1) == 0) {
         int lo, hi;

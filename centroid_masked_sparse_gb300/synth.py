@@ -71,6 +71,9 @@ WORKLOADS = {
                         table_from="uniform"),
     "shared": Workload("shared", 5, 262144, 2048, 4096, 128, 256, 0.02,
                        prototypes=8, noise_std=0.1),
+    # the draft-dimension sweep point: a drafter whose hidden size is 256
+    "draft256": Workload("draft256", 6, 262144, 256, 2048, 32, 64, 0.02,
+                         batches=(1, 8, 64)),
 }
 
 

@@ -103,13 +103,26 @@ typedef enum mtp_status {
  *   embed_packed     optional packed copy of the embedding table built by
  *                    mtp_pack_embeddings (layout below), 256-byte aligned.  When set,
  *                    the masked calls that run the tensor-core gather read each chunk's
- *                    candidate rows as contiguous 4 KB blocks instead of gathering
- *                    them row by row, and the library routes more calls there.  Token
+ *                    candidate rows as runs of contiguous 16 KB blocks instead of
+ *                    gathering them row by row, and the library routes more calls
+ *                    there (see mtp_gather_plan).  Token
  *                    ids are the same either way; logits agree within fp32 rounding
  *                    of the summation order (bit for bit when the same gather kernel
  *                    runs).  NULL: gather from embed_w (the page's layout).  It must
  *                    have been packed from this descriptor's tables; the library does
- *                    not check that. */
+ *                    not check that.
+ *   cluster_begin,   the clusters this GPU owns when the head is sharded over GPUs by
+ *   cluster_end      cluster: [cluster_begin, cluster_end), 0 <= begin <= end <= C;
+ *                    (0, 0) means all clusters.  The projection and top-K still run
+ *                    over all C centroids (the centroid table is replicated); only
+ *                    selected clusters inside the range are gathered.  The argmax
+ *                    finish then gives this shard's best candidate of each row
+ *                    (combine shards with mtp_masked_topk_keys, a max all-reduce and
+ *                    mtp_decode_keys), the scatter finish writes only this shard's
+ *                    candidates (-inf elsewhere; the elementwise max over shards is
+ *                    the whole row), and a packed table holds only these clusters.
+ *                    embed_w stays indexed by token id; only the rows of this
+ *                    shard's tokens are read. */
 typedef struct mtp_head_desc {
     int32_t vocab_size;
     int32_t hidden_size;
@@ -123,6 +136,8 @@ typedef struct mtp_head_desc {
     const int32_t *token_ordering;
     const int32_t *cluster_offsets;
     const void *embed_packed;
+    int32_t cluster_begin;
+    int32_t cluster_end;
 } mtp_head_desc;
 
 /* Bytes of device workspace that the masked calls and the dense head's argmax
@@ -229,9 +244,11 @@ MTP_API mtp_status mtp_masked_topk_tokens_noalloc(const mtp_head_desc *desc, con
  *   - after the blocks (SG = ceil(groups / 4) super-groups, groups the bound
  *     below): int32 poff[0..C].
  * mtp_packed_embeddings_bytes gives the size for the descriptor's shapes: with
- * uniform clusters exactly C * ceil(S/32) groups of 32, with explicit cluster
- * offsets the upper bound ceil((V + 31 C) / 32) groups; 0 for an invalid
- * descriptor. */
+ * uniform clusters exactly n * ceil(S/32) groups of 32, with explicit cluster
+ * offsets the upper bound ceil((V + 31 n) / 32) groups, n the clusters the
+ * descriptor owns (cluster_end - cluster_begin, or C); 0 for an invalid
+ * descriptor.  A sharded descriptor's table holds only its clusters (the others
+ * count as empty in poff). */
 MTP_API size_t mtp_packed_embeddings_bytes(const mtp_head_desc *desc);
 
 /* Fill `packed` (packed_bytes >= mtp_packed_embeddings_bytes(desc), 256-byte
@@ -243,6 +260,23 @@ MTP_API size_t mtp_packed_embeddings_bytes(const mtp_head_desc *desc);
  * (16-byte aligned, at least 64 bytes; the word is not cleared first). */
 MTP_API mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, size_t packed_bytes,
                                        void *workspace, void *stream);
+
+/* The sparse argmax as per-row keys, for combining shards of a cluster-sharded
+ * head (desc->cluster_begin/end) across GPUs: out_keys[b] orders this shard's
+ * best candidate of row b so that the larger signed 64-bit value is the larger
+ * logit, the lower token id on equal logits, and INT64_MIN means no candidate.
+ * The shards' keys combine by an elementwise max (an all-reduce with MAX over
+ * int64); mtp_decode_keys turns the result into token ids and logits.
+ *   out_keys   int64 [batch] out
+ * Workspace as for mtp_masked_topk_tokens. */
+MTP_API mtp_status mtp_masked_topk_keys(const mtp_head_desc *desc, const void *hidden, int32_t batch,
+                                        int64_t *out_keys, void *workspace, size_t workspace_bytes,
+                                        void *stream);
+
+/* Keys of mtp_masked_topk_keys (after any combination) -> out_tokens int32
+ * [batch] (-1 for INT64_MIN) and out_max fp32 [batch] or NULL (-inf for -1). */
+MTP_API mtp_status mtp_decode_keys(const int64_t *keys, int32_t batch, int32_t *out_tokens,
+                                   float *out_max, void *stream);
 
 /* CUDA graphs of the masked calls.  Gemma4Proposer._setup_centroids_cuda_graphs
  * ("Add Gemma4 MTP speculative decoding with centroids masking", vLLM

@@ -210,3 +210,28 @@ def test_select_and_score_rejects_bad_arguments(L):
     assert L.mtp_select_and_score(ctypes.byref(d), FAKE, 4, out, ids, WS, 16, None) == -4
     assert L.mtp_select_and_score(ctypes.byref(d), FAKE, -2, out, ids, WS, 1 << 30, None) == -2
     assert L.mtp_select_and_score(ctypes.byref(d), None, 0, None, None, None, 0, None) == 0
+
+
+def test_cluster_range_checks_and_packed_size(L):
+    out = ctypes.c_void_p(0x8000)
+    for b, e in ((5, 3), (-1, 4), (0, 2049)):
+        d = _desc()
+        d.cluster_begin, d.cluster_end = b, e
+        assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 1 << 30, None) == -2
+        assert L.mtp_packed_embeddings_bytes(ctypes.byref(d)) == 0
+    # a shard of half the clusters packs half the blocks (poff still covers all C)
+    d = _desc()
+    d.cluster_begin, d.cluster_end = 0, 1024
+    assert L.mtp_packed_embeddings_bytes(ctypes.byref(d)) == 1024 * 24 * 16384 + 2049 * 4
+    d.cluster_begin, d.cluster_end = 1024, 2048
+    assert L.mtp_packed_embeddings_bytes(ctypes.byref(d)) == 1024 * 24 * 16384 + 2049 * 4
+    # keys: argument checks
+    keys = ctypes.c_void_p(0xB000)
+    d = _desc()
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, 4, None, WS, 1 << 30, None) == -1
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, 4, keys, WS, 16, None) == -4
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, 0, None, None, 0, None) == 0
+    assert L.mtp_decode_keys(None, 4, out, None, None) == -1
+    assert L.mtp_decode_keys(keys, 4, None, None, None) == -1
+    assert L.mtp_decode_keys(keys, -1, out, None, None) == -2
+    assert L.mtp_decode_keys(None, 0, None, None, None) == 0

@@ -77,3 +77,46 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _key(logit, token):
+    """A key in the order the library's keys follow: larger logit, then lower token id,
+    as a signed 64-bit integer (used here only to feed the exchange step)."""
+    import struct
+    bits = struct.unpack("<I", struct.pack("<f", logit))[0]
+    ordv = bits | 0x80000000 if bits < 0x80000000 else (~bits) & 0xFFFFFFFF
+    u = (ordv << 32) | (0xFFFFFFFF - token)
+    u ^= 1 << 63
+    return u - (1 << 64) if u >= 1 << 63 else u
+
+
+def _combine_main(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    dist.init_process_group("gloo", init_method="env://", rank=rank, world_size=ws)
+    try:
+        from centroid_masked_sparse_gb300 import combine_keys
+        # row 0: rank 1 has the larger logit; row 1: equal logits, rank 0 has the lower id;
+        # row 2: only rank 0 has a candidate (rank 1 reports "none"); row 3: negative logits
+        mine = {0: [_key(1.5, 10), _key(2.0, 7), _key(0.25, 3), _key(-3.0, 5)],
+                1: [_key(2.5, 99), _key(2.0, 8), -(1 << 63), _key(-2.0, 6)]}[rank]
+        keys = torch.tensor(mine, dtype=torch.int64)
+        combine_keys(keys)
+        q.put((rank, keys.tolist()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sharded_argmax_exchange_is_a_max_all_reduce():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_combine_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    res = dict(q.get(timeout=5) for _ in range(2))
+    want = [_key(2.5, 99), _key(2.0, 7), _key(0.25, 3), _key(-2.0, 6)]
+    assert res[0] == want and res[1] == want

@@ -260,7 +260,7 @@ def _full_check(m, oh, dh, hidden, what):
     return ref
 
 
-@pytest.mark.parametrize("H", [8, 72, 264, 4096])
+@pytest.mark.parametrize("H", [8, 72, 256, 264, 4096])
 def test_hidden_sizes(build_lib, H):
     m = build_lib
     t, oh, dh = _custom(m, 2048, H, 32, 3, seed=H)
@@ -774,3 +774,73 @@ def test_captured_pair_graph(build_lib):
             assert torch.equal(lg, elg) and torch.equal(ids, eids)
         finally:
             g.close()
+
+
+@pytest.mark.parametrize("B,packed", [(1, False), (8, False), (64, False), (64, True)])
+def test_draft256_full_size(build_lib, B, packed):
+    """The H=256 draft-dimension workload at Gemma scale (V=262144, C=2048, K=32)."""
+    m = build_lib
+    oh, dh = device_head(m, "draft256")
+    if packed:
+        dh.use_packed_table()
+    try:
+        hidden, ref = check_topk(m, "draft256", B)
+        if B == 64:
+            check_selection(m, dh, oh, hidden, ref["sel"])
+    finally:
+        if packed:
+            dh.drop_packed_table()
+
+
+# ---------------------------------------------------------------------------
+# cluster-sharded head (shards emulated on one GPU, combined by an elementwise max)
+
+
+@pytest.mark.parametrize("name,B,packed,shards", [
+    ("uniform", 8, False, 2),
+    ("uniform", 64, False, 3),
+    ("uniform", 64, True, 2),       # per-shard packed tables: the tensor-core gather
+    ("shared", 256, False, 2),      # large buckets
+    ("variable", 64, False, 3),
+])
+def test_sharded_head_equals_unsharded(build_lib, name, B, packed, shards):
+    """Each shard gathers only its clusters; the max of the shards' keys decodes to the
+    unsharded argmax and the max of their scatter rows is the unsharded scatter, bit
+    for bit (every candidate's logit is computed by one shard, with the same arithmetic)."""
+    m = build_lib
+    oh, dh = device_head(m, name)
+    hidden = synth.hidden_batch(name, B, None, helpers.tables(name).prototypes, row0=123)
+    h = helpers.bf16_tensor(hidden)
+    C = oh.C
+    cuts = [round(i * C / shards) for i in range(shards + 1)]
+    heads = [m.MaskedHead(dh.centroid_w, dh.embed_w, dh.token_ordering, oh.K, dh.cluster_offsets,
+                          vocab_size=oh.V, cluster_range=(cuts[i], cuts[i + 1])) for i in range(shards)]
+    if packed:
+        dh.use_packed_table()
+        full = m.mtp_packed_embeddings_bytes(dh)
+        for sh in heads:
+            sh.use_packed_table()
+            assert sh.embed_packed.numel() < full / shards + 2 * 16384 * 24 + 4 * (C + 1)
+    try:
+        ref_tok, ref_max = m.mtp_masked_topk_tokens(dh, h)
+        ref_sc = m.mtp_masked_scatter_logits(dh, h)
+        keys = [m.mtp_masked_topk_keys(sh, h) for sh in heads]
+        scs = [m.mtp_masked_scatter_logits(sh, h) for sh in heads]
+        combined = keys[0].clone()
+        for k in keys[1:]:
+            combined = torch.maximum(combined, k)
+        tok, mx = m.mtp_decode_keys(combined)
+        sc = scs[0].clone()
+        for x in scs[1:]:
+            sc = torch.maximum(sc, x)
+        torch.cuda.synchronize()
+        assert torch.equal(tok, ref_tok) and torch.equal(mx, ref_max)
+        assert torch.equal(sc, ref_sc)
+        # each shard wrote only its own clusters' tokens
+        finite = [torch.isfinite(x).sum().item() for x in scs]
+        assert sum(finite) == torch.isfinite(ref_sc).sum().item()
+        for sh in heads:
+            assert m.mtp_read_device_error(sh.workspace(B)) == 0
+    finally:
+        if packed:
+            dh.drop_packed_table()
