@@ -32,6 +32,17 @@
  *   - a row whose selected clusters are all empty has no candidate: its token
  *     is -1 and its max logit -inf.
  *
+ * Reference-fidelity options (the `flags` argument; 0 is the reading above):
+ *   ORC_FLAG_FILL_FINFO_MIN  forward fills with bf16's finite minimum, the
+ *                            value the page's code uses (finfo(dtype).min);
+ *   ORC_FLAG_BF16_SCORES     the selection uses the centroid scores rounded to
+ *                            bf16, as the page's bf16 Linear returns them;
+ *   ORC_FLAG_BF16_LOGITS     the sparse (and dense) logits are rounded to bf16,
+ *                            as the page's bf16 einsum returns them, before the
+ *                            argmax and the scatter.
+ * Rounding to bf16 is round-to-nearest-even of the exact fp64 value to 8
+ * significant bits (bf16's exponent range, its subnormals included).
+ *
  * Parity pins live in tests/test_oracle_pins.py (hand-worked example, brute
  * force top-K by subset enumeration, K=C and C=1 dense identities, integer
  * exact cases, invariants).
@@ -46,6 +57,31 @@
 #define ORC_OK 0
 #define ORC_ERR_ARG -1
 #define ORC_ERR_NOMEM -2
+
+#define ORC_FLAG_FILL_FINFO_MIN 1
+#define ORC_FLAG_BF16_SCORES 2
+#define ORC_FLAG_BF16_LOGITS 4
+
+/* bf16's largest finite value, (2 - 2^-7) * 2^127. */
+#define ORC_BF16_MAX 3.3895313892515355e38
+
+/* x rounded to the nearest bf16 value, ties to even: 8 significant bits while
+ * |x| >= 2^-126, a fixed quantum of 2^-133 below (bf16 subnormals), infinity
+ * beyond ORC_BF16_MAX after rounding. */
+double orc_round_bf16(double x)
+{
+    if (x == 0.0 || !isfinite(x))
+        return x;
+    int e;
+    frexp(x, &e);                 /* |x| in [2^(e-1), 2^e) */
+    int q = e - 8;                /* exponent of the last of 8 significant bits */
+    if (q < -133)
+        q = -133;
+    double r = ldexp(nearbyint(ldexp(x, -q)), q);   /* nearbyint: nearest, ties even */
+    if (fabs(r) > ORC_BF16_MAX)
+        return r > 0 ? INFINITY : -INFINITY;
+    return r;
+}
 
 /* bf16 bit pattern -> exact double. */
 static double bf16_value(uint16_t bits)
@@ -152,7 +188,7 @@ static void select_and_score_row(const uint16_t *h_row, int64_t H,
                                  const uint16_t *embed_w, int64_t ld_embed,
                                  const int32_t *ordering, const int32_t *off,
                                  int64_t V, int64_t C, const int32_t *sel, int64_t K,
-                                 int32_t *tokens, double *logits)
+                                 int32_t *tokens, double *logits, int64_t flags)
 {
     int64_t j = 0;
     for (int64_t k = 0; k < K; ++k) {
@@ -162,6 +198,8 @@ static void select_and_score_row(const uint16_t *h_row, int64_t H,
             int32_t t = ordering[p];
             tokens[j] = t;
             logits[j] = dot_bf16(h_row, embed_w + (int64_t)t * ld_embed, H);
+            if (flags & ORC_FLAG_BF16_LOGITS)
+                logits[j] = orc_round_bf16(logits[j]);
             ++j;
         }
     }
@@ -182,7 +220,7 @@ int orc_masked_topk_tokens(const uint16_t *hidden, int64_t b0, int64_t b1, int64
                            const uint16_t *embed_w, int64_t ld_embed, int64_t V,
                            const int32_t *ordering, const int32_t *off,
                            int32_t *tokens, double *max_logit, double *score_margin,
-                           double *logit_margin, int32_t *sel_out, int64_t *n_cand)
+                           double *logit_margin, int32_t *sel_out, int64_t *n_cand, int64_t flags)
 {
     if (!hidden || !centroid_w || !embed_w || !ordering || !tokens || H <= 0 || C <= 0 ||
         K <= 0 || K > C || V <= 0 || ld_embed < H || b0 < 0 || b1 < b0)
@@ -199,8 +237,11 @@ int orc_masked_topk_tokens(const uint16_t *hidden, int64_t b0, int64_t b1, int64
     int rc = ORC_OK;
     for (int64_t b = b0; b < b1 && rc == ORC_OK; ++b) {
         const uint16_t *h_row = hidden + b * H;
-        for (int64_t c = 0; c < C; ++c)
+        for (int64_t c = 0; c < C; ++c) {
             scores[c] = dot_bf16(h_row, centroid_w + c * H, H);
+            if (flags & ORC_FLAG_BF16_SCORES)
+                scores[c] = orc_round_bf16(scores[c]);
+        }
         double smargin;
         rc = orc_topk_row(scores, C, K, sel, &smargin);
         if (rc != ORC_OK)
@@ -215,7 +256,7 @@ int orc_masked_topk_tokens(const uint16_t *hidden, int64_t b0, int64_t b1, int64
             break;
         }
         select_and_score_row(h_row, H, embed_w, ld_embed, ordering, off, V, C, sel, K,
-                             cand_tok, cand_log);
+                             cand_tok, cand_log, flags);
         int32_t best_t = -1;
         double best = -INFINITY, second = -INFINITY;
         for (int64_t j = 0; j < n; ++j) {
@@ -254,7 +295,8 @@ int orc_masked_topk_tokens(const uint16_t *hidden, int64_t b0, int64_t b1, int64
 int orc_masked_scatter_logits(const uint16_t *hidden, int64_t b0, int64_t b1, int64_t H,
                               const uint16_t *centroid_w, int64_t C, int64_t K,
                               const uint16_t *embed_w, int64_t ld_embed, int64_t V,
-                              const int32_t *ordering, const int32_t *off, double *out)
+                              const int32_t *ordering, const int32_t *off, double *out,
+                              int64_t flags)
 {
     if (!hidden || !centroid_w || !embed_w || !ordering || !out || H <= 0 || C <= 0 ||
         K <= 0 || K > C || V <= 0 || ld_embed < H || b0 < 0 || b1 < b0)
@@ -272,10 +314,14 @@ int orc_masked_scatter_logits(const uint16_t *hidden, int64_t b0, int64_t b1, in
     for (int64_t b = b0; b < b1 && rc == ORC_OK; ++b) {
         const uint16_t *h_row = hidden + b * H;
         double *row = out + b * V;
+        const double fill = (flags & ORC_FLAG_FILL_FINFO_MIN) ? -ORC_BF16_MAX : -INFINITY;
         for (int64_t t = 0; t < V; ++t)
-            row[t] = -INFINITY;
-        for (int64_t c = 0; c < C; ++c)
+            row[t] = fill;
+        for (int64_t c = 0; c < C; ++c) {
             scores[c] = dot_bf16(h_row, centroid_w + c * H, H);
+            if (flags & ORC_FLAG_BF16_SCORES)
+                scores[c] = orc_round_bf16(scores[c]);
+        }
         rc = orc_topk_row(scores, C, K, sel, NULL);
         if (rc != ORC_OK)
             break;
@@ -289,7 +335,7 @@ int orc_masked_scatter_logits(const uint16_t *hidden, int64_t b0, int64_t b1, in
             break;
         }
         select_and_score_row(h_row, H, embed_w, ld_embed, ordering, off, V, C, sel, K,
-                             cand_tok, cand_log);
+                             cand_tok, cand_log, flags);
         for (int64_t j = 0; j < n; ++j)
             row[cand_tok[j]] = cand_log[j];
         free(cand_tok);
@@ -308,7 +354,8 @@ int orc_select_and_score_row(const uint16_t *hidden, int64_t b, int64_t H,
                              const uint16_t *centroid_w, int64_t C, int64_t K,
                              const uint16_t *embed_w, int64_t ld_embed, int64_t V,
                              const int32_t *ordering, const int32_t *off,
-                             int32_t *tokens, double *logits, int64_t cap, int64_t *n)
+                             int32_t *tokens, double *logits, int64_t cap, int64_t *n,
+                             int64_t flags)
 {
     if (!hidden || !centroid_w || !embed_w || !ordering || !tokens || !logits || !n ||
         K <= 0 || K > C || (!off && V % C != 0))
@@ -321,8 +368,11 @@ int orc_select_and_score_row(const uint16_t *hidden, int64_t b, int64_t H,
         return ORC_ERR_NOMEM;
     }
     const uint16_t *h_row = hidden + b * H;
-    for (int64_t c = 0; c < C; ++c)
+    for (int64_t c = 0; c < C; ++c) {
         scores[c] = dot_bf16(h_row, centroid_w + c * H, H);
+        if (flags & ORC_FLAG_BF16_SCORES)
+            scores[c] = orc_round_bf16(scores[c]);
+    }
     int rc = orc_topk_row(scores, C, K, sel, NULL);
     if (rc == ORC_OK) {
         *n = candidate_count(sel, K, V, C, off);
@@ -330,7 +380,7 @@ int orc_select_and_score_row(const uint16_t *hidden, int64_t b, int64_t H,
             rc = ORC_ERR_ARG;
         else
             select_and_score_row(h_row, H, embed_w, ld_embed, ordering, off, V, C, sel, K,
-                                 tokens, logits);
+                                 tokens, logits, flags);
     }
     free(scores);
     free(sel);
@@ -340,13 +390,18 @@ int orc_select_and_score_row(const uint16_t *hidden, int64_t b, int64_t H,
 /* Dense comparator (the LogitsProcessor path without softcapping): out[b, t]
  * = sum_h h[b,h] E[t,h] for rows [b0, b1) and every token t < V. */
 int orc_dense_logits(const uint16_t *hidden, int64_t b0, int64_t b1, int64_t H,
-                     const uint16_t *embed_w, int64_t ld_embed, int64_t V, double *out)
+                     const uint16_t *embed_w, int64_t ld_embed, int64_t V, double *out,
+                     int64_t flags)
 {
     if (!hidden || !embed_w || !out || H <= 0 || V <= 0 || ld_embed < H || b0 < 0 || b1 < b0)
         return ORC_ERR_ARG;
     for (int64_t b = b0; b < b1; ++b)
         for (int64_t t = 0; t < V; ++t)
+        {
             out[b * V + t] = dot_bf16(hidden + b * H, embed_w + t * ld_embed, H);
+            if (flags & ORC_FLAG_BF16_LOGITS)
+                out[b * V + t] = orc_round_bf16(out[b * V + t]);
+        }
     return ORC_OK;
 }
 

@@ -47,12 +47,12 @@ _SIGS = {
     "orc_centroid_scores": [_p, _i64, _i64, _i64, _p, _i64, _p],
     "orc_topk_row": [_p, _i64, _i64, _p, _p],
     "orc_masked_topk_tokens": [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64, _i64,
-                               _p, _p, _p, _p, _p, _p, _p, _p],
+                               _p, _p, _p, _p, _p, _p, _p, _p, _i64],
     "orc_masked_scatter_logits": [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64,
-                                  _i64, _p, _p, _p],
+                                  _i64, _p, _p, _p, _i64],
     "orc_select_and_score_row": [_p, _i64, _i64, _p, _i64, _i64, _p, _i64, _i64,
-                                 _p, _p, _p, _p, _i64, _p],
-    "orc_dense_logits": [_p, _i64, _i64, _i64, _p, _i64, _i64, _p],
+                                 _p, _p, _p, _p, _i64, _p, _i64],
+    "orc_dense_logits": [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64],
     "orc_dense_logits_at": [_p, _i64, _p, _i64, _p, _p, _i64, _p],
     "orc_is_permutation": [_p, _i64],
 }
@@ -65,6 +65,8 @@ def load_library(path: str):
         f = getattr(L, name)
         f.argtypes = args
         f.restype = ctypes.c_int
+    L.orc_round_bf16.argtypes = [ctypes.c_double]
+    L.orc_round_bf16.restype = ctypes.c_double
     return L
 
 
@@ -75,6 +77,16 @@ def lib():
             build()
             _lib = load_library(_LIB_PATH)
     return _lib
+
+
+FLAG_FILL_FINFO_MIN = 1
+FLAG_BF16_SCORES = 2
+FLAG_BF16_LOGITS = 4
+
+
+def round_bf16(x: float) -> float:
+    """x rounded to the nearest bf16 value, ties to even (the oracle's own rounding)."""
+    return float(lib().orc_round_bf16(float(x)))
 
 
 def _ptr(a: np.ndarray | None):
@@ -103,9 +115,10 @@ class Head:
     embed_w      uint16 [V', ld] bf16 bits, token-id order, V' >= V, ld >= H
     ordering     int32  [V]      ordered position -> token id
     offsets      int32  [C+1] or None (uniform clusters of V/C)
+    flags        FLAG_* reference-fidelity options (0: fp64 scores and logits, -inf fill)
     """
 
-    def __init__(self, centroid_w, embed_w, ordering, offsets, top_k, vocab=None):
+    def __init__(self, centroid_w, embed_w, ordering, offsets, top_k, vocab=None, flags=0):
         self.centroid_w = np.ascontiguousarray(centroid_w, dtype=np.uint16)
         self.embed_w = np.ascontiguousarray(embed_w, dtype=np.uint16)
         self.ordering = np.ascontiguousarray(ordering, dtype=np.int32)
@@ -114,6 +127,7 @@ class Head:
         self.ld = self.embed_w.shape[1]
         self.V = int(vocab) if vocab is not None else int(self.ordering.shape[0])
         self.K = int(top_k)
+        self.flags = int(flags)
 
     @classmethod
     def from_tables(cls, t, top_k=None):
@@ -164,7 +178,7 @@ def masked_topk_tokens(head: Head, hidden: np.ndarray, threads: int | None = Non
             _ptr(hidden), r[0], r[1], head.H, _ptr(head.centroid_w), head.C, head.K,
             _ptr(head.embed_w), head.ld, head.V, _ptr(head.ordering), _ptr(head.offsets),
             _ptr(res["tokens"]), _ptr(res["max_logit"]), _ptr(res["score_margin"]),
-            _ptr(res["logit_margin"]), _ptr(res["sel"]), _ptr(res["n_cand"])),
+            _ptr(res["logit_margin"]), _ptr(res["sel"]), _ptr(res["n_cand"]), head.flags),
             "masked_topk_tokens")
 
     nt = _threads(threads)
@@ -186,7 +200,7 @@ def masked_scatter_logits(head: Head, hidden: np.ndarray, threads: int | None = 
         _check(L.orc_masked_scatter_logits(
             _ptr(hidden), r[0], r[1], head.H, _ptr(head.centroid_w), head.C, head.K,
             _ptr(head.embed_w), head.ld, head.V, _ptr(head.ordering), _ptr(head.offsets),
-            _ptr(out)), "masked_scatter_logits")
+            _ptr(out), head.flags), "masked_scatter_logits")
 
     nt = _threads(threads)
     with ThreadPoolExecutor(nt) as ex:
@@ -204,7 +218,7 @@ def select_and_score_row(head: Head, hidden: np.ndarray, b: int):
     _check(lib().orc_select_and_score_row(
         _ptr(hidden), b, head.H, _ptr(head.centroid_w), head.C, head.K, _ptr(head.embed_w),
         head.ld, head.V, _ptr(head.ordering), _ptr(head.offsets), _ptr(toks), _ptr(logs),
-        cap, ctypes.byref(n)), "select_and_score_row")
+        cap, ctypes.byref(n), head.flags), "select_and_score_row")
     return logs[:n.value].copy(), toks[:n.value].copy()
 
 
@@ -216,7 +230,7 @@ def dense_logits(head: Head, hidden: np.ndarray, threads: int | None = None) -> 
 
     def run(r):
         _check(L.orc_dense_logits(_ptr(hidden), r[0], r[1], head.H, _ptr(head.embed_w),
-                                  head.ld, head.V, _ptr(out)), "dense_logits")
+                                  head.ld, head.V, _ptr(out), head.flags), "dense_logits")
 
     nt = _threads(threads)
     with ThreadPoolExecutor(nt) as ex:

@@ -30,7 +30,12 @@ MUTATIONS = [
     ("subtracted products (wrong sign)",
      "s += bf16_value(x[i]) * bf16_value(w[i]);", "s -= bf16_value(x[i]) * bf16_value(w[i]);"),
     ("full-vocab fill of 0 instead of -inf",
-     "row[t] = -INFINITY;", "row[t] = 0.0;"),
+     "? -ORC_BF16_MAX : -INFINITY;", "? -ORC_BF16_MAX : 0.0;"),
+    ("bf16 rounding with ties away from zero",
+     "ldexp(nearbyint(ldexp(x, -q)), q)", "ldexp(round(ldexp(x, -q)), q)"),
+    ("bf16-score option rounds the logits instead",
+     "        if (flags & ORC_FLAG_BF16_SCORES)\n                scores[c] = orc_round_bf16(scores[c]);\n        }\n        double smargin;",
+     "        if (flags & ORC_FLAG_BF16_LOGITS)\n                scores[c] = orc_round_bf16(scores[c]);\n        }\n        double smargin;"),
     ("uniform clusters one position short",
      "*hi = (c + 1) * s;", "*hi = (c + 1) * s - 1;"),
     ("variable clusters read one offset too far",
@@ -53,7 +58,9 @@ def _pin_calls():
               ("k_eq_c", lambda: pins.test_k_equals_c_is_dense(5, [1, 30, 7, 0, 20, 11, 2, 25])),
               ("dense_numpy", lambda: pins.test_dense_matches_numpy_matmul(1)),
               ("single", pins.test_single_centroid_is_dense),
-              ("variable", pins.test_variable_cluster_candidate_counts)]
+              ("variable", pins.test_variable_cluster_candidate_counts),
+              ("round_bf16", pins.test_round_bf16_values),
+              ("flags", pins.test_fidelity_flags_hand_example)]
     return calls
 
 

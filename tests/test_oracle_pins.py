@@ -253,3 +253,56 @@ def test_generator_basics():
     a = synth.hidden_batch("uniform", 4)
     b = synth.hidden_batch("uniform", 4, attempts=np.array([0, 1, 0, 0]))
     assert (a[0] == b[0]).all() and (a[2] == b[2]).all() and not (a[1] == b[1]).all()
+
+
+def test_round_bf16_values():
+    """Round-to-nearest-even to bf16 (8 significant bits), values worked by hand."""
+    r = oracle.round_bf16
+    assert r(256.0) == 256.0
+    assert r(257.0) == 256.0            # midpoint of 256 and 258: the even mantissa (256)
+    assert r(259.0) == 260.0            # midpoint of 258 and 260: 260 is even
+    assert r(-257.0) == -256.0
+    assert r(257.5) == 258.0            # above the midpoint
+    assert r(1 + 2 ** -8) == 1.0        # midpoint of 1 and 1 + 2^-7
+    assert r(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    assert r(0.1) == 0.10009765625      # bf16 0x3DCD
+    assert r(2.0 ** -140) == 0.0        # below half the smallest subnormal 2^-133
+    assert r(3 * 2.0 ** -134) == 2 * 2.0 ** -133   # 1.5 quanta: the even multiple
+    assert r(3.3895313892515355e38) == 3.3895313892515355e38
+    assert r(3.4e38) == float("inf")
+    assert r(0.0) == 0.0
+
+
+def _flag_head(flags):
+    # C = 2 centroids of H = 2: h = (1, 1) scores 256 and 257; clusters of 2 positions,
+    # ordering [3, 0, 1, 2]: centroid 0 owns tokens 3 and 0, centroid 1 tokens 1 and 2
+    one, big = 0x3F80, 0x4380          # bf16 1.0 and 256.0
+    cw = np.array([[big, 0], [big, one]], np.uint16)
+    ew = np.array([[big, 0], [one, 0], [0, one], [big, one]], np.uint16)   # token rows 0..3
+    return oracle.Head(cw, ew, np.array([3, 0, 1, 2], np.int32), None, 1, flags=flags)
+
+
+def test_fidelity_flags_hand_example():
+    h = np.array([[0x3F80, 0x3F80]], np.uint16)
+    # plain reading: centroid 1 (257 > 256), tokens 1 and 2 both score 1: lower id
+    r = oracle.masked_topk_tokens(_flag_head(0), h, threads=1)
+    assert r["sel"].tolist() == [[1]] and r["tokens"].tolist() == [1] and r["max_logit"][0] == 1.0
+    # bf16 scores: 257 rounds to 256, a tie with centroid 0, whose lower index wins; its
+    # tokens 3 and 0 score 257 and 256
+    f = oracle.FLAG_BF16_SCORES
+    r = oracle.masked_topk_tokens(_flag_head(f), h, threads=1)
+    assert r["sel"].tolist() == [[0]] and r["tokens"].tolist() == [3] and r["max_logit"][0] == 257.0
+    # bf16 logits too: 257 -> 256 ties with token 0, the lower id
+    f = oracle.FLAG_BF16_SCORES | oracle.FLAG_BF16_LOGITS
+    r = oracle.masked_topk_tokens(_flag_head(f), h, threads=1)
+    assert r["tokens"].tolist() == [0] and r["max_logit"][0] == 256.0
+    logs, toks = oracle.select_and_score_row(_flag_head(f), h, 0)
+    assert toks.tolist() == [3, 0] and logs.tolist() == [256.0, 256.0]
+    # finite fill: bf16's largest negative value where the page's code puts finfo.min
+    f = oracle.FLAG_BF16_SCORES | oracle.FLAG_FILL_FINFO_MIN
+    sc = oracle.masked_scatter_logits(_flag_head(f), h, threads=1)
+    m = -3.3895313892515355e38
+    assert sc.tolist() == [[256.0, m, m, 257.0]]
+    # dense logits with bf16 rounding
+    d = oracle.dense_logits(_flag_head(oracle.FLAG_BF16_LOGITS), h, threads=1)
+    assert d.tolist() == [[256.0, 1.0, 1.0, 256.0]]
