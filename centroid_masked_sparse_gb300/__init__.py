@@ -20,7 +20,8 @@ import ctypes
 from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_MAX_BATCH,
                    MtpError, MtpHeadDesc, check, lib)
 
-__all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "MTP_FINISH_PAIR", "mtp_workspace_bytes", "mtp_centroid_scores",
+__all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "MTP_FINISH_PAIR",
+           "MTP_FLAG_FILL_FINFO_MIN", "MTP_FLAG_BF16_SCORES", "MTP_FLAG_BF16_LOGITS", "mtp_workspace_bytes", "mtp_centroid_scores",
            "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_select_and_score", "mtp_dense_lm_head",
            "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
            "mtp_masked_topk_keys", "mtp_decode_keys", "combine_keys", "sharded_topk_tokens",
@@ -53,10 +54,11 @@ class MaskedHead:
     cluster_offsets  int32 [C + 1] or None (uniform clusters of V / C)
     cluster_range    (begin, end): the clusters this GPU owns when the head is sharded
                      over GPUs by cluster, or None for all of them
+    flags            MTP_FLAG_* reference-fidelity options (0: fp32 scores and logits, -inf)
     """
 
     def __init__(self, centroid_w, embed_w, token_ordering, top_k, cluster_offsets=None,
-                 vocab_size=None, embed_packed=None, cluster_range=None):
+                 vocab_size=None, embed_packed=None, cluster_range=None, flags=0):
         torch = _torch()
         if centroid_w is not None:
             assert centroid_w.dtype == torch.bfloat16 and centroid_w.is_contiguous()
@@ -76,7 +78,7 @@ class MaskedHead:
         self.vocab_size, self.hidden_size, self.num_centroids, self.top_k = V, H, C, int(top_k)
         self.desc = MtpHeadDesc(
             vocab_size=V, hidden_size=H, num_centroids=C, top_k=int(top_k),
-            device=self.device.index or 0, reserved0=0,
+            device=self.device.index or 0, flags=int(flags),
             centroid_w=None if centroid_w is None else centroid_w.data_ptr(),
             embed_w=embed_w.data_ptr(), ld_embed=int(embed_w.stride(0)),
             token_ordering=None if token_ordering is None else token_ordering.data_ptr(),
@@ -251,6 +253,7 @@ def mtp_gather_plan(head, batch: int) -> str:
 
 
 MTP_FINISH_ARGMAX, MTP_FINISH_SCATTER, MTP_FINISH_PAIR = 0, 1, 2
+MTP_FLAG_FILL_FINFO_MIN, MTP_FLAG_BF16_SCORES, MTP_FLAG_BF16_LOGITS = 1, 2, 4
 
 
 class CapturedCalls:

@@ -35,7 +35,7 @@ class MtpHeadDesc(ctypes.Structure):
         ("num_centroids", ctypes.c_int32),
         ("top_k", ctypes.c_int32),
         ("device", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
         ("centroid_w", ctypes.c_void_p),
         ("embed_w", ctypes.c_void_p),
         ("ld_embed", ctypes.c_int64),

@@ -1,6 +1,7 @@
 // Device helpers and launch parameters shared by the head's kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -109,6 +110,9 @@ __device__ __forceinline__ uint32_t ord_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// v rounded to the nearest bf16 value (ties to even), as an fp32 value.
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
 __device__ __forceinline__ float ord_value(uint32_t k)
 {
     uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
@@ -182,6 +186,7 @@ struct TopkParams {
     uint32_t *ctrl;
     int chunk;               // tokens per work item
     int c_begin, c_end;      // clusters this shard gathers (bucketing skips the others)
+    int bf16_scores;         // select on the scores rounded to bf16
 };
 
 struct GatherParams {
@@ -207,6 +212,7 @@ struct GatherParams {
     int32_t *out_ids;               // [B, sparse_width] or null
     const int32_t *topk;            // [B, K] the rows' selections (ranks for the sparse pair)
     int K;
+    int bf16_logits;                // round every logit to bf16 before storing or comparing it
     int B, H, V, S, W, C;
     int chunk;                      // ordered positions per work item
     int ring;                       // embedding-row slots per CTA

@@ -94,6 +94,7 @@ struct Params {
     int32_t *out_tokens;
     float *out_max;
     int sparse_width;         // sparse pair: row stride K*S of out_logits / out_ids; 0 otherwise
+    int bf16_logits;          // logits rounded to bf16 before they are stored or compared
     int32_t *out_ids;
     const int32_t *topk;      // [B, K]
     int K;
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 16; ++j) {
                     const int col = c0 + j;
                     if (col >= n) break;
-                    const float v = __uint_as_float(r[j]);
+                    const float v = p.bf16_logits ? round_bf16(__uint_as_float(r[j])) : __uint_as_float(r[j]);
                     const int row = m.rows[col];
                     if (SCATTER) {
                         if (tok >= 0) {
@@ -579,6 +580,7 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     p.out_tokens = g.out_tokens;
     p.out_max = g.out_max;
     p.sparse_width = g.sparse_width;
+    p.bf16_logits = g.bf16_logits;
     p.out_ids = g.out_ids;
     p.topk = g.topk;
     p.K = g.K;

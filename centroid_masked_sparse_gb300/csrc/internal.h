@@ -56,7 +56,7 @@ cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s
 constexpr int kTcGatherChunk = 128;
 // Expected rows per selected cluster (B*K/C) from which the tensor-core gather is used.
 constexpr int kTcGatherMinReuse = 4;
-cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s);
+cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s);
 // The packed embedding table of the tensor-core gather (gather_tc.cu): byte size for
 // the shapes (an upper bound with explicit offsets) and the kernels that fill it.
 // n = clusters the table holds (a shard's [c0, c1), or all C).
@@ -83,6 +83,7 @@ struct TcGemmArgs {
     uint32_t *ctrl;         // workspace control words: ticket for keys, error word
     int32_t *out_tokens;    // with keys
     float *out_max;         // with keys, optional
+    bool round_bf16;        // round each output to bf16 first (dense head option)
     uint32_t *zero;         // words cleared at kernel start (may be null)
     int zero_words;
 };

@@ -2,6 +2,7 @@
 // layout and the launch sequence of each call.  Declarations and the contract
 // of every entry point are in include/mtp_head.h.
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 #include <unordered_map>
 
@@ -169,6 +170,8 @@ mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool o
         if (!aligned16(d->centroid_w)) return MTP_ERR_ALIGN;
         if (!span_ok(d)) return MTP_ERR_SHAPE;
     }
+    if (d->flags & ~(MTP_FLAG_FILL_FINFO_MIN | MTP_FLAG_BF16_SCORES | MTP_FLAG_BF16_LOGITS))
+        return MTP_ERR_UNSUPPORTED;
     if (ordering && !d->cluster_offsets && d->vocab_size % d->num_centroids != 0) return MTP_ERR_SHAPE;
     return MTP_OK;
 }
@@ -254,6 +257,7 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
     }
     if (!topk) return MTP_OK;
     TopkParams tp{};
+    tp.bf16_scores = (d->flags & MTP_FLAG_BF16_SCORES) ? 1 : 0;
     tp.scores = scores;
     tp.topk = topk;
     tp.B = B;
@@ -336,7 +340,8 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     char *ws = (char *)workspace;
     if (out_logits && !sparse) {
         Prof pr(MTP_KERNEL_FILL, s);
-        st = cuda_status(launch_fill_neg_inf(out_logits, (size_t)B * d->vocab_size, s));
+        const float fill = (d->flags & MTP_FLAG_FILL_FINFO_MIN) ? -3.3895313892515355e38f : -INFINITY;
+        st = cuda_status(launch_fill(out_logits, (size_t)B * d->vocab_size, fill, s));
         if (st != MTP_OK) return st;
     }
     int chunk = 0;
@@ -365,6 +370,7 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     gp.out_tokens = out_tokens;
     gp.out_max = out_max;
     gp.topk = (const int32_t *)(ws + L.topk);
+    gp.bf16_logits = (d->flags & MTP_FLAG_BF16_LOGITS) ? 1 : 0;
     gp.K = d->top_k;
     gp.sparse_width = sparse ? d->top_k * (d->vocab_size / d->num_centroids) : 0;
     gp.out_ids = sparse ? out_ids : nullptr;
@@ -488,6 +494,7 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
     g.K = desc->hidden_size;
     g.splits = 1;
     g.out = out_logits;
+    g.round_bf16 = (desc->flags & MTP_FLAG_BF16_LOGITS) != 0;
     g.ldo = desc->vocab_size;
     g.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
     g.ctrl = out_tokens ? (uint32_t *)ws : nullptr;

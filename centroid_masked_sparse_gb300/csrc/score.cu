@@ -377,7 +377,8 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
                         a3 = fma2_bf16(e[c].w, x.w, a3);
                     }
                 }
-                const float acc = warp_sum((a0 + a1) + (a2 + a3));
+                float acc = warp_sum((a0 + a1) + (a2 + a3));
+                if (p.bf16_logits) acc = round_bf16(acc);
                 if (lane == r) {
                     const int row = hm.rows[r];
                     if (SCATTER) {
@@ -560,9 +561,10 @@ cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s)
 
 // forward's fill: every entry of the [B, V] row block is -inf before the
 // scatter writes the candidates' logits.
-__global__ void __launch_bounds__(256) k_fill_neg_inf(float *out, size_t n)
+// The scatter's background: -inf, or bf16's finite minimum under the fidelity option.
+__global__ void __launch_bounds__(256) k_fill(float *out, size_t n, float value)
 {
-    const float ninf = __int_as_float(0xff800000);
+    const float ninf = value;
     const float4 v = make_float4(ninf, ninf, ninf, ninf);
     float4 *o4 = reinterpret_cast<float4 *>(out);
     const size_t n4 = n / 4;
@@ -604,11 +606,11 @@ cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, floa
     return cudaGetLastError();
 }
 
-cudaError_t launch_fill_neg_inf(float *out, size_t n, cudaStream_t s)
+cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s)
 {
-    const int per_sm = blocks_per_sm((const void *)k_fill_neg_inf, 256, 0);
+    const int per_sm = blocks_per_sm((const void *)k_fill, 256, 0);
     const int grid = sm_count() * (per_sm > 0 ? per_sm : 1);
-    k_fill_neg_inf<<<grid, 256, 0, s>>>(out, n);
+    k_fill<<<grid, 256, 0, s>>>(out, n, value);
     return cudaGetLastError();
 }
 

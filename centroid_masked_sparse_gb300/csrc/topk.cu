@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     const float *row = p.scores + (size_t)b * p.C;
     float lmin = __int_as_float(0x7f800000), lmax = __int_as_float(0xff800000);
     for (int c = tid; c < p.C; c += kTopkThreads) {
-        const float v = row[c];
+        const float v = p.bf16_scores ? round_bf16(row[c]) : row[c];
         keys[c] = ord_key(v);
         lmin = fminf(lmin, v);
         lmax = fmaxf(lmax, v);

@@ -123,13 +123,32 @@ typedef enum mtp_status {
  *                    the whole row), and a packed table holds only these clusters.
  *                    embed_w stays indexed by token id; only the rows of this
  *                    shard's tokens are read. */
+/* Reference-fidelity options (desc->flags; 0 = the library's default reading:
+ * fp32 scores and logits, -inf fill).  The page's head runs in the model dtype,
+ * bf16 ("Add Gemma4 MTP speculative decoding with centroids masking",
+ * gemma4_mtp.py, Gemma4MTPMaskedEmbedder._select_and_score and forward):
+ *   MTP_FLAG_FILL_FINFO_MIN  the full-vocabulary scatter fills with bf16's finite
+ *                            minimum (-3.3895314e38, torch.finfo(bfloat16).min)
+ *                            instead of -inf;
+ *   MTP_FLAG_BF16_SCORES     the top-K selects on the centroid scores rounded to
+ *                            bf16 (round to nearest even; ties then go to the
+ *                            lower centroid index); the fp32 scores that
+ *                            mtp_centroid_scores returns are not rounded;
+ *   MTP_FLAG_BF16_LOGITS     every sparse and dense logit is rounded to bf16 before
+ *                            it is stored and before the argmax (ties then go to
+ *                            the lower token id); outputs stay fp32 arrays.
+ * Other bits: MTP_ERR_UNSUPPORTED. */
+#define MTP_FLAG_FILL_FINFO_MIN 1
+#define MTP_FLAG_BF16_SCORES 2
+#define MTP_FLAG_BF16_LOGITS 4
+
 typedef struct mtp_head_desc {
     int32_t vocab_size;
     int32_t hidden_size;
     int32_t num_centroids;
     int32_t top_k;
     int32_t device;
-    int32_t reserved0;
+    int32_t flags;
     const void *centroid_w;
     const void *embed_w;
     int64_t ld_embed;

@@ -48,7 +48,7 @@ def _desc(V=262144, H=1536, C=2048, K=32, cw=0x1000, ew=0x2000, ordering=0x3000,
           ld=None):
     from centroid_masked_sparse_gb300._lib import MtpHeadDesc
     return MtpHeadDesc(vocab_size=V, hidden_size=H, num_centroids=C, top_k=K, device=0,
-                       reserved0=0, centroid_w=cw, embed_w=ew, ld_embed=ld if ld else H,
+                       flags=0, centroid_w=cw, embed_w=ew, ld_embed=ld if ld else H,
                        token_ordering=ordering, cluster_offsets=offsets)
 
 
@@ -235,3 +235,13 @@ def test_cluster_range_checks_and_packed_size(L):
     assert L.mtp_decode_keys(keys, 4, None, None, None) == -1
     assert L.mtp_decode_keys(keys, -1, out, None, None) == -2
     assert L.mtp_decode_keys(None, 0, None, None, None) == 0
+
+
+def test_unknown_flags_are_refused(L):
+    out = ctypes.c_void_p(0x8000)
+    d = _desc()
+    d.flags = 8
+    assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 1 << 30, None) == -6
+    assert L.mtp_dense_lm_head(ctypes.byref(d), FAKE, 4, out, None, None, None, 0, None) == -6
+    d.flags = 7
+    assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 16, None) == -4

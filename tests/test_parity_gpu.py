@@ -844,3 +844,54 @@ def test_sharded_head_equals_unsharded(build_lib, name, B, packed, shards):
     finally:
         if packed:
             dh.drop_packed_table()
+
+
+# ---------------------------------------------------------------------------
+# reference-fidelity options (bf16 scores and logits, finite fill)
+
+
+@pytest.mark.parametrize("flags", [2, 4, 6, 7])
+@pytest.mark.parametrize("B,K,packed", [(12, 3, False), (32, 8, False), (32, 8, True)])
+def test_fidelity_flags_integer_inputs(build_lib, flags, B, K, packed):
+    """Integer inputs large enough for bf16 rounding to bite (|sums| up to 8192, bf16
+    spacing up to 32): every sum is exact in fp32 and fp64 and both sides round the same
+    values to nearest even, so selection, argmax, scatter, pair and dense head must equal
+    the oracle bit for bit, many ties included."""
+    m = build_lib
+    g = np.random.default_rng(21 + flags)
+    V, C, H = 512, 16, 64
+    cw = synth.bf16_bits(g.integers(-8, 9, size=(C, H)).astype(np.float32))
+    ew = synth.bf16_bits(g.integers(-8, 9, size=(V, H)).astype(np.float32))
+    perm = g.permutation(V).astype(np.int32)
+    hid = synth.bf16_bits(g.integers(-16, 17, size=(B, H)).astype(np.float32))
+    oh = oracle.Head(cw, ew, perm, None, K, flags=flags)
+    dh = m.MaskedHead(helpers.bf16_tensor(cw), helpers.bf16_tensor(ew), torch.from_numpy(perm).cuda(), K,
+                      flags=flags)
+    if packed:
+        dh.use_packed_table()
+    h = helpers.bf16_tensor(hid)
+    scores, topk = m.mtp_centroid_scores(dh, h)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    plog, pids = m.mtp_select_and_score(dh, h)
+    dl, dtok, dmax = m.mtp_dense_lm_head(dh, h, want_tokens=True)
+    torch.cuda.synchronize()
+    ref = oracle.masked_topk_tokens(oh, hid)
+    np.testing.assert_array_equal(scores.cpu().numpy(), oracle.centroid_scores(oh, hid))   # unrounded
+    np.testing.assert_array_equal(topk.cpu().numpy(), ref["sel"])
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+    np.testing.assert_array_equal(mx.cpu().numpy(), ref["max_logit"])
+    np.testing.assert_array_equal(sc.cpu().numpy(), oracle.masked_scatter_logits(oh, hid).astype(np.float32))
+    for b in range(B):
+        rl, rt = oracle.select_and_score_row(oh, hid, b)
+        np.testing.assert_array_equal(pids[b].cpu().numpy(), rt)
+        np.testing.assert_array_equal(plog[b].cpu().numpy(), rl.astype(np.float32))
+    dref = oracle.dense_logits(oh, hid)
+    np.testing.assert_array_equal(dl.cpu().numpy(), dref.astype(np.float32))
+    np.testing.assert_array_equal(dtok.cpu().numpy(), np.argmax(dref, axis=1))
+    # the rounding really acts on these inputs: many scores and logits are not bf16 values
+    raw = oracle.centroid_scores(oh, hid)
+    assert sum(oracle.round_bf16(x) != x for x in raw.ravel()) > raw.size // 10
+    if flags & 4:
+        raw_d = oracle.dense_logits(oracle.Head(cw, ew, perm, None, K), hid)
+        assert (dref != raw_d).mean() > 0.1

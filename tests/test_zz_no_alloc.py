@@ -55,7 +55,7 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     from centroid_masked_sparse_gb300._lib import MtpHeadDesc
     # 1024 rows x 4096 centroids of fp32 scores alone need 16 MiB
     d = MtpHeadDesc(vocab_size=262144, hidden_size=2048, num_centroids=4096, top_k=128, device=0,
-                    reserved0=0, centroid_w=0x1000, embed_w=0x2000, ld_embed=2048,
+                    flags=0, centroid_w=0x1000, embed_w=0x2000, ld_embed=2048,
                     token_ordering=0x3000, cluster_offsets=None)
     assert L.mtp_workspace_bytes(ctypes.byref(d), 1024) > 8 << 20
     out = ctypes.c_void_p(0x8000)
