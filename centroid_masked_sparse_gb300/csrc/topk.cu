@@ -5,10 +5,11 @@
 // the centroid scores of each row.  Ties go to the lower centroid index, and
 // the selected list is written sorted by (score desc, index asc).
 //
-// One CTA per row.  Fast path: 256 buckets linear in the score between the
-// row's min and max; the candidates are the scores in the bucket of the K-th
-// largest and above (a few dozen for Gaussian-like scores), ranked exactly by
-// 64-bit (score, lower index) keys.  When that bucket is crowded (ties, odd
+// One CTA per row.  Fast path: in the pass that reads the scores, a histogram
+// over the top 10 bits of their order-preserving keys (1024 buckets, each a
+// half-octave of one sign); the candidates are the keys in the bucket of the
+// K-th largest and above (a few dozen for Gaussian-like scores), ranked exactly
+// by 64-bit (score, lower index) keys.  When that bucket is crowded (ties, odd
 // distributions) the fallback is a 4-pass radix select (8 bits a pass) over
 // order-preserving uint32 keys, then every key above the K-th plus the
 // lowest-indexed keys equal to it.  No sort of the C scores is needed.
@@ -54,15 +55,13 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int *s_scan, int *total
 }
 
 constexpr int kCandCap = 512;
-
-// Bucket of a score for the fast path: monotone non-decreasing in v (each float
-// step rounds monotonically), clamped so that any input stays in range.
-__device__ __forceinline__ int value_bucket(float v, float vmin, float scale)
-{
-    const float x = (v - vmin) * scale;
-    int q = x >= 0.f ? (int)x : 0;
-    return q > 255 ? 255 : q;
-}
+// Fast-path buckets: the top 10 bits of the order-preserving key (sign, exponent
+// and one mantissa bit: half-octaves).
+constexpr int kKeyBits = 10;
+constexpr int kKeyBuckets = 1 << kKeyBits;
+constexpr int kKeyShift = 32 - kKeyBits;
+static_assert(kKeyBuckets % kTopkThreads == 0, "whole buckets per thread");
+static_assert(kCandCap * 8 <= kKeyBuckets * 4, "the candidates reuse the histogram's memory");
 
 __device__ __forceinline__ unsigned long long select_key(uint32_t ord, int c)
 {
@@ -95,74 +94,52 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     extern __shared__ uint32_t sm[];
     uint32_t *keys = sm;                                      // [C]
     int32_t *sel = reinterpret_cast<int32_t *>(sm + p.C);     // [K]
-    __shared__ uint32_t hist[256];
+    // the histogram, then (once scanned) the candidate keys in the same memory
+    __shared__ __align__(8) uint32_t hist[kKeyBuckets];
+    unsigned long long *s_cand = reinterpret_cast<unsigned long long *>(hist);
     __shared__ int s_scan[kWarp + 1];
     __shared__ uint32_t s_digit, s_above;
-    __shared__ float s_min[kTopkThreads / kWarp], s_max[kTopkThreads / kWarp];
-    __shared__ unsigned long long s_cand[kCandCap];
     __shared__ int s_ncand;
 
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid / kWarp;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    for (int i = tid; i < kKeyBuckets; i += kTopkThreads) hist[i] = 0u;
+    if (tid == 0) s_ncand = 0;
+    __syncthreads();
     // the scores are written by the projection kernel that precedes this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const float *row = p.scores + (size_t)b * p.C;
-    float lmin = __int_as_float(0x7f800000), lmax = __int_as_float(0xff800000);
+
+    // Fast path: one pass reads the scores, keeps their order-preserving keys and
+    // histograms them by the keys' top bits (sign, exponent and one mantissa bit:
+    // buckets a half-octave wide, monotone in the score); the candidates are the
+    // keys in the bucket of the K-th largest and above, ranked exactly by 64-bit
+    // (score, lower index) keys.
     for (int c = tid; c < p.C; c += kTopkThreads) {
         const float v = p.bf16_scores ? round_bf16(row[c]) : row[c];
-        keys[c] = ord_key(v);
-        lmin = fminf(lmin, v);
-        lmax = fmaxf(lmax, v);
+        const uint32_t k = ord_key(v);
+        keys[c] = k;
+        atomicAdd(&hist[k >> kKeyShift], 1u);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
-        lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-    }
-    if (lane == 0) {
-        s_min[warp] = lmin;
-        s_max[warp] = lmax;
-    }
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
-    if (tid == 0) s_ncand = 0;
     __syncthreads();
-
-    // Fast path: 256 buckets linear in the score between the row's min and max (the
-    // Gaussian-like scores then spread over many buckets), the bucket holding the
-    // K-th largest score, and an exact rank of every score in or above it.
-    float vmin = s_min[0], vmax = s_max[0];
-    for (int w = 1; w < kTopkThreads / kWarp; ++w) {
-        vmin = fminf(vmin, s_min[w]);
-        vmax = fmaxf(vmax, s_max[w]);
-    }
-    const float span = vmax - vmin;
-    const float scale = (span > 0.f && span < __int_as_float(0x7f800000)) ? 255.5f / span : 0.f;
-    // the scores are read from global memory once: later passes take them back from the
-    // order-preserving keys in shared memory
-    for (int c = tid; c < p.C; c += kTopkThreads)
-        atomicAdd(&hist[value_bucket(ord_value(keys[c]), vmin, scale)], 1u);
-    __syncthreads();
-    if (tid < kWarp) {
-        uint32_t loc[8], sum = 0u;
+    // thread t owns the per buckets below kKeyBuckets - per*t, largest first
+    {
+        constexpr int per = kKeyBuckets / kTopkThreads;
+        uint32_t loc[per], sum = 0u;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            loc[j] = hist[255 - (lane * 8 + j)];
+        for (int j = 0; j < per; ++j) {
+            loc[j] = hist[kKeyBuckets - 1 - (tid * per + j)];
             sum += loc[j];
         }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < kWarp; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - sum;
+        int total;
+        const uint32_t excl = (uint32_t)cta_exclusive_scan((int)sum, s_scan, &total);
         const uint32_t need = (uint32_t)p.K;
-        if (excl < need && need <= incl) {
+        if (excl < need && need <= excl + sum) {
             uint32_t run = excl;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < per; ++j) {
                 if (run + loc[j] >= need) {
-                    s_digit = 255u - (uint32_t)(lane * 8 + j);
+                    s_digit = (uint32_t)(kKeyBuckets - 1 - (tid * per + j));
                     s_above = run + loc[j];   // candidates: this bucket and every one above
                     break;
                 }
@@ -171,29 +148,38 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
         }
     }
     __syncthreads();
-    const int kbucket = (int)s_digit;
+    const uint32_t kbucket = s_digit;
     const int ncand = (int)s_above;
     if (ncand <= kCandCap) {
         for (int c = tid; c < p.C; c += kTopkThreads) {
-            if (value_bucket(ord_value(keys[c]), vmin, scale) >= kbucket) {
+            const uint32_t k = keys[c];
+            if ((k >> kKeyShift) >= kbucket) {
                 const int pos = atomicAdd(&s_ncand, 1);
-                s_cand[pos] = select_key(keys[c], c);
+                s_cand[pos] = select_key(k, c);
             }
         }
         __syncthreads();
-        for (int i = tid; i < ncand; i += kTopkThreads) {
+        // rank of each candidate = candidates with a larger key; with few candidates four
+        // threads (an aligned group of lanes) split one candidate's comparisons.  The
+        // thread that finds a rank below K stores and buckets that selection at once.
+        const int tpc = ncand <= kTopkThreads / 4 ? 4 : 1;
+        const int q = tid % tpc;
+        for (int i = tid / tpc; i < ncand; i += kTopkThreads / tpc) {
             const unsigned long long ki = s_cand[i];
             int rank = 0;
-            for (int j = 0; j < ncand; ++j) rank += s_cand[j] > ki;
-            if (rank < p.K) {
+#pragma unroll 4
+            for (int j = q; j < ncand; j += tpc) rank += s_cand[j] > ki;
+            if (tpc == 4) {
+                const unsigned grp = 0xfu << ((tid & (kWarp - 1)) & ~3);
+                rank += __shfl_xor_sync(grp, rank, 1);
+                rank += __shfl_xor_sync(grp, rank, 2);
+            }
+            if (q == 0 && rank < p.K) {
                 const int c = (int)(0xffffffffu - (uint32_t)(ki & 0xffffffffull));
                 p.topk[(size_t)b * p.K + rank] = c;
-                sel[rank] = c;
+                if (p.rowmask) bucket_selection(p, b, c);
             }
         }
-        __syncthreads();
-        if (p.rowmask)
-            for (int i = tid; i < p.K; i += kTopkThreads) bucket_selection(p, b, sel[i]);
         return;
     }
 
