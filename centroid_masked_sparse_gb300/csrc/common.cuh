@@ -170,6 +170,7 @@ struct ProjParams {
     int zero_words;
     int B, H, C;
     int rows_per_group;      // hidden rows staged in shared memory at a time
+    int after_fill;          // launched behind the scatter's fill, overlapping it
 };
 
 struct TopkParams {

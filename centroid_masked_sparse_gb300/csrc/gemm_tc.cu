@@ -326,6 +326,9 @@ __global__ void __launch_bounds__(kTcThreads)
         }
         cluster_sync_all();  // no CTA leaves while another still reads its shared memory
     }
+    // launched behind the scatter's fill (which it does not read): complete only after it,
+    // so that every later kernel of the call sees the fill done (no-op otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!p.keys) return;
     // the last CTA to finish turns the argmax keys into token ids
     __threadfence();
@@ -455,6 +458,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     if (!p.cluster_reduce) {
         int grid = sm_count();
         if (grid > p.units) grid = p.units;
+        if (a.after_fill) return launch_dependent(k_tc_gemm, dim3(grid), dim3(kTcThreads), smem, s, map_a, map_b, p);
         k_tc_gemm<<<grid, kTcThreads, smem, s>>>(map_a, map_b, p);
         return cudaGetLastError();
     }
@@ -464,13 +468,15 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)p.splits;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.after_fill ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, k_tc_gemm, map_a, map_b, p);
 }
 

@@ -84,6 +84,7 @@ struct TcGemmArgs {
     int32_t *out_tokens;    // with keys
     float *out_max;         // with keys, optional
     bool round_bf16;        // round each output to bf16 first (dense head option)
+    bool after_fill;        // launched behind the scatter's fill, overlapping it
     uint32_t *zero;         // words cleared at kernel start (may be null)
     int zero_words;
 };

@@ -220,7 +220,8 @@ mtp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MTP_OK : MTP_E
 
 // Steps 1-2: projection (+ workspace reset) and top-K (+ bucketing when rowmask is set).
 mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *scores,
-                      int32_t *topk, char *ws, const Layout *L, int chunk, cudaStream_t s)
+                      int32_t *topk, char *ws, const Layout *L, int chunk, cudaStream_t s,
+                      bool after_fill = false)
 {
     if (B >= kTcProjMinBatch) {
         // tensor cores: M = C centroid rows, N = batch, K = H, split-K in a cluster
@@ -237,6 +238,7 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
         g.ctrl = ws ? (uint32_t *)ws : nullptr;
         g.zero = ws ? (uint32_t *)ws : nullptr;
         g.zero_words = ws ? (int)(L->zero_end / sizeof(uint32_t)) : 0;
+        g.after_fill = after_fill;
         Prof pr(MTP_KERNEL_PROJECTION, s);
         mtp_status st = cuda_status(launch_tc_gemm(g, s));
         if (st != MTP_OK) return st;
@@ -251,6 +253,7 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
         pp.H = d->hidden_size;
         pp.C = d->num_centroids;
         pp.rows_per_group = proj_rows_per_group(B, d->hidden_size);
+        pp.after_fill = after_fill ? 1 : 0;
         Prof pr(MTP_KERNEL_PROJECTION, s);
         mtp_status st = cuda_status(launch_projection(pp, s));
         if (st != MTP_OK) return st;
@@ -346,7 +349,8 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     }
     int chunk = 0;
     const bool tc_gather = tc_gather_plan(d, B, &chunk);
-    st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s);
+    st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s,
+                    out_logits && !sparse);
     if (st != MTP_OK) return st;
 
     GatherParams gp{};

@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(kProjThreads) k_projection(ProjParams p)
             }
         }
     }
+    // launched behind the scatter's fill (which it does not read): complete only after it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int NCH>
@@ -81,6 +83,7 @@ static cudaError_t run_projection(const ProjParams &p, cudaStream_t s)
         return e;
     const int rows_per_cta = (kProjThreads / kWarp) * kProjRowsPerWarp;
     const int grid = (p.C + rows_per_cta - 1) / rows_per_cta;
+    if (p.after_fill) return launch_dependent(k_projection<NCH>, dim3(grid), dim3(kProjThreads), smem, s, p);
     k_projection<NCH><<<grid, kProjThreads, smem, s>>>(p);
     return cudaGetLastError();
 }

@@ -564,6 +564,10 @@ cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s)
 // The scatter's background: -inf, or bf16's finite minimum under the fidelity option.
 __global__ void __launch_bounds__(256) k_fill(float *out, size_t n, float value)
 {
+    // the projection and top-K that follow never read this buffer: let them start now
+    // (the projection waits for this kernel before it exits, so the gather, which runs
+    // after the top-K, writes into a finished fill)
+    asm volatile("griddepcontrol.launch_dependents;");
     const float ninf = value;
     const float4 v = make_float4(ninf, ninf, ninf, ninf);
     float4 *o4 = reinterpret_cast<float4 *>(out);
@@ -608,9 +612,9 @@ cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, floa
 
 cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s)
 {
-    const int per_sm = blocks_per_sm((const void *)k_fill, 256, 0);
-    const int grid = sm_count() * (per_sm > 0 ? per_sm : 1);
-    k_fill<<<grid, 256, 0, s>>>(out, n, value);
+    // two CTAs per SM: enough stores in flight for the write stream, and room left on
+    // every SM for the projection and top-K that start behind it
+    k_fill<<<sm_count() * 2, 256, 0, s>>>(out, n, value);
     return cudaGetLastError();
 }
 
