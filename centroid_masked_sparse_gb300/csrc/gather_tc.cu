@@ -30,8 +30,8 @@
 //            loads so that its dependent global reads (item record, row mask,
 //            token ids) never stall the stream;
 //   warp 6   TMA issue: per unit and k-block, one stage of A and B loads;
-//   warp 5   one thread issues tcgen05.mma (kind::f16, fp32 in TMEM, two
-//            accumulators so the epilogue of one unit overlaps the next);
+//   warp 5   one thread issues tcgen05.mma (kind::f16, fp32 in TMEM, four
+//            accumulators so the epilogues of the last units overlap the next);
 //   warps 0-3 epilogue: tcgen05.ld of the unit's logits (thread = candidate),
 //            then the scatter store or the per-row argmax fold.
 // Every mbarrier wait is bounded and records MTP_DEVERR_TIMEOUT if it gives up.
@@ -45,6 +45,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "internal.h"
@@ -60,12 +61,14 @@ constexpr int kThreads = 224;
 constexpr int kTileM = 128;        // MMA M: candidate positions per unit (at most)
 constexpr int kTileK = 64;         // bf16 per k-block (128-byte rows)
 constexpr int kMaxN = 128;         // bucket rows per unit (at most)
-constexpr int kMeta = 4;           // unit-metadata ring
+constexpr int kMeta = 8;           // unit-metadata ring
+constexpr int kAcc = 4;            // TMEM accumulators: the epilogues of the last units overlap the MMAs
 constexpr int kMaxStages = 32;
 constexpr uint32_t kRowBytes = kTileK * 2;
 constexpr uint32_t kFullABytes = kTileM * kRowBytes;   // what one M = 128 MMA reads
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kMetaReaders = 6;   // 4 epilogue warps + the MMA thread + the TMA warp
+constexpr int kNoPos = INT_MIN;        // a candidate slot past the chunk's end
 constexpr int kPackRows = 32;          // clusters are padded to multiples of this
 constexpr int kPackSuper = 128;        // rows per packed block
 constexpr uint32_t kPackBlock = kPackSuper * kRowBytes;  // 16384 bytes
@@ -124,11 +127,11 @@ __device__ __forceinline__ void timeout(const Params &p)
     atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TIMEOUT);
 }
 
-// Rows of the bucket of cluster c in row order, block `blk` (nmax rows per block):
-// the warp writes them to `rows` and returns how many (all lanes).
-__device__ int bucket_rows(const Params &p, int c, int blk, int lane, int *rows)
+// Rows of a bucket in row order, block `blk` (nmax rows per block), from the
+// bucket's row mask (word `lane` in w): the warp writes them to `rows` and returns
+// how many (all lanes).
+__device__ int bucket_rows(const Params &p, uint32_t w, int blk, int lane, int *rows)
 {
-    const uint32_t w = lane < p.W ? __ldcg(p.rowmask + (size_t)c * p.W + lane) : 0u;
     const int cnt = __popc(w);
     int incl = cnt;
 #pragma unroll
@@ -144,29 +147,68 @@ __device__ int bucket_rows(const Params &p, int c, int blk, int lane, int *rows)
     return max(0, min(p.nmax, total - lo));
 }
 
+// The metadata warp's view of one work item: its range and the loads its units
+// need (this lane's row-mask word and token ids, the packed group), issued one
+// item before they are used so that their latency overlaps the current item.
+struct ItemPre {
+    int valid;      // a real item with candidates
+    int c, y, lo, p0, nvalid, g0;
+    uint32_t w;     // row-mask word `lane` of the cluster
+    int tok[kTileM / kWarp];   // token ids at positions p0 + j*32 + lane (kNoPos beyond nvalid)
+};
+
+__device__ __forceinline__ void load_item(const Params &p, int2 rec, bool have, int lane, ItemPre &m)
+{
+    m.valid = 0;
+    m.c = rec.x;
+    m.y = rec.y;
+    m.lo = m.p0 = m.nvalid = m.g0 = 0;
+    m.w = 0u;
+#pragma unroll
+    for (int j = 0; j < kTileM / kWarp; ++j) m.tok[j] = kNoPos;
+    if (!have) return;
+    int lo = 0, hi = 0;
+    if ((unsigned)rec.x < (unsigned)p.C && rec.y >= 0)
+        cluster_range(p.offsets, p.V, p.S, rec.x, &lo, &hi, nullptr);
+    const int p0 = rec.y > hi - lo ? hi : lo + rec.y;
+    const int nvalid = max(0, min(p.chunk, hi - p0));
+    m.lo = lo;
+    m.p0 = p0;
+    m.nvalid = nvalid;
+    if (nvalid == 0) return;
+    m.valid = 1;
+    if (lane < p.W) m.w = __ldcg(p.rowmask + (size_t)rec.x * p.W + lane);
+#pragma unroll
+    for (int j = 0; j < kTileM / kWarp; ++j) {
+        const int t = j * kWarp + lane;
+        if (t < nvalid) m.tok[j] = __ldg(p.ordering + p0 + t);
+    }
+    // packed table: the chunk starts at padded position poff[c] + y, a group boundary
+    if (p.packed) m.g0 = (__ldg(p.poff + rec.x) + rec.y) / kPackRows;
+}
+
 // Metadata warp: publishes the units of this CTA's items (items blockIdx.x,
-// blockIdx.x + G, ...), then an end-of-stream entry.  False after a timed-out wait.
+// blockIdx.x + G, ...; records two items ahead, their loads one item ahead), then
+// an end-of-stream entry.  False after a timed-out wait.
 __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, uint32_t mempty0, int lane)
 {
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
     const int G = (int)gridDim.x;
     const long long packed_groups = p.packed ? __ldg(p.poff + p.C) / kPackRows : 0;
+    const int2 none = make_int2(-1, 0);
     int u = 0;
     int it = blockIdx.x;
-    int2 item = it < n_items ? p.items[it] : make_int2(-1, 0);
+    ItemPre nxt;
+    load_item(p, it < n_items ? p.items[it] : none, it < n_items, lane, nxt);
+    int2 rec2 = it + G < n_items ? p.items[it + G] : none;
     for (; it < n_items; it += G) {
-        const int2 cur = item;
-        if (it + G < n_items) item = p.items[it + G];   // the next record, loaded early
-        int lo = 0, hi = 0;
-        if ((unsigned)cur.x < (unsigned)p.C && cur.y >= 0)
-            cluster_range(p.offsets, p.V, p.S, cur.x, &lo, &hi, nullptr);
-        const int p0 = cur.y > hi - lo ? hi : lo + cur.y;
-        const int nvalid = max(0, min(p.chunk, hi - p0));
-        if (nvalid == 0) continue;
-        // packed table: the chunk starts at padded position poff[c] + y, a group boundary;
-        // a chunk reaching past the table's last group (tables packed from other
+        const ItemPre cur = nxt;
+        load_item(p, rec2, it + G < n_items, lane, nxt);
+        rec2 = it + 2 * G < n_items ? p.items[it + 2 * G] : none;
+        if (!cur.valid) continue;
+        const int nvalid = cur.nvalid, p0 = cur.p0, g0 = cur.g0;
+        // a chunk reaching past the packed table's last group (a table packed from other
         // offsets) is skipped and flagged instead of read
-        const int g0 = p.packed ? (__ldg(p.poff + cur.x) + cur.y) / kPackRows : 0;
         if (p.packed && (long long)g0 + (nvalid + kPackRows - 1) / kPackRows > packed_groups) {
             if (lane == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
             continue;
@@ -177,22 +219,20 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
             // unit: its phase is unchanged until a unit is published in it
             if (!mbar_wait(mempty0 + 8u * um, ((uint32_t)(u / kMeta) & 1u) ^ 1u, kWaitNs)) return false;
             UnitMeta &m = meta[um];
-            const int n = bucket_rows(p, cur.x, blk, lane, m.rows);
+            const int n = bucket_rows(p, cur.w, blk, lane, m.rows);
             if (n == 0) break;
             const int npad = (n + 15) & ~15;
             for (int r = n + lane; r < npad; r += kWarp) m.rows[r] = p.B;   // zero rows
 #pragma unroll
             for (int j = 0; j < kTileM / kWarp; ++j) {
-                const int t = j * kWarp + lane;
-                int tok = -1;
-                if (t < nvalid) {
-                    tok = __ldg(p.ordering + p0 + t);
-                    if ((unsigned)tok >= (unsigned)p.V) {
-                        atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
-                        tok = -1;
-                    }
+                int tok = cur.tok[j];
+                if (tok == kNoPos) {
+                    tok = -1;
+                } else if ((unsigned)tok >= (unsigned)p.V) {
+                    atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
+                    tok = -1;
                 }
-                m.tok[t] = tok;
+                m.tok[j * kWarp + lane] = tok;
             }
             if (p.sparse_width) {
                 // the sparse pair's column block of each row: the cluster's rank in its top-K
@@ -201,7 +241,7 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                     const int32_t *sel = p.topk + (size_t)m.rows[r] * p.K;
                     int rank = -1;
                     for (int k0 = 0; k0 < p.K && rank < 0; k0 += kWarp) {
-                        const bool hit = k0 + lane < p.K && __ldcg(sel + k0 + lane) == cur.x;
+                        const bool hit = k0 + lane < p.K && __ldcg(sel + k0 + lane) == cur.c;
                         const unsigned bal = __ballot_sync(0xffffffffu, hit);
                         if (bal) rank = k0 + __ffs(bal) - 1;
                     }
@@ -212,7 +252,7 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                 m.n = n;
                 m.npad = npad;
                 m.nvalid = nvalid;
-                m.local0 = p0 - lo;
+                m.local0 = p0 - cur.lo;
                 m.p0 = p.packed ? g0 : p0;
                 m.box = (nvalid + kPackRows - 1) / kPackRows;
             }
@@ -339,13 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     UnitMeta *meta = reinterpret_cast<UnitMeta *>(tail);
     unsigned long long *best = reinterpret_cast<unsigned long long *>(meta + kMeta);
     uint64_t *bars = reinterpret_cast<uint64_t *>(best + p.B);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5 + 2 * kMeta);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 2 * kAcc + 1 + 2 * kMeta);
     __shared__ int s_last;
 
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x & (kWarp - 1);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8u * S;
-    const uint32_t tfull0 = empty0 + 8u * S, tempty0 = tfull0 + 16u;
-    const uint32_t mfull0 = tempty0 + 16u, mempty0 = mfull0 + 8u * kMeta;
+    const uint32_t tfull0 = empty0 + 8u * S, tempty0 = tfull0 + 8u * kAcc;
+    const uint32_t mfull0 = tempty0 + 8u * kAcc, mempty0 = mfull0 + 8u * kMeta;
     const uint32_t drain_bar = mempty0 + 8u * kMeta;
 
     if (threadIdx.x == 0) {
@@ -353,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(tfull0 + 8u * a, 1);
             mbar_init(tempty0 + 8u * a, 4);
         }
@@ -373,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
     // the work items and buckets come from the top-K kernel before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t acc_cols = p.tmem_cols / 2;
+    const uint32_t acc_cols = p.tmem_cols / kAcc;
 
     if (warp == 4) {
         if (!publish_units(p, meta, mfull0, mempty0, lane) && lane == 0) timeout(p);
@@ -426,8 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mma_commit(tfull0 + 8u * acc);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                if (++acc == kAcc) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
             }
             // every MMA issued has completed before the accumulators are freed
             mma_commit(drain_bar);
@@ -495,8 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(tempty0 + 8u * acc);
                 mbar_arrive(mempty0 + 8u * um);
             }
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            if (++acc == kAcc) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
     }
 
@@ -561,7 +605,7 @@ bool encode_rows(CUtensorMap *map, const void *base, long long inner, long long 
 size_t smem_bytes(const Params &p, int stages)
 {
     return 1024 + (size_t)stages * (p.a_bytes + p.b_bytes) + (kFullABytes - p.a_bytes) +
-           kMeta * sizeof(UnitMeta) + (size_t)p.B * 8 + (size_t)(2 * stages + 5 + 2 * kMeta) * 8 + 16;
+           kMeta * sizeof(UnitMeta) + (size_t)p.B * 8 + (size_t)(2 * stages + 2 * kAcc + 1 + 2 * kMeta) * 8 + 16;
 }
 
 }  // namespace
@@ -605,7 +649,7 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     p.a_bytes = (uint32_t)a_rows * kRowBytes;
     p.b_bytes = (uint32_t)p.nmax * kRowBytes;
     uint32_t cols = 32;
-    while (cols < 2u * (uint32_t)p.nmax) cols <<= 1;
+    while (cols < (uint32_t)kAcc * (uint32_t)p.nmax) cols <<= 1;
     p.tmem_cols = cols;
     int stages = kMaxStages;
     while (stages > 2 && smem_bytes(p, stages) > 220 * 1024) --stages;
