@@ -151,11 +151,19 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     const uint32_t kbucket = s_digit;
     const int ncand = (int)s_above;
     if (ncand <= kCandCap) {
-        for (int c = tid; c < p.C; c += kTopkThreads) {
-            const uint32_t k = keys[c];
-            if ((k >> kKeyShift) >= kbucket) {
-                const int pos = atomicAdd(&s_ncand, 1);
-                s_cand[pos] = select_key(k, c);
+        // compaction: one shared atomic per warp and pass (the candidates of a warp take
+        // consecutive slots), not one per candidate on a single counter
+        const int lane = tid & (kWarp - 1);
+        for (int c0 = 0; c0 < p.C; c0 += kTopkThreads) {
+            const int c = c0 + tid;
+            const uint32_t k = c < p.C ? keys[c] : 0u;
+            const bool hit = c < p.C && (k >> kKeyShift) >= kbucket;
+            const unsigned bal = __ballot_sync(0xffffffffu, hit);
+            if (bal) {
+                int base = 0;
+                if (lane == __ffs(bal) - 1) base = atomicAdd(&s_ncand, __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, __ffs(bal) - 1);
+                if (hit) s_cand[base + __popc(bal & ((1u << lane) - 1u))] = select_key(k, c);
             }
         }
         __syncthreads();
