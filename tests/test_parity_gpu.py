@@ -895,3 +895,54 @@ def test_fidelity_flags_integer_inputs(build_lib, flags, B, K, packed):
     if flags & 4:
         raw_d = oracle.dense_logits(oracle.Head(cw, ew, perm, None, K), hid)
         assert (dref != raw_d).mean() > 0.1
+
+
+# ---------------------------------------------------------------------------
+# seeded random shapes through every finish
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_shapes(build_lib, seed):
+    """Random V, C, H, K, B, uniform or ragged clusters (empty ones included), with or without
+    the packed table: every finish against the oracle (token ids exact on rows whose margins
+    are clear, logits within the tolerance)."""
+    m = build_lib
+    g = np.random.default_rng(900 + seed)
+    C = int(g.integers(2, 65))
+    K = int(g.integers(1, C + 1))
+    H = 8 * int(g.integers(1, 65))
+    B = int(g.integers(1, 81))
+    ragged = bool(g.integers(0, 2))
+    if ragged:
+        sizes = g.integers(0, 200, size=C)
+        sizes[g.integers(0, C)] = 0
+        sizes[g.integers(0, C)] += 1
+        V = int(sizes.sum())
+    else:
+        sizes = None
+        V = C * int(g.integers(1, 160))
+    t, oh, dh = _custom(m, V, H, C, K, seed=1000 + seed, sizes=sizes)
+    packed = bool(g.integers(0, 2))
+    if packed:
+        dh.use_packed_table()
+    hidden = synth.random_hidden(B, H, 2000 + seed)
+    h = helpers.bf16_tensor(hidden)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    torch.cuda.synchronize()
+    ref = oracle.masked_topk_tokens(oh, hidden)
+    sel_ok = ref["score_margin"] > helpers.MARGIN
+    clear = sel_ok & (ref["logit_margin"] > helpers.MARGIN)
+    what = f"seed {seed}: V={V} C={C} K={K} H={H} B={B} ragged={ragged} packed={packed}"
+    np.testing.assert_array_equal(tok.cpu().numpy()[clear], ref["tokens"][clear], err_msg=what)
+    helpers.assert_close(mx.cpu().numpy()[sel_ok], ref["max_logit"][sel_ok], what + " max")
+    helpers.assert_close(sc.cpu().numpy()[sel_ok], oracle.masked_scatter_logits(oh, hidden)[sel_ok],
+                         what + " scatter")
+    if not ragged:
+        plog, pids = m.mtp_select_and_score(dh, h)
+        torch.cuda.synchronize()
+        for b in np.nonzero(sel_ok)[0][:8]:
+            rl, rt = oracle.select_and_score_row(oh, hidden, int(b))
+            np.testing.assert_array_equal(pids[b].cpu().numpy(), rt, err_msg=what)
+            helpers.assert_close(plog[b].cpu().numpy(), rl, what + " pair")
+    assert m.mtp_read_device_error(dh.workspace(B)) == 0, what
