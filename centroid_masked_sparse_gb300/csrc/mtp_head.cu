@@ -172,7 +172,8 @@ mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool o
     }
     if (d->flags & ~(MTP_FLAG_FILL_FINFO_MIN | MTP_FLAG_BF16_SCORES | MTP_FLAG_BF16_LOGITS))
         return MTP_ERR_UNSUPPORTED;
-    if (ordering && !d->cluster_offsets && d->vocab_size % d->num_centroids != 0) return MTP_ERR_SHAPE;
+    if (ordering && !d->cluster_offsets && (d->num_centroids < 1 || d->vocab_size % d->num_centroids != 0))
+        return MTP_ERR_SHAPE;
     return MTP_OK;
 }
 
