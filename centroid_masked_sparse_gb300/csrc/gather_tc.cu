@@ -16,20 +16,24 @@
 //     with plain bulk copies: few large copies are what streams HBM fastest;
 //   * with the token-order table they are gathered four rows per instruction
 //     (tile::gather4), skipping groups that are all padding;
-//   * the bucket's hidden rows are always gathered (tile::gather4), only the
-//     groups of four that hold real rows (a padding row inside such a group uses
-//     an out-of-range row, which TMA fills with zeros without reading memory).
-// Each gather4 costs the TMA unit far more time than its 512 bytes suggest, so
-// the count of gathers per k-block, not bytes, sets this kernel's pace once
-// buckets are large; tile rows that no load wrote hold stale data, which only
-// feeds TMEM lanes and columns the epilogue ignores.
+//   * a small bucket's hidden rows (at most kGatherRowsMax) come by tile::gather4
+//     with the A tile, only the groups of four that hold real rows (a padding row
+//     inside such a group uses an out-of-range row, which TMA fills with zeros);
+//   * a larger bucket's rows are copied by four B warps from L2 (the whole batch
+//     stays there) with 16-byte cp.async into the swizzled tile: a gather4 costs
+//     the TMA unit far more time than its 512 bytes suggest, so with many rows
+//     per bucket the count of gathers, not bytes, would set the pace.
+// Tile rows that no load wrote hold stale data, which only feeds TMEM lanes and
+// columns the epilogue ignores.
 //
-// Warp roles per CTA (one CTA per SM, 224 threads):
+// Warp roles per CTA (one CTA per SM, 352 threads):
 //   warp 4   metadata: walks this CTA's items and publishes each unit's token
 //            and row lists into a ring of kMeta entries, running ahead of the
 //            loads so that its dependent global reads (item record, row mask,
 //            token ids) never stall the stream;
-//   warp 6   TMA issue: per unit and k-block, one stage of A and B loads;
+//   warp 6   TMA issue: per unit and k-block, one stage of A loads (and B for a
+//            small bucket);
+//   warps 7-10 B: the hidden rows of larger buckets, by cp.async (see load_b);
 //   warp 5   one thread issues tcgen05.mma (kind::f16, fp32 in TMEM, four
 //            accumulators so the epilogues of the last units overlap the next);
 //   warps 0-3 epilogue: tcgen05.ld of the unit's logits (thread = candidate),
@@ -57,7 +61,8 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kThreads = 224;
+constexpr int kBWarps = 4;         // warps that copy the buckets' hidden rows (the B operand)
+constexpr int kThreads = (7 + kBWarps) * kWarp;
 constexpr int kTileM = 128;        // MMA M: candidate positions per unit (at most)
 constexpr int kTileK = 64;         // bf16 per k-block (128-byte rows)
 constexpr int kMaxN = 128;         // bucket rows per unit (at most)
@@ -67,7 +72,10 @@ constexpr int kMaxStages = 32;
 constexpr uint32_t kRowBytes = kTileK * 2;
 constexpr uint32_t kFullABytes = kTileM * kRowBytes;   // what one M = 128 MMA reads
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr uint32_t kMetaReaders = 6;   // 4 epilogue warps + the MMA thread + the TMA warp
+constexpr uint32_t kMetaReaders = 6 + kBWarps;   // epilogue warps, MMA thread, TMA warp, B warps
+constexpr int kBRowsPerThread = kMaxN / (kBWarps * kWarp / 8);   // 8 threads per 128-byte row slice
+constexpr int kBLag = 6;               // B copy groups in flight before a stage is signalled full
+constexpr int kGatherRowsMax = 8;      // buckets up to this size: B by TMA gather4 (at most two), not the B warps
 constexpr int kNoPos = INT_MIN;        // a candidate slot past the chunk's end
 constexpr int kPackRows = 32;          // clusters are padded to multiples of this
 constexpr int kPackSuper = 128;        // rows per packed block
@@ -101,6 +109,8 @@ struct Params {
     int32_t *out_ids;
     const int32_t *topk;      // [B, K]
     int K;
+    const uint16_t *hidden;   // [B, H]
+    int b_lag;                // B copy groups a B thread keeps in flight (<= kBLag, < stages - 1)
     int B, H, V, S, W, C;
     int chunk;      // positions per work item (<= 128; a multiple of 32 when packed)
     const uint8_t *packed;    // packed table blocks, or null (token-order gathers)
@@ -306,13 +316,13 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
         const int n = m.n;
         if (n < 0) return true;
         const int nvalid = m.nvalid, g0 = m.p0, groups = m.box;
-        // lane j gathers candidate rows 4j..4j+3 (token-order table) and bucket rows
-        // 4j..4j+3 while 4j < n
+        // lane j gathers candidate rows 4j..4j+3 (token-order table) and, for a small
+        // bucket, bucket rows 4j..4j+3 while 4j < n (larger buckets: the B warps)
         const int y0 = m.tok[4 * lane] >= 0 ? m.tok[4 * lane] : p.V;
         const int y1 = m.tok[4 * lane + 1] >= 0 ? m.tok[4 * lane + 1] : p.V;
         const int y2 = m.tok[4 * lane + 2] >= 0 ? m.tok[4 * lane + 2] : p.V;
         const int y3 = m.tok[4 * lane + 3] >= 0 ? m.tok[4 * lane + 3] : p.V;
-        const bool has_b = 4 * lane < n;
+        const bool has_b = n <= kGatherRowsMax && 4 * lane < n;
         const int z0 = has_b ? m.rows[4 * lane] : 0, z1 = has_b ? m.rows[4 * lane + 1] : 0;
         const int z2 = has_b ? m.rows[4 * lane + 2] : 0, z3 = has_b ? m.rows[4 * lane + 3] : 0;
         __syncwarp();
@@ -332,7 +342,7 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
         const uint8_t *pk_src = p.packed ? p.packed + (size_t)(blk0 + lane) * p.num_kb * kPackBlock +
                                                (lane == 0 ? (size_t)r0 * kRowBytes : 0)
                                          : nullptr;
-        const uint32_t tx = a_tx + (uint32_t)((n + 3) / 4) * 4 * kRowBytes;
+        const uint32_t tx = a_tx + (n <= kGatherRowsMax ? (uint32_t)((n + 3) / 4) * 4 * kRowBytes : 0u);
         for (int kb = 0; kb < p.num_kb; ++kb) {
             int wok = 1;
             if (lane == 0) {
@@ -363,6 +373,124 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
     }
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait(int groups_in_flight)
+{
+    switch (groups_in_flight) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    }
+}
+
+// B warps: per (unit, k-block) the bucket's hidden rows, 64 columns each, copied
+// from L2 (the whole [B, H] batch stays there) into the stage's B tile with
+// 16-byte cp.async in the 128-byte swizzle; columns at or past H read as zeros.
+// Thread t always copies piece t % 8 of rows t / 8, t / 8 + 16, ...  A stage is
+// signalled full (one arrival per B warp) once its copies have landed and been
+// fenced for the tensor cores, b_lag stages after it was filled, so that copies
+// for several stages are in flight.  False after a timed-out wait (the copies
+// issued are waited for and signalled before returning).
+__device__ bool load_b(const Params &p, const UnitMeta *meta, uint8_t *b_smem, uint32_t full0, uint32_t empty0,
+                       uint32_t mfull0, uint32_t mempty0, int bt, int lane)
+{
+    const int j = bt & 7, r0 = bt >> 3;
+    const int S = p.stages;
+    int stage = 0;
+    uint32_t phase = 0, filled = 0, signalled = 0;
+    bool ok = true;
+    auto signal_one = [&]() {
+        fence_proxy_async_smem();   // this thread's copies, visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full0 + 8u * (signalled % (uint32_t)S));
+        ++signalled;
+    };
+    // every wait is lane 0's, broadcast: the warp stays converged even if a wait gives
+    // up, and __syncwarp orders the other lanes after the completion lane 0 observed
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) {
+        int w = lane == 0 ? (int)mbar_wait(bar, parity, kWaitNs) : 1;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        __syncwarp();
+        return w != 0;
+    };
+    for (int u = 0; ok; ++u) {
+        const int um = u % kMeta;
+        if (!warp_wait(mfull0 + 8u * um, (uint32_t)(u / kMeta) & 1u)) {
+            ok = false;
+            break;
+        }
+        const UnitMeta &m = meta[um];
+        const int n = m.n;
+        if (n < 0) break;
+        const bool mine = n > kGatherRowsMax;   // small buckets come with the A tile (gather4)
+        int rows[kBRowsPerThread];
+#pragma unroll
+        for (int i = 0; i < kBRowsPerThread; ++i) {
+            const int r = r0 + 16 * i;
+            rows[i] = mine && r < n ? m.rows[r] : -1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mempty0 + 8u * um);   // the rows are in registers now
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!warp_wait(empty0 + 8u * stage, phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            if (!mine) {
+                // nothing to copy: settle the stages still owed a signal, then this one
+                if (signalled < filled) {
+                    cp_async_wait(0);
+                    while (signalled < filled) signal_one();
+                }
+                ++filled;
+                signal_one();
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                continue;
+            }
+            const uint32_t dst0 = smem_u32(b_smem + (size_t)stage * p.b_bytes);
+            const int k0 = kb * kTileK + j * 8;
+            const uint32_t src_bytes = k0 < p.H ? 16u : 0u;
+            const int kk = k0 < p.H ? k0 : 0;
+#pragma unroll
+            for (int i = 0; i < kBRowsPerThread; ++i) {
+                if (rows[i] >= 0) {
+                    const int r = r0 + 16 * i;
+                    cp_async16(dst0 + (uint32_t)(r * kRowBytes) + (uint32_t)((j ^ (r & 7)) << 4),
+                               p.hidden + (size_t)rows[i] * p.H + kk, src_bytes);
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            ++filled;
+            // more than b_lag stages unsignalled: the oldest one's copies have landed once at
+            // most b_lag groups are pending (count the gap, not the total: small buckets
+            // signal their stages at once)
+            if (filled - signalled > (uint32_t)p.b_lag) {
+                cp_async_wait(p.b_lag);
+                signal_one();
+            }
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // the stages still owed a signal (normal end or not)
+    cp_async_wait(0);
+    while (signalled < filled) signal_one();
+    return ok;
+}
+
 template <bool SCATTER>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_h,
@@ -390,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8u * s, 1);
+            mbar_init(full0 + 8u * s, 1 + kBWarps);   // the TMA warp (with the A bytes), the B warps
             mbar_init(empty0 + 8u * s, 1);
         }
         for (int a = 0; a < kAcc; ++a) {
@@ -420,6 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 6) {
         if (!issue_loads(p, meta, &tmap_e, &tmap_h, a_smem, b_smem, full0, empty0, mfull0, mempty0, lane) &&
             lane == 0)
+            timeout(p);
+    } else if (warp >= 7) {
+        if (!load_b(p, meta, b_smem, full0, empty0, mfull0, mempty0, threadIdx.x - 7 * kWarp, lane) && lane == 0)
             timeout(p);
     } else if (warp == 5) {
         // ------------------------------------------------------------- MMA issuer
@@ -655,10 +786,13 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     while (stages > 2 && smem_bytes(p, stages) > 220 * 1024) --stages;
     p.stages = stages;
     alignas(64) CUtensorMap map_e;
-    alignas(64) CUtensorMap map_h;
     // the token-order map is encoded either way (unused with the packed table)
     if (!encode_rows(&map_e, g.embed, g.H, g.V, g.ld, 1)) return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap map_h;
     if (!encode_rows(&map_h, g.hidden, g.H, g.B, g.H, 1)) return cudaErrorInvalidValue;
+    p.hidden = g.hidden;
+    p.b_lag = std::min(kBLag, p.stages - 2);
+    if (p.b_lag < 0) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes(p, stages);
     if (scatter) {
         cudaError_t e = allow_smem((const void *)k_gather_tc<true>, smem);
