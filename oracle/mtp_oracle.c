@@ -40,6 +40,9 @@
  *   ORC_FLAG_BF16_LOGITS     the sparse (and dense) logits are rounded to bf16,
  *                            as the page's bf16 einsum returns them, before the
  *                            argmax and the scatter.
+ * The dense comparator can also apply the final logit softcap of the page's
+ * dense path (Gemma4MTP.compute_logits through the logits processor):
+ * cap * tanh(logit / cap) for cap > 0, before any bf16 rounding.
  * Rounding to bf16 is round-to-nearest-even of the exact fp64 value to 8
  * significant bits (bf16's exponent range, its subnormals included).
  *
@@ -391,7 +394,7 @@ int orc_select_and_score_row(const uint16_t *hidden, int64_t b, int64_t H,
  * = sum_h h[b,h] E[t,h] for rows [b0, b1) and every token t < V. */
 int orc_dense_logits(const uint16_t *hidden, int64_t b0, int64_t b1, int64_t H,
                      const uint16_t *embed_w, int64_t ld_embed, int64_t V, double *out,
-                     int64_t flags)
+                     int64_t flags, double softcap)
 {
     if (!hidden || !embed_w || !out || H <= 0 || V <= 0 || ld_embed < H || b0 < 0 || b1 < b0)
         return ORC_ERR_ARG;
@@ -399,6 +402,8 @@ int orc_dense_logits(const uint16_t *hidden, int64_t b0, int64_t b1, int64_t H,
         for (int64_t t = 0; t < V; ++t)
         {
             out[b * V + t] = dot_bf16(hidden + b * H, embed_w + t * ld_embed, H);
+            if (softcap > 0.0)
+                out[b * V + t] = softcap * tanh(out[b * V + t] / softcap);
             if (flags & ORC_FLAG_BF16_LOGITS)
                 out[b * V + t] = orc_round_bf16(out[b * V + t]);
         }

@@ -52,7 +52,7 @@ _SIGS = {
                                   _i64, _p, _p, _p, _i64],
     "orc_select_and_score_row": [_p, _i64, _i64, _p, _i64, _i64, _p, _i64, _i64,
                                  _p, _p, _p, _p, _i64, _p, _i64],
-    "orc_dense_logits": [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64],
+    "orc_dense_logits": [_p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64, ctypes.c_double],
     "orc_dense_logits_at": [_p, _i64, _p, _i64, _p, _p, _i64, _p],
     "orc_is_permutation": [_p, _i64],
 }
@@ -116,9 +116,11 @@ class Head:
     ordering     int32  [V]      ordered position -> token id
     offsets      int32  [C+1] or None (uniform clusters of V/C)
     flags        FLAG_* reference-fidelity options (0: fp64 scores and logits, -inf fill)
+    softcap      the dense comparator's final logit softcap (0: none)
     """
 
-    def __init__(self, centroid_w, embed_w, ordering, offsets, top_k, vocab=None, flags=0):
+    def __init__(self, centroid_w, embed_w, ordering, offsets, top_k, vocab=None, flags=0,
+                 softcap=0.0):
         self.centroid_w = np.ascontiguousarray(centroid_w, dtype=np.uint16)
         self.embed_w = np.ascontiguousarray(embed_w, dtype=np.uint16)
         self.ordering = np.ascontiguousarray(ordering, dtype=np.int32)
@@ -128,6 +130,7 @@ class Head:
         self.V = int(vocab) if vocab is not None else int(self.ordering.shape[0])
         self.K = int(top_k)
         self.flags = int(flags)
+        self.softcap = float(softcap)
 
     @classmethod
     def from_tables(cls, t, top_k=None):
@@ -230,7 +233,8 @@ def dense_logits(head: Head, hidden: np.ndarray, threads: int | None = None) -> 
 
     def run(r):
         _check(L.orc_dense_logits(_ptr(hidden), r[0], r[1], head.H, _ptr(head.embed_w),
-                                  head.ld, head.V, _ptr(out), head.flags), "dense_logits")
+                                  head.ld, head.V, _ptr(out), head.flags, head.softcap),
+               "dense_logits")
 
     nt = _threads(threads)
     with ThreadPoolExecutor(nt) as ex:

@@ -31,6 +31,8 @@ MUTATIONS = [
      "s += bf16_value(x[i]) * bf16_value(w[i]);", "s -= bf16_value(x[i]) * bf16_value(w[i]);"),
     ("full-vocab fill of 0 instead of -inf",
      "? -ORC_BF16_MAX : -INFINITY;", "? -ORC_BF16_MAX : 0.0;"),
+    ("dense softcap without dividing by the cap",
+     "softcap * tanh(out[b * V + t] / softcap)", "softcap * tanh(out[b * V + t])"),
     ("bf16 rounding with ties away from zero",
      "ldexp(nearbyint(ldexp(x, -q)), q)", "ldexp(round(ldexp(x, -q)), q)"),
     ("bf16-score option rounds the logits instead",
@@ -60,7 +62,8 @@ def _pin_calls():
               ("single", pins.test_single_centroid_is_dense),
               ("variable", pins.test_variable_cluster_candidate_counts),
               ("round_bf16", pins.test_round_bf16_values),
-              ("flags", pins.test_fidelity_flags_hand_example)]
+              ("flags", pins.test_fidelity_flags_hand_example),
+              ("softcap", pins.test_dense_softcap_hand_example)]
     return calls
 
 

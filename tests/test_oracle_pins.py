@@ -306,3 +306,18 @@ def test_fidelity_flags_hand_example():
     # dense logits with bf16 rounding
     d = oracle.dense_logits(_flag_head(oracle.FLAG_BF16_LOGITS), h, threads=1)
     assert d.tolist() == [[256.0, 1.0, 1.0, 256.0]]
+
+
+def test_dense_softcap_hand_example():
+    """cap * tanh(logit / cap) on the dense comparator: with cap 2 the logits 256 and 1 of the
+    two-centroid example become 2 tanh(128) and 2 tanh(1/2), worked by hand."""
+    import math
+    h = np.array([[0x3F80, 0x3F80]], np.uint16)
+    head = _flag_head(0)
+    head.softcap = 2.0
+    d = oracle.dense_logits(head, h, threads=1)
+    want = [2 * math.tanh(128.0), 2 * math.tanh(0.5), 2 * math.tanh(0.5), 2 * math.tanh(128.5)]
+    assert d.tolist() == [want]
+    assert abs(d[0, 1] - 0.9242343145200195) < 1e-15   # 2 tanh(1/2)
+    head.softcap = 0.0
+    assert oracle.dense_logits(head, h, threads=1).tolist() == [[256.0, 1.0, 1.0, 257.0]]
