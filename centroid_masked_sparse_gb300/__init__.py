@@ -55,10 +55,11 @@ class MaskedHead:
     cluster_range    (begin, end): the clusters this GPU owns when the head is sharded
                      over GPUs by cluster, or None for all of them
     flags            MTP_FLAG_* reference-fidelity options (0: fp32 scores and logits, -inf)
+    softcap          the dense head's final logit softcap, cap * tanh(logit / cap) (0: none)
     """
 
     def __init__(self, centroid_w, embed_w, token_ordering, top_k, cluster_offsets=None,
-                 vocab_size=None, embed_packed=None, cluster_range=None, flags=0):
+                 vocab_size=None, embed_packed=None, cluster_range=None, flags=0, softcap=0.0):
         torch = _torch()
         if centroid_w is not None:
             assert centroid_w.dtype == torch.bfloat16 and centroid_w.is_contiguous()
@@ -85,7 +86,8 @@ class MaskedHead:
             cluster_offsets=None if cluster_offsets is None else cluster_offsets.data_ptr(),
             embed_packed=None,
             cluster_begin=0 if cluster_range is None else int(cluster_range[0]),
-            cluster_end=0 if cluster_range is None else int(cluster_range[1]))
+            cluster_end=0 if cluster_range is None else int(cluster_range[1]),
+            final_logit_softcap=float(softcap))
         self.cluster_range = cluster_range
         self.embed_packed = None
         self._ws = None

@@ -44,6 +44,7 @@ class MtpHeadDesc(ctypes.Structure):
         ("embed_packed", ctypes.c_void_p),
         ("cluster_begin", ctypes.c_int32),
         ("cluster_end", ctypes.c_int32),
+        ("final_logit_softcap", ctypes.c_float),
     ]
 
 

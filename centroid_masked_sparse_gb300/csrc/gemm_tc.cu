@@ -59,6 +59,7 @@ struct TcParams {
     int zero_words;
     int cluster_reduce;     // splits > 1: one cluster per output tile, summed through DSMEM
     int round_bf16;         // dense head: logits rounded to bf16 before they are stored or compared
+    float softcap;          // dense head: final logit softcap (cap * tanh(v / cap)), 0 = none
 };
 
 // Unit u = (m tile, n block, k split) with the split innermost, so that the
@@ -255,7 +256,9 @@ __global__ void __launch_bounds__(kTcThreads)
                 for (int j = 0; j < 16; ++j) {
                     const int n = nb * p.n_pad + c0 + j;
                     if (n >= p.N) break;
-                    const float v = p.round_bf16 ? round_bf16(__uint_as_float(r[j])) : __uint_as_float(r[j]);
+                    float v = __uint_as_float(r[j]);
+                    if (p.softcap > 0.f) v = p.softcap * tanhf(v / p.softcap);
+                    if (p.round_bf16) v = round_bf16(v);
                     if (outp && m_ok) outp[(size_t)n * p.ldo + m] = v;
                     if (p.keys) {
                         unsigned long long key = m_ok ? argmax_key(v, m) : 0ull;
@@ -443,6 +446,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     p.zero_words = a.zero ? a.zero_words : 0;
     p.cluster_reduce = p.splits > 1;
     p.round_bf16 = a.round_bf16 ? 1 : 0;
+    p.softcap = a.softcap;
     if (p.cluster_reduce && (size_t)stages * stage_bytes < (size_t)p.n_pad * kTileM * 4)
         return cudaErrorInvalidValue;
     if (p.cluster_reduce && (p.keys || p.splits > 8 || p.units > 65535)) return cudaErrorInvalidValue;

@@ -85,6 +85,7 @@ struct TcGemmArgs {
     float *out_max;         // with keys, optional
     bool round_bf16;        // round each output to bf16 first (dense head option)
     bool after_fill;        // launched behind the scatter's fill, overlapping it
+    float softcap;          // dense head: cap * tanh(v / cap) for cap > 0
     uint32_t *zero;         // words cleared at kernel start (may be null)
     int zero_words;
 };

@@ -172,6 +172,7 @@ mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool o
     }
     if (d->flags & ~(MTP_FLAG_FILL_FINFO_MIN | MTP_FLAG_BF16_SCORES | MTP_FLAG_BF16_LOGITS))
         return MTP_ERR_UNSUPPORTED;
+    if (!(d->final_logit_softcap >= 0.f)) return MTP_ERR_SHAPE;   // negative or NaN
     if (ordering && !d->cluster_offsets && (d->num_centroids < 1 || d->vocab_size % d->num_centroids != 0))
         return MTP_ERR_SHAPE;
     return MTP_OK;
@@ -500,6 +501,7 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
     g.splits = 1;
     g.out = out_logits;
     g.round_bf16 = (desc->flags & MTP_FLAG_BF16_LOGITS) != 0;
+    g.softcap = desc->final_logit_softcap;
     g.ldo = desc->vocab_size;
     g.keys = out_tokens ? (unsigned long long *)(ws + L.keys) : nullptr;
     g.ctrl = out_tokens ? (uint32_t *)ws : nullptr;

@@ -122,7 +122,13 @@ typedef enum mtp_status {
  *                    candidates (-inf elsewhere; the elementwise max over shards is
  *                    the whole row), and a packed table holds only these clusters.
  *                    embed_w stays indexed by token id; only the rows of this
- *                    shard's tokens are read. */
+ *                    shard's tokens are read.
+ *   final_logit_softcap  the dense head's final logit softcap (the page's dense path,
+ *                    Gemma4MTP.compute_logits, applies final_logit_softcapping): each
+ *                    dense logit becomes cap * tanh(logit / cap) before it is stored,
+ *                    rounded (MTP_FLAG_BF16_LOGITS) or compared; 0 = none.  The masked
+ *                    calls never apply it (the page's masked path does not).  Negative
+ *                    or NaN: MTP_ERR_SHAPE. */
 /* Reference-fidelity options (desc->flags; 0 = the library's default reading:
  * fp32 scores and logits, -inf fill).  The page's head runs in the model dtype,
  * bf16 ("Add Gemma4 MTP speculative decoding with centroids masking",
@@ -157,6 +163,7 @@ typedef struct mtp_head_desc {
     const void *embed_packed;
     int32_t cluster_begin;
     int32_t cluster_end;
+    float final_logit_softcap;
 } mtp_head_desc;
 
 /* Bytes of device workspace that the masked calls and the dense head's argmax

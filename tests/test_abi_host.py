@@ -245,3 +245,14 @@ def test_unknown_flags_are_refused(L):
     assert L.mtp_dense_lm_head(ctypes.byref(d), FAKE, 4, out, None, None, None, 0, None) == -6
     d.flags = 7
     assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 16, None) == -4
+
+
+def test_softcap_checks(L):
+    out = ctypes.c_void_p(0x8000)
+    for cap in (-1.0, float("nan")):
+        d = _desc()
+        d.final_logit_softcap = cap
+        assert L.mtp_dense_lm_head(ctypes.byref(d), FAKE, 4, out, None, None, None, 0, None) == -2
+    d = _desc()
+    d.final_logit_softcap = 30.0
+    assert L.mtp_dense_lm_head(ctypes.byref(d), FAKE, 4, None, None, None, None, 0, None) == -1

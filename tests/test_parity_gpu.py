@@ -946,3 +946,30 @@ def test_random_shapes(build_lib, seed):
             np.testing.assert_array_equal(pids[b].cpu().numpy(), rt, err_msg=what)
             helpers.assert_close(plog[b].cpu().numpy(), rl, what + " pair")
     assert m.mtp_read_device_error(dh.workspace(B)) == 0, what
+
+
+@pytest.mark.parametrize("cap,flags", [(3.0, 0), (30.0, 0), (3.0, 4)])
+def test_dense_softcap(build_lib, cap, flags):
+    """The dense head's final logit softcap against the oracle's cap * tanh(logit / cap);
+    the masked calls ignore it."""
+    m = build_lib
+    t = synth.custom_tables(4096, 128, 32, 55, std=0.2)
+    oh = oracle.Head(t.centroid_w, t.embed_w, t.token_ordering, None, 4, flags=flags, softcap=cap)
+    dh = m.MaskedHead(helpers.bf16_tensor(t.centroid_w), helpers.bf16_tensor(t.embed_w),
+                      torch.from_numpy(t.token_ordering).cuda(), 4, flags=flags, softcap=cap)
+    hidden = synth.random_hidden(8, 128, 56)
+    h = helpers.bf16_tensor(hidden)
+    dl, dtok, dmax = m.mtp_dense_lm_head(dh, h, want_tokens=True)
+    tok, _ = m.mtp_masked_topk_tokens(dh, h)
+    torch.cuda.synchronize()
+    ref = oracle.dense_logits(oh, hidden)
+    got = dl.cpu().numpy()
+    helpers.assert_close(got, ref, f"softcap {cap}")
+    assert np.abs(got).max() <= cap
+    np.testing.assert_array_equal(dtok.cpu().numpy(), np.argmax(got, axis=1))
+    np.testing.assert_array_equal(dmax.cpu().numpy(), got.max(axis=1))
+    # the masked argmax is uncapped: same as without the cap
+    plain = m.MaskedHead(dh.centroid_w, dh.embed_w, dh.token_ordering, 4, flags=flags)
+    ptok, _ = m.mtp_masked_topk_tokens(plain, h)
+    torch.cuda.synchronize()
+    assert torch.equal(tok, ptok)
