@@ -358,17 +358,16 @@ def measure_e2e(ctx, t, dh, name, B, steps, warmup):
     hb = make_batches(synth, t, name, B, 4, 20000)
     host_in = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory() for h in hb]
     dev_in = torch.empty(B, t.workload.hidden, dtype=torch.bfloat16, device=ctx["device"])
-    tok = torch.empty(B, dtype=torch.int32, device=ctx["device"])
-    mx = torch.empty(B, dtype=torch.float32, device=ctx["device"])
-    host_tok = torch.empty(B, dtype=torch.int32).pin_memory()
-    host_mx = torch.empty(B, dtype=torch.float32).pin_memory()
+    # token ids and max logits side by side in one buffer: one D2H copy per step
+    dev_out = torch.empty(2 * B, dtype=torch.int32, device=ctx["device"])
+    tok, mx = dev_out[:B], dev_out[B:].view(torch.float32)
+    host_out = torch.empty(2 * B, dtype=torch.int32).pin_memory()
     ws = dh.workspace(B)
 
     def fn(i):
         dev_in.copy_(host_in[i % 4], non_blocking=True)
         m.mtp_masked_topk_tokens(dh, dev_in, out_tokens=tok, out_max=mx, workspace=ws)
-        host_tok.copy_(tok, non_blocking=True)
-        host_mx.copy_(mx, non_blocking=True)
+        host_out.copy_(dev_out, non_blocking=True)
 
     call, _, _, _ = ctx["timer"].run(fn, steps, warmup, ws=ctx["ws"])
     return float(np.mean(call)), B * t.workload.hidden * 2, B * 8
@@ -529,7 +528,8 @@ def other_workloads(ctx, args, hbm):
     steps = max(10, args.steps // 8)
     cases = (("scatter", True, False), ("variable", False, False), ("shared", False, False),
              ("shared", True, False), ("uniform", False, False), ("uniform", False, True),
-             ("variable", False, True), ("shared", False, True), ("shared", True, True))
+             ("variable", False, True), ("shared", False, True), ("shared", True, True),
+             ("draft256", False, False), ("draft256", False, True))
     for name, scatter, packed in cases:
         w = synth.WORKLOADS[name]
         t = synth.make_tables(name)
