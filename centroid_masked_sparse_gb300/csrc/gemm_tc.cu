@@ -252,13 +252,22 @@ __global__ void __launch_bounds__(kTcThreads)
                     for (int j = 0; j < 16; ++j) red[(c0 + j) * kTileM + m_local] = __uint_as_float(r[j]);
                     continue;
                 }
+                // the dense head's options act on the 16 loaded values before any
+                // store or comparison, behind one uniform test per group
+                if (p.softcap > 0.f || p.round_bf16) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float v = __uint_as_float(r[j]);
+                        if (p.softcap > 0.f) v = p.softcap * tanhf(v / p.softcap);
+                        if (p.round_bf16) v = round_bf16(v);
+                        r[j] = __float_as_uint(v);
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = nb * p.n_pad + c0 + j;
                     if (n >= p.N) break;
-                    float v = __uint_as_float(r[j]);
-                    if (p.softcap > 0.f) v = p.softcap * tanhf(v / p.softcap);
-                    if (p.round_bf16) v = round_bf16(v);
+                    const float v = __uint_as_float(r[j]);
                     if (outp && m_ok) outp[(size_t)n * p.ldo + m] = v;
                     if (p.keys) {
                         unsigned long long key = m_ok ? argmax_key(v, m) : 0ull;
