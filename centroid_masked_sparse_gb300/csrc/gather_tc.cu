@@ -13,7 +13,8 @@
 // by TMA in the 128-byte-swizzled layout the MMA descriptors expect:
 //   * with the packed embedding table (below) the chunk's candidate rows are one
 //     or two contiguous, pre-swizzled runs of a 16 KB block per k-block, fetched
-//     with plain bulk copies: few large copies are what streams HBM fastest;
+//     with plain bulk copies that stop at the chunk's last real row (a cluster's
+//     padding is never read): few large copies are what streams HBM fastest;
 //   * with the token-order table they are gathered four rows per instruction
 //     (tile::gather4), skipping groups that are all padding;
 //   * a small bucket's hidden rows (at most kGatherRowsMax) come by tile::gather4
@@ -26,7 +27,8 @@
 // Tile rows that no load wrote hold stale data, which only feeds TMEM lanes and
 // columns the epilogue ignores.
 //
-// Warp roles per CTA (one CTA per SM, 352 threads):
+// Warp roles per CTA (352 threads; two CTAs per SM where their TMEM and shared
+// memory fit, else one):
 //   warp 4   metadata: walks this CTA's items and publishes each unit's token
 //            and row lists into a ring of kMeta entries, running ahead of the
 //            loads so that its dependent global reads (item record, row mask,
@@ -51,6 +53,8 @@
 #include <algorithm>
 #include <climits>
 #include <mutex>
+#include <map>
+#include <tuple>
 
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -69,6 +73,7 @@ constexpr int kMaxN = 128;         // bucket rows per unit (at most)
 constexpr int kMeta = 8;           // unit-metadata ring
 constexpr int kAcc = 4;            // TMEM accumulators: the epilogues of the last units overlap the MMAs
 constexpr int kMaxStages = 32;
+constexpr uint32_t kSmTmemCols = 512;  // TMEM columns of one SM
 constexpr uint32_t kRowBytes = kTileK * 2;
 constexpr uint32_t kFullABytes = kTileM * kRowBytes;   // what one M = 128 MMA reads
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -87,7 +92,6 @@ struct UnitMeta {
     int n;              // rows in this unit; -1: end of stream
     int npad, nvalid;
     int p0;             // token-order table: first ordered position; packed: first group
-    int box;            // token-order table: unused; packed: groups of 32 rows
     int local0;         // position of the chunk's first candidate inside its cluster
     int pad[2];
     int ranks[kMaxN];   // sparse pair: rank of the cluster in each row's top-K
@@ -264,7 +268,6 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                 m.nvalid = nvalid;
                 m.local0 = p0 - cur.lo;
                 m.p0 = p.packed ? g0 : p0;
-                m.box = (nvalid + kPackRows - 1) / kPackRows;
             }
             __syncwarp();
             if (lane == 0) {
@@ -315,7 +318,7 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
         const UnitMeta &m = meta[um];
         const int n = m.n;
         if (n < 0) return true;
-        const int nvalid = m.nvalid, g0 = m.p0, groups = m.box;
+        const int nvalid = m.nvalid, g0 = m.p0;
         // lane j gathers candidate rows 4j..4j+3 (token-order table) and, for a small
         // bucket, bucket rows 4j..4j+3 while 4j < n (larger buckets: the B warps)
         const int y0 = m.tok[4 * lane] >= 0 ? m.tok[4 * lane] : p.V;
@@ -328,12 +331,14 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
         __syncwarp();
         if (lane == 0) mbar_arrive(mempty0 + 8u * um);   // the entry is in registers now
         const bool has_a = 4 * lane < nvalid;
-        const uint32_t a_tx = p.packed ? (uint32_t)groups * kPackRows * kRowBytes
+        const uint32_t a_tx = p.packed ? (uint32_t)nvalid * kRowBytes
                                        : (uint32_t)((nvalid + 3) / 4) * 4 * kRowBytes;
-        // packed: rows [pp0, pp0 + groups*32) of the padded table, pp0 = 32*g0; the run
-        // is in block pp0/128 from row pp0%128 on, and continues at row 0 of the next
-        // block if it crosses the block's end (lane 0 copies the first part, lane 1 the rest)
-        const int prow0 = g0 * kPackRows, nrows = groups * kPackRows;
+        // packed: rows [pp0, pp0 + nvalid) of the padded table, pp0 = 32*g0 (the cluster's
+        // padding rows are not read; the tile rows past nvalid keep stale data, which only
+        // reaches accumulator rows the epilogue skips); the run is in block pp0/128 from
+        // row pp0%128 on, and continues at row 0 of the next block if it crosses the
+        // block's end (lane 0 copies the first part, lane 1 the rest)
+        const int prow0 = g0 * kPackRows, nrows = nvalid;
         const int blk0 = prow0 / kPackSuper, r0 = prow0 % kPackSuper;
         const int first = min(nrows, kPackSuper - r0);
         const bool has_pk = lane == 0 || (lane == 1 && nrows > first);
@@ -492,7 +497,7 @@ __device__ bool load_b(const Params &p, const UnitMeta *meta, uint8_t *b_smem, u
 }
 
 template <bool SCATTER>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_h,
                 const Params p)
 {
@@ -741,6 +746,47 @@ size_t smem_bytes(const Params &p, int stages)
 
 }  // namespace
 
+namespace {
+
+// Whether two CTAs of `kfn` with `smem` bytes of dynamic shared memory fit on one SM
+// (shared memory with the per-block reservation, threads, registers), from the
+// device's and the kernel's attributes (cached per kernel, device and size).  The
+// runtime's occupancy query answers one CTA here where two run side by side, so
+// the fit is worked out directly; the launch asks for the largest shared-memory
+// carveout so that the driver places both.  Were the answer ever wrong, the grid
+// would run in two waves: slower, still correct (each CTA holds at most half the
+// TMEM, so no allocation waits on a CTA that is not running).
+bool two_ctas_fit(const void *kfn, size_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, size_t>, bool> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const auto key = std::make_tuple(kfn, dev, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int smem_sm = 0, resv = 0, regs_sm = 0, thr_sm = 0;
+    cudaFuncAttributes fa{};
+    bool fit = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+               cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
+               cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) == cudaSuccess &&
+               cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) == cudaSuccess &&
+               cudaFuncGetAttributes(&fa, kfn) == cudaSuccess;
+    fit = fit && fa.numRegs > 0 &&
+          2 * (smem + fa.sharedSizeBytes + (size_t)resv) <= (size_t)smem_sm && 2 * kThreads <= thr_sm &&
+          2LL * kThreads * fa.numRegs <= (long long)regs_sm &&
+          cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = fit;
+    return fit;
+}
+
+}  // namespace
+
 cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s)
 {
     Params p{};
@@ -782,8 +828,26 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     uint32_t cols = 32;
     while (cols < (uint32_t)kAcc * (uint32_t)p.nmax) cols <<= 1;
     p.tmem_cols = cols;
-    int stages = kMaxStages;
-    while (stages > 2 && smem_bytes(p, stages) > 220 * 1024) --stages;
+    const void *kfn = scatter ? (const void *)k_gather_tc<true> : (const void *)k_gather_tc<false>;
+    auto fit_stages = [&](size_t budget) {
+        int st = kMaxStages;
+        while (st > 2 && smem_bytes(p, st) > budget) --st;
+        return st;
+    };
+    // Two CTAs per SM where both fit (accumulators in half the TMEM each, stages in
+    // half the shared memory): each CTA's single-thread MMA issue, TMA issue and
+    // barrier round trips cost a few hundred ns per k-block, so a second pipeline per
+    // SM is what lets short chunks and small H reach the HBM rate.
+    int per_sm = 1;
+    int stages = fit_stages(220 * 1024);
+    if (p.tmem_cols <= kSmTmemCols / 2) {
+        const int st2 = fit_stages(110 * 1024);
+        const size_t smem2 = smem_bytes(p, st2);
+        if (st2 >= 3 && two_ctas_fit(kfn, smem2)) {
+            per_sm = 2;
+            stages = st2;
+        }
+    }
     p.stages = stages;
     alignas(64) CUtensorMap map_e;
     // the token-order map is encoded either way (unused with the packed table)
@@ -794,14 +858,11 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     p.b_lag = std::min(kBLag, p.stages - 2);
     if (p.b_lag < 0) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes(p, stages);
-    if (scatter) {
-        cudaError_t e = allow_smem((const void *)k_gather_tc<true>, smem);
-        if (e != cudaSuccess) return e;
-        return launch_dependent(k_gather_tc<true>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_h, p);
-    }
-    cudaError_t e = allow_smem((const void *)k_gather_tc<false>, smem);
+    cudaError_t e = allow_smem(kfn, smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(k_gather_tc<false>, dim3(sm_count()), dim3(kThreads), smem, s, map_e, map_h, p);
+    const dim3 grid((unsigned)(per_sm * sm_count()));
+    if (scatter) return launch_dependent(k_gather_tc<true>, grid, dim3(kThreads), smem, s, map_e, map_h, p);
+    return launch_dependent(k_gather_tc<false>, grid, dim3(kThreads), smem, s, map_e, map_h, p);
 }
 
 // ---------------------------------------------------------------------------

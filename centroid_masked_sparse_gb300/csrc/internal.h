@@ -56,6 +56,9 @@ cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s
 constexpr int kTcGatherChunk = 128;
 // Expected rows per selected cluster (B*K/C) from which the tensor-core gather is used.
 constexpr int kTcGatherMinReuse = 4;
+// Batch sizes up to which the tensor-core gather's accumulators take at most half an
+// SM's TMEM, so that it runs two CTAs per SM.
+constexpr int kTcGatherPairBatch = 64;
 cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s);
 // The packed embedding table of the tensor-core gather (gather_tc.cu): byte size for
 // the shapes (an upper bound with explicit offsets) and the kernels that fill it.

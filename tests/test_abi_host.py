@@ -167,12 +167,25 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), -1) == -2
     assert L.mtp_gather_plan(ctypes.byref(d), 2000) == -6
     assert L.mtp_gather_plan(ctypes.byref(_desc(K=0)), 8) == -2
-    d.embed_packed = 0xA000                                  # packed table, uniform clusters
+    d.embed_packed = 0xA000                                  # packed table: from B*K >= C/2 up to batch 64
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 0
-    d = _desc(offsets=0x5000)                                # ragged clusters: only large buckets
+    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 31) == 0
+    d = _desc(K=16)                                          # above batch 64: from B*K >= C
     d.embed_packed = 0xA000
+    assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 65) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 128) == 1
+    d = _desc(H=256)                                         # small hidden size: from B*K >= C/8
+    d.embed_packed = 0xA000
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 7) == 0
+    d = _desc(offsets=0x5000)                                # ragged clusters: the same rules
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
+    d.embed_packed = 0xA000
+    assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 16) == 0
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1
 
 

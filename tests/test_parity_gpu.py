@@ -590,6 +590,8 @@ def _same_outputs(m, dh, h):
     (264, 64, None),               # large buckets: the tensor-core gather either way, K tail
     (264, 4, None),                # B*K = C: packed -> tensor cores, token order -> CUDA cores
     (64, 41, "ragged"),            # empty and oversized clusters, padding groups, table end
+    (64, 8, "ragged"),             # the same at B*K >= C: packed -> tensor cores, copies
+                                   # that stop short of a group's end
 ])
 def test_packed_table_parity(build_lib, H, B, sizes):
     """With the packed table attached every finish matches the oracle; where both
@@ -618,7 +620,8 @@ def test_packed_table_parity(build_lib, H, B, sizes):
         dh.drop_packed_table()
 
 
-@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64), ("uniform", 8), ("variable", 64)])
+@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64), ("uniform", 32), ("uniform", 8),
+                                    ("variable", 64), ("variable", 32)])
 def test_packed_table_full_size(build_lib, name, B):
     """Full-size tables with the packed table: token ids match the oracle and the
     token-order path exactly, logits within the fp32 tolerance (the packed call may run
