@@ -21,7 +21,7 @@ from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_M
                    MtpError, MtpHeadDesc, check, lib)
 
 __all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "MTP_FINISH_PAIR",
-           "MTP_FLAG_FILL_FINFO_MIN", "MTP_FLAG_BF16_SCORES", "MTP_FLAG_BF16_LOGITS", "mtp_workspace_bytes", "mtp_centroid_scores",
+           "MTP_FLAG_FILL_FINFO_MIN", "MTP_FLAG_BF16_SCORES", "MTP_FLAG_BF16_LOGITS", "MTP_FLAG_HOST_HIDDEN", "mtp_workspace_bytes", "mtp_centroid_scores",
            "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_select_and_score", "mtp_dense_lm_head",
            "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
            "mtp_masked_topk_keys", "mtp_decode_keys", "combine_keys", "sharded_topk_tokens",
@@ -54,7 +54,9 @@ class MaskedHead:
     cluster_offsets  int32 [C + 1] or None (uniform clusters of V / C)
     cluster_range    (begin, end): the clusters this GPU owns when the head is sharded
                      over GPUs by cluster, or None for all of them
-    flags            MTP_FLAG_* reference-fidelity options (0: fp32 scores and logits, -inf)
+    flags            MTP_FLAG_* options: the reference-fidelity readings (0: fp32 scores and
+                     logits, -inf), and MTP_FLAG_HOST_HIDDEN (hidden states may be pinned
+                     CPU tensors, staged into the workspace by the call itself)
     softcap          the dense head's final logit softcap, cap * tanh(logit / cap) (0: none)
     """
 
@@ -107,6 +109,15 @@ class MaskedHead:
         self.desc.embed_packed = packed.data_ptr()
         return packed
 
+    def with_flags(self, flags):
+        """A head over the same device tables (and packed table) with other flags."""
+        h = MaskedHead(self.centroid_w, self.embed_w, self.token_ordering, self.top_k,
+                       self.cluster_offsets, self.vocab_size, cluster_range=self.cluster_range,
+                       flags=flags, softcap=self.desc.final_logit_softcap)
+        if self.embed_packed is not None:
+            h.use_packed_table(self.embed_packed)
+        return h
+
     def drop_packed_table(self):
         self.embed_packed = None
         self.desc.embed_packed = None
@@ -145,10 +156,23 @@ def mtp_workspace_bytes(head: MaskedHead, max_batch: int) -> int:
 
 
 def _hidden_ok(head, hidden):
+    """Batch rows of `hidden`: on the head's GPU, or (MTP_FLAG_HOST_HIDDEN) a pinned CPU
+    tensor, which the library checks again and stages into the workspace."""
     torch = _torch()
     assert hidden.dtype == torch.bfloat16 and hidden.is_contiguous() and hidden.dim() == 2
-    assert hidden.shape[1] == head.hidden_size and hidden.device == head.device
+    assert hidden.shape[1] == head.hidden_size
+    if hidden.device != head.device:
+        assert head.desc.flags & MTP_FLAG_HOST_HIDDEN and hidden.device.type == "cpu" and hidden.is_pinned(), \
+            "hidden must be on the head's device, or a pinned CPU tensor with MTP_FLAG_HOST_HIDDEN"
     return int(hidden.shape[0])
+
+
+def _out_ok(head, *outs):
+    """Output arrays the device can write: on the head's GPU or pinned CPU tensors."""
+    for t in outs:
+        if t is not None and t.device != head.device:
+            assert t.device.type == "cpu" and t.is_pinned(), \
+                "outputs must be on the head's device or pinned CPU tensors"
 
 
 def mtp_centroid_scores(head, hidden, scores=None, topk_idx=None, with_topk=True, stream=None):
@@ -174,6 +198,7 @@ def mtp_masked_topk_tokens(head, hidden, out_tokens=None, out_max=None, workspac
         out_tokens = torch.empty(B, dtype=torch.int32, device=head.device)
     if with_max and out_max is None:
         out_max = torch.empty(B, dtype=torch.float32, device=head.device)
+    _out_ok(head, out_tokens, out_max)
     ws = workspace if workspace is not None else head.workspace(B)
     check(lib().mtp_masked_topk_tokens(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_tokens),
                                        _ptr(out_max), _ptr(ws), ws.numel() * ws.element_size(),
@@ -188,6 +213,7 @@ def mtp_masked_scatter_logits(head, hidden, out=None, workspace=None, stream=Non
     B = _hidden_ok(head, hidden)
     if out is None:
         out = torch.empty(B, head.vocab_size, dtype=torch.float32, device=head.device)
+    _out_ok(head, out)
     ws = workspace if workspace is not None else head.workspace(B)
     check(lib().mtp_masked_scatter_logits(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out),
                                           _ptr(ws), ws.numel() * ws.element_size(),
@@ -206,6 +232,7 @@ def mtp_select_and_score(head, hidden, out_logits=None, out_ids=None, with_ids=T
         out_logits = torch.empty(B, width, dtype=torch.float32, device=head.device)
     if with_ids and out_ids is None:
         out_ids = torch.empty(B, width, dtype=torch.int32, device=head.device)
+    _out_ok(head, out_logits, out_ids)
     ws = workspace if workspace is not None else head.workspace(B)
     check(lib().mtp_select_and_score(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_logits),
                                      _ptr(out_ids), _ptr(ws), ws.numel() * ws.element_size(),
@@ -224,8 +251,9 @@ def mtp_dense_lm_head(head, hidden, out_logits=None, out_tokens=None, out_max=No
         out_tokens = torch.empty(B, dtype=torch.int32, device=head.device)
         if out_max is None:
             out_max = torch.empty(B, dtype=torch.float32, device=head.device)
+    _out_ok(head, out_logits, out_tokens, out_max)
     ws = None
-    if out_tokens is not None:
+    if out_tokens is not None or head.desc.flags & MTP_FLAG_HOST_HIDDEN:
         ws = workspace if workspace is not None else head.workspace(B)
     check(lib().mtp_dense_lm_head(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_logits),
                                   _ptr(out_tokens), _ptr(out_max), _ptr(ws),
@@ -255,7 +283,7 @@ def mtp_gather_plan(head, batch: int) -> str:
 
 
 MTP_FINISH_ARGMAX, MTP_FINISH_SCATTER, MTP_FINISH_PAIR = 0, 1, 2
-MTP_FLAG_FILL_FINFO_MIN, MTP_FLAG_BF16_SCORES, MTP_FLAG_BF16_LOGITS = 1, 2, 4
+MTP_FLAG_FILL_FINFO_MIN, MTP_FLAG_BF16_SCORES, MTP_FLAG_BF16_LOGITS, MTP_FLAG_HOST_HIDDEN = 1, 2, 4, 8
 
 
 class CapturedCalls:
@@ -360,6 +388,7 @@ def mtp_masked_topk_keys(head, hidden, out_keys=None, workspace=None, stream=Non
     B = _hidden_ok(head, hidden)
     if out_keys is None:
         out_keys = torch.empty(B, dtype=torch.int64, device=head.device)
+    _out_ok(head, out_keys)
     ws = workspace if workspace is not None else head.workspace(B)
     check(lib().mtp_masked_topk_keys(ctypes.byref(head.desc), _ptr(hidden), B, _ptr(out_keys), _ptr(ws),
                                      ws.numel() * ws.element_size(), _stream_ptr(stream, head.device)),

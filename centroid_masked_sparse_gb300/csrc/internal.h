@@ -60,6 +60,9 @@ constexpr int kTcGatherMinReuse = 4;
 // SM's TMEM, so that it runs two CTAs per SM.
 constexpr int kTcGatherPairBatch = 64;
 cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s);
+// Copy `bytes` (a multiple of 16, both ends 16-byte aligned) from memory the device can
+// read (pinned host memory included) to device memory with one kernel.
+cudaError_t launch_stage_rows(void *dst, const void *src, size_t bytes, cudaStream_t s);
 // The packed embedding table of the tensor-core gather (gather_tc.cu): byte size for
 // the shapes (an upper bound with explicit offsets) and the kernels that fill it.
 // n = clusters the table holds (a shard's [c0, c1), or all C).

@@ -95,7 +95,7 @@ constexpr int kMaxChunk = 64;
 void *g_prof[5][2] = {};
 
 struct Layout {
-    size_t ctrl, keys, ccount, rowmask, zero_end, scores, topk, items, total;
+    size_t ctrl, keys, ccount, rowmask, zero_end, scores, topk, items, hidden, total;
     int W;
     int items_cap;
 };
@@ -124,6 +124,9 @@ Layout layout_for(const mtp_head_desc *d, int B)
     const size_t max_items = V / kMinChunk + nsel + 1;
     L.items = take(max_items * sizeof(int2));
     L.items_cap = (int)max_items;
+    // the staged copy of host-resident hidden states (last, so that a call with fewer
+    // rows than the workspace was sized for still fits)
+    L.hidden = (d->flags & MTP_FLAG_HOST_HIDDEN) ? take((size_t)B * d->hidden_size * 2) : off;
     L.total = off;
     return L;
 }
@@ -170,7 +173,7 @@ mtp_status check_desc(const mtp_head_desc *d, bool centroids, bool embed, bool o
         if (!aligned16(d->centroid_w)) return MTP_ERR_ALIGN;
         if (!span_ok(d)) return MTP_ERR_SHAPE;
     }
-    if (d->flags & ~(MTP_FLAG_FILL_FINFO_MIN | MTP_FLAG_BF16_SCORES | MTP_FLAG_BF16_LOGITS))
+    if (d->flags & ~(MTP_FLAG_FILL_FINFO_MIN | MTP_FLAG_BF16_SCORES | MTP_FLAG_BF16_LOGITS | MTP_FLAG_HOST_HIDDEN))
         return MTP_ERR_UNSUPPORTED;
     if (!(d->final_logit_softcap >= 0.f)) return MTP_ERR_SHAPE;   // negative or NaN
     if (ordering && !d->cluster_offsets && (d->num_centroids < 1 || d->vocab_size % d->num_centroids != 0))
@@ -219,6 +222,28 @@ struct Prof {
 };
 
 mtp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA; }
+
+// MTP_FLAG_HOST_HIDDEN: check that the device can read `hidden` (pinned or registered
+// host memory at its device address, managed memory, or this GPU's memory), copy the
+// batch's rows into the workspace's staging region with one kernel, and point the
+// rest of the call at that copy.  Launches nothing when the pointer is unusable.
+mtp_status stage_hidden(const mtp_head_desc *d, const void **hidden, int B, char *ws, const Layout &L,
+                        cudaStream_t s)
+{
+    if (!(d->flags & MTP_FLAG_HOST_HIDDEN)) return MTP_OK;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, *hidden) != cudaSuccess) {
+        cudaGetLastError();   // the failed query also sets the runtime's last error
+        return MTP_ERR_UNSUPPORTED;
+    }
+    if (a.type == cudaMemoryTypeUnregistered || a.devicePointer != *hidden) return MTP_ERR_UNSUPPORTED;
+    if (a.type == cudaMemoryTypeDevice && a.device != d->device) return MTP_ERR_UNSUPPORTED;
+    void *dst = ws + L.hidden;
+    mtp_status st = cuda_status(launch_stage_rows(dst, *hidden, (size_t)B * d->hidden_size * 2, s));
+    if (st != MTP_OK) return st;
+    *hidden = dst;
+    return MTP_OK;
+}
 
 // Steps 1-2: projection (+ workspace reset) and top-K (+ bucketing when rowmask is set).
 mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *scores,
@@ -350,6 +375,7 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     mtp_status st = use_device(d->device);
     if (st != MTP_OK) return st;
     char *ws = (char *)workspace;
+    if ((st = stage_hidden(d, &hidden, B, ws, L, s)) != MTP_OK) return st;
     if (out_logits && !sparse) {
         Prof pr(MTP_KERNEL_FILL, s);
         const float fill = (d->flags & MTP_FLAG_FILL_FINFO_MIN) ? -3.3895313892515355e38f : -INFINITY;
@@ -420,6 +446,7 @@ mtp_status mtp_centroid_scores(const mtp_head_desc *desc, const void *hidden, in
     if (st != MTP_OK) return st;
     if ((st = check_batch(batch)) != MTP_OK) return st;
     if (batch == 0) return MTP_OK;
+    if (desc->flags & MTP_FLAG_HOST_HIDDEN) return MTP_ERR_UNSUPPORTED;   // no workspace to stage into
     if (!hidden || !scores) return MTP_ERR_NULL;
     if (!aligned16(hidden)) return MTP_ERR_ALIGN;
     if ((st = use_device(desc->device)) != MTP_OK) return st;
@@ -482,18 +509,22 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
     if (!aligned16(hidden)) return MTP_ERR_ALIGN;
     cudaStream_t s = (cudaStream_t)stream;
     char *ws = (char *)workspace;
+    const bool host_hidden = (desc->flags & MTP_FLAG_HOST_HIDDEN) != 0;
     Layout L{};
-    if (out_tokens) {
-        // the workspace layout only depends on V, C, K, B; C and K may be unset for a dense head
+    if (out_tokens || host_hidden) {
+        // the workspace layout only depends on V, C, K, B (and the flags); C and K may be
+        // unset for a dense head
         mtp_head_desc d = *desc;
         if (d.num_centroids < 1) d.num_centroids = 1;
         if (d.top_k < 1 || d.top_k > d.num_centroids) d.top_k = 1;
         L = layout_for(&d, batch);
-        if (!ws || workspace_bytes < L.keys + (size_t)batch * sizeof(unsigned long long))
-            return MTP_ERR_WORKSPACE;
+        size_t need = out_tokens ? L.keys + (size_t)batch * sizeof(unsigned long long) : 0;
+        if (host_hidden) need = std::max(need, L.hidden + (size_t)batch * desc->hidden_size * 2);
+        if (!ws || workspace_bytes < need) return MTP_ERR_WORKSPACE;
         if (!aligned16(ws)) return MTP_ERR_ALIGN;
     }
     if ((st = use_device(desc->device)) != MTP_OK) return st;
+    if ((st = stage_hidden(desc, &hidden, batch, ws, L, s)) != MTP_OK) return st;
     if (out_tokens) {
         st = cuda_status(cudaMemsetAsync(ws, 0, L.keys + (size_t)batch * sizeof(unsigned long long), s));
         if (st != MTP_OK) return st;

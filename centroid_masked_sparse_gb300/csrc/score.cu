@@ -41,6 +41,8 @@
 // CTA to finish (a ticket, never a wait) turns the per-row keys into token
 // ids.  Every mbarrier wait gives up after a wall-clock limit and records
 // MTP_DEVERR_TIMEOUT rather than hanging.
+#include <algorithm>
+
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -607,6 +609,27 @@ cudaError_t launch_export_keys(const unsigned long long *keys, int B, int64_t *o
 cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, float *maxv, cudaStream_t s)
 {
     k_decode_keys<<<(B + 255) / 256, 256, 0, s>>>(keys, B, tokens, maxv);
+    return cudaGetLastError();
+}
+
+// Copy of the batch's hidden rows from memory the device reads over the host link
+// (pinned host memory) into the workspace: one 16-byte load per thread and round,
+// all of them in flight at once, so the copy costs about one link round trip.
+__global__ void __launch_bounds__(256) k_stage_rows(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
+                                                    size_t n16)
+{
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_stage_rows(void *dst, const void *src, size_t bytes, cudaStream_t s)
+{
+    if ((bytes & 15) || ((uintptr_t)dst & 15) || ((uintptr_t)src & 15)) return cudaErrorInvalidValue;
+    const size_t n16 = bytes / 16;
+    if (n16 == 0) return cudaSuccess;
+    const size_t blocks = std::min<size_t>((n16 + 255) / 256, (size_t)sm_count());
+    k_stage_rows<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<uint4 *>(dst),
+                                                 reinterpret_cast<const uint4 *>(src), n16);
     return cudaGetLastError();
 }
 

@@ -143,10 +143,31 @@ typedef enum mtp_status {
  *   MTP_FLAG_BF16_LOGITS     every sparse and dense logit is rounded to bf16 before
  *                            it is stored and before the argmax (ties then go to
  *                            the lower token id); outputs stay fp32 arrays.
+ * An input-placement option, not a reading of the page:
+ *   MTP_FLAG_HOST_HIDDEN     `hidden` may live in pinned host memory (cudaHostAlloc,
+ *                            cudaMallocHost, or cudaHostRegister'ed memory, at its
+ *                            device address: the same as the host address under
+ *                            unified addressing).  The call first copies the batch's
+ *                            rows into its workspace with one kernel of this
+ *                            library reading over the host link, then reads only
+ *                            that copy; this replaces a separate host-to-device
+ *                            copy ahead of the call and the wait for it.  The
+ *                            pointer is checked with cudaPointerGetAttributes:
+ *                            host memory the device cannot address (pageable,
+ *                            unregistered) or another GPU's memory give
+ *                            MTP_ERR_UNSUPPORTED and nothing is launched; device
+ *                            and managed memory are accepted and copied the same
+ *                            way.  The workspace grows by batch * H * 2 bytes
+ *                            (mtp_workspace_bytes counts it); calls without a
+ *                            workspace (mtp_centroid_scores, and the dense head
+ *                            without one) return MTP_ERR_UNSUPPORTED with it.
+ *                            Output arrays need no flag: any address the device
+ *                            can write works, pinned host memory included.
  * Other bits: MTP_ERR_UNSUPPORTED. */
 #define MTP_FLAG_FILL_FINFO_MIN 1
 #define MTP_FLAG_BF16_SCORES 2
 #define MTP_FLAG_BF16_LOGITS 4
+#define MTP_FLAG_HOST_HIDDEN 8
 
 typedef struct mtp_head_desc {
     int32_t vocab_size;
@@ -178,7 +199,7 @@ MTP_API size_t mtp_workspace_bytes(const mtp_head_desc *desc, int32_t max_batch)
  *   scores    fp32 [batch, C] out: s[b, c]
  *   topk_idx  int32 [batch, K] out, or NULL: the selected centroids of each row,
  *             sorted by (score desc, index asc) like a sorted topk
- * Needs no workspace. */
+ * Needs no workspace (so MTP_FLAG_HOST_HIDDEN is not accepted here). */
 MTP_API mtp_status mtp_centroid_scores(const mtp_head_desc *desc, const void *hidden, int32_t batch,
                                float *scores, int32_t *topk_idx, void *stream);
 
@@ -219,7 +240,8 @@ MTP_API mtp_status mtp_select_and_score(const mtp_head_desc *desc, const void *h
  *   out_logits  fp32 [batch, V] out (row stride V), or NULL
  *   out_tokens  int32 [batch] out, or NULL: dense argmax, lower id on ties
  *   out_max     fp32 [batch] out, or NULL (only with out_tokens)
- *   workspace   needed only when out_tokens != NULL (same size rule as above)
+ *   workspace   needed only when out_tokens != NULL or with MTP_FLAG_HOST_HIDDEN
+ *               (same size rule as above)
  * centroid_w, token_ordering and cluster_offsets are not read; at least one of
  * out_logits and out_tokens must be non-NULL. */
 MTP_API mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int32_t batch,

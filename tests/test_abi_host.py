@@ -253,10 +253,33 @@ def test_cluster_range_checks_and_packed_size(L):
 def test_unknown_flags_are_refused(L):
     out = ctypes.c_void_p(0x8000)
     d = _desc()
-    d.flags = 8
-    assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 1 << 30, None) == -6
-    assert L.mtp_dense_lm_head(ctypes.byref(d), FAKE, 4, out, None, None, None, 0, None) == -6
+    for bad in (16, 1 << 30, 15 | 32):
+        d.flags = bad
+        assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 1 << 30, None) == -6
+        assert L.mtp_dense_lm_head(ctypes.byref(d), FAKE, 4, out, None, None, None, 0, None) == -6
     d.flags = 7
+    assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 16, None) == -4
+
+
+def test_host_hidden_flag_host_checks(L):
+    """MTP_FLAG_HOST_HIDDEN: the workspace grows by the staged rows (B * H * 2 bytes,
+    with the layout's 256-byte rounding), calls without a workspace refuse the flag, and
+    a short workspace is refused before anything else happens."""
+    out = ctypes.c_void_p(0x8000)
+    d = _desc()
+    plain = [L.mtp_workspace_bytes(ctypes.byref(d), b) for b in (1, 7, 64)]
+    d.flags = 8
+    staged = [L.mtp_workspace_bytes(ctypes.byref(d), b) for b in (1, 7, 64)]
+    for b, p0, p1 in zip((1, 7, 64), plain, staged):
+        assert p1 - p0 == (b * 1536 * 2 + 255) // 256 * 256
+    scores = ctypes.c_void_p(0x9000)
+    assert L.mtp_centroid_scores(ctypes.byref(d), FAKE, 4, scores, None, None) == -6
+    assert L.mtp_centroid_scores(ctypes.byref(d), FAKE, 0, scores, None, None) == 0
+    # the dense head needs the workspace for the staged rows even without an argmax
+    assert L.mtp_dense_lm_head(ctypes.byref(d), FAKE, 4, out, None, None, None, 0, None) == -4
+    need = L.mtp_workspace_bytes(ctypes.byref(d), 4)
+    assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, need - 1, None) == -4
+    d.flags = 8 | 7   # combines with the fidelity options
     assert L.mtp_masked_topk_tokens(ctypes.byref(d), FAKE, 4, out, None, WS, 16, None) == -4
 
 

@@ -976,3 +976,86 @@ def test_dense_softcap(build_lib, cap, flags):
     ptok, _ = m.mtp_masked_topk_tokens(plain, h)
     torch.cuda.synchronize()
     assert torch.equal(tok, ptok)
+
+
+# ---------------------------------------------------------------------------
+# hidden states in pinned host memory, staged by the call itself
+
+
+@pytest.mark.parametrize("name,B,packed", [("uniform", 64, True), ("uniform", 8, False), ("variable", 32, True),
+                                           ("tiny", 1, False)])
+def test_host_hidden_equals_device_hidden(build_lib, name, B, packed):
+    """With MTP_FLAG_HOST_HIDDEN a call reads a pinned CPU batch through its staging kernel;
+    every finish then gives the same bits as the same call on a device copy of the batch,
+    with outputs on the device or in pinned host memory, and graphs capture the staging."""
+    m = build_lib
+    oh, dh = device_head(m, name)
+    if packed:
+        dh.use_packed_table()
+    try:
+        hh = dh.with_flags(m.MTP_FLAG_HOST_HIDDEN)
+        hidden = synth.hidden_batch(name, B, row0=777)
+        h_dev = helpers.bf16_tensor(hidden)
+        h_host = h_dev.cpu().pin_memory()
+        tok, mx = m.mtp_masked_topk_tokens(dh, h_dev)
+        sc = m.mtp_masked_scatter_logits(dh, h_dev)
+        keys = m.mtp_masked_topk_keys(dh, h_dev)
+        dl, dtok, dmax = m.mtp_dense_lm_head(dh, h_dev, want_tokens=True)
+        tok2, mx2 = m.mtp_masked_topk_tokens(hh, h_host)
+        tok3 = torch.empty(B, dtype=torch.int32).pin_memory()
+        mx3 = torch.empty(B, dtype=torch.float32).pin_memory()
+        m.mtp_masked_topk_tokens(hh, h_host, out_tokens=tok3, out_max=mx3)
+        sc2 = m.mtp_masked_scatter_logits(hh, h_host)
+        keys2 = m.mtp_masked_topk_keys(hh, h_host)
+        dl2, dtok2, dmax2 = m.mtp_dense_lm_head(hh, h_host, want_tokens=True)
+        dl3, _, _ = m.mtp_dense_lm_head(hh, h_host)          # no argmax: workspace for the staging only
+        torch.cuda.synchronize()
+        for a, b in ((tok, tok2), (mx, mx2), (sc, sc2), (keys, keys2), (dl, dl2), (dtok, dtok2), (dmax, dmax2),
+                     (dl, dl3)):
+            assert torch.equal(a, b)
+        assert torch.equal(tok.cpu(), tok3) and torch.equal(mx.cpu(), mx3)
+        ref = oracle.masked_topk_tokens(oh, hidden)
+        np.testing.assert_array_equal(tok2.cpu().numpy(), ref["tokens"])
+        if not synth.WORKLOADS[name].variable_clusters:
+            pl, pi = m.mtp_select_and_score(dh, h_dev)
+            pl2, pi2 = m.mtp_select_and_score(hh, h_host)
+            torch.cuda.synchronize()
+            assert torch.equal(pl, pl2) and torch.equal(pi, pi2)
+        assert m.mtp_read_device_error(hh.workspace(B)) == 0
+        # the staging kernel inside a captured graph (its static input is device memory,
+        # which the flag accepts as well)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            g = m.CapturedCalls(hh, sizes=(B,))
+            try:
+                gt, gm = g(h_dev)
+                torch.cuda.synchronize()
+                assert torch.equal(gt[:B], tok) and torch.equal(gm[:B], mx)
+            finally:
+                g.close()
+    finally:
+        dh.drop_packed_table()
+
+
+def test_host_hidden_refuses_memory_the_device_cannot_read(build_lib):
+    """A pageable (unregistered) CPU buffer with MTP_FLAG_HOST_HIDDEN is refused by the
+    library's pointer check (MTP_ERR_UNSUPPORTED, nothing launched) and by the binding."""
+    import ctypes
+    m = build_lib
+    _, dh = device_head(m, "tiny")
+    hh = dh.with_flags(m.MTP_FLAG_HOST_HIDDEN)
+    h = torch.zeros(2, dh.hidden_size, dtype=torch.bfloat16)
+    assert not h.is_pinned()
+    out = torch.full((2,), -7, dtype=torch.int32, device="cuda")
+    ws = hh.workspace(2)
+    st = m._lib.lib().mtp_masked_topk_tokens(ctypes.byref(hh.desc), ctypes.c_void_p(h.data_ptr()), 2,
+                                             ctypes.c_void_p(out.data_ptr()), None,
+                                             ctypes.c_void_p(ws.data_ptr()), ws.numel(), None)
+    assert st == -6
+    torch.cuda.synchronize()
+    assert (out.cpu() == -7).all()
+    with pytest.raises(AssertionError):
+        m.mtp_masked_topk_tokens(hh, h)
+    with pytest.raises(AssertionError):
+        m.mtp_masked_topk_tokens(dh, helpers.bf16_tensor(np.zeros((2, dh.hidden_size), np.uint16)),
+                                 out_tokens=torch.empty(2, dtype=torch.int32))   # pageable output
