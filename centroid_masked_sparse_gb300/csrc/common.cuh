@@ -171,6 +171,8 @@ struct ProjParams {
     int B, H, C;
     int rows_per_group;      // hidden rows staged in shared memory at a time
     int after_fill;          // launched behind the scatter's fill, overlapping it
+    int after_stage;         // launched behind the staging of host-resident hidden rows:
+                             // reads them only after griddepcontrol.wait
 };
 
 struct TopkParams {

@@ -60,6 +60,8 @@ struct TcParams {
     int cluster_reduce;     // splits > 1: one cluster per output tile, summed through DSMEM
     int round_bf16;         // dense head: logits rounded to bf16 before they are stored or compared
     float softcap;          // dense head: final logit softcap (cap * tanh(v / cap)), 0 = none
+    int after_stage;        // launched behind the staging of the hidden rows: the producer
+                            // waits for it (griddepcontrol.wait) before its first load
 };
 
 // Unit u = (m tile, n block, k split) with the split innermost, so that the
@@ -148,6 +150,8 @@ __global__ void __launch_bounds__(kTcThreads)
         if (lane == 0) {
             tma_prefetch_map(&tmap_a);
             tma_prefetch_map(&tmap_b);
+            // the B operand (hidden rows) is written by the staging kernel before this one
+            if (p.after_stage) asm volatile("griddepcontrol.wait;" ::: "memory");
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_par = 0;
             bool ok = true;
@@ -456,6 +460,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     p.cluster_reduce = p.splits > 1;
     p.round_bf16 = a.round_bf16 ? 1 : 0;
     p.softcap = a.softcap;
+    p.after_stage = a.after_stage ? 1 : 0;
     if (p.cluster_reduce && (size_t)stages * stage_bytes < (size_t)p.n_pad * kTileM * 4)
         return cudaErrorInvalidValue;
     if (p.cluster_reduce && (p.keys || p.splits > 8 || p.units > 65535)) return cudaErrorInvalidValue;
@@ -471,7 +476,8 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     if (!p.cluster_reduce) {
         int grid = sm_count();
         if (grid > p.units) grid = p.units;
-        if (a.after_fill) return launch_dependent(k_tc_gemm, dim3(grid), dim3(kTcThreads), smem, s, map_a, map_b, p);
+        if (a.after_fill || a.after_stage)
+            return launch_dependent(k_tc_gemm, dim3(grid), dim3(kTcThreads), smem, s, map_a, map_b, p);
         k_tc_gemm<<<grid, kTcThreads, smem, s>>>(map_a, map_b, p);
         return cudaGetLastError();
     }
@@ -489,7 +495,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.after_fill ? 2 : 1;
+    cfg.numAttrs = (a.after_fill || a.after_stage) ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, k_tc_gemm, map_a, map_b, p);
 }
 

@@ -91,6 +91,7 @@ struct TcGemmArgs {
     float *out_max;         // with keys, optional
     bool round_bf16;        // round each output to bf16 first (dense head option)
     bool after_fill;        // launched behind the scatter's fill, overlapping it
+    bool after_stage;       // launched behind the staging of host-resident hidden rows
     float softcap;          // dense head: cap * tanh(v / cap) for cap > 0
     uint32_t *zero;         // words cleared at kernel start (may be null)
     int zero_words;

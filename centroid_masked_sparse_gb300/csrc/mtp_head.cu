@@ -248,7 +248,7 @@ mtp_status stage_hidden(const mtp_head_desc *d, const void **hidden, int B, char
 // Steps 1-2: projection (+ workspace reset) and top-K (+ bucketing when rowmask is set).
 mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *scores,
                       int32_t *topk, char *ws, const Layout *L, int chunk, cudaStream_t s,
-                      bool after_fill = false)
+                      bool after_fill = false, bool after_stage = false)
 {
     if (B >= kTcProjMinBatch) {
         // tensor cores: M = C centroid rows, N = batch, K = H, split-K in a cluster
@@ -266,6 +266,7 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
         g.zero = ws ? (uint32_t *)ws : nullptr;
         g.zero_words = ws ? (int)(L->zero_end / sizeof(uint32_t)) : 0;
         g.after_fill = after_fill;
+        g.after_stage = after_stage;
         Prof pr(MTP_KERNEL_PROJECTION, s);
         mtp_status st = cuda_status(launch_tc_gemm(g, s));
         if (st != MTP_OK) return st;
@@ -281,6 +282,7 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
         pp.C = d->num_centroids;
         pp.rows_per_group = proj_rows_per_group(B, d->hidden_size);
         pp.after_fill = after_fill ? 1 : 0;
+        pp.after_stage = after_stage ? 1 : 0;
         Prof pr(MTP_KERNEL_PROJECTION, s);
         mtp_status st = cuda_status(launch_projection(pp, s));
         if (st != MTP_OK) return st;
@@ -384,8 +386,11 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     }
     int chunk = 0;
     const bool tc_gather = tc_gather_plan(d, B, &chunk);
-    st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s,
-                    out_logits && !sparse);
+    // the projection starts behind the staging kernel (programmatic launch) when it is the
+    // next kernel; behind the scatter's fill it is ordered by the fill's own launch
+    const bool fill = out_logits && !sparse;
+    st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s, fill,
+                    (d->flags & MTP_FLAG_HOST_HIDDEN) && !fill);
     if (st != MTP_OK) return st;
 
     GatherParams gp{};
@@ -524,11 +529,12 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
         if (!aligned16(ws)) return MTP_ERR_ALIGN;
     }
     if ((st = use_device(desc->device)) != MTP_OK) return st;
-    if ((st = stage_hidden(desc, &hidden, batch, ws, L, s)) != MTP_OK) return st;
     if (out_tokens) {
         st = cuda_status(cudaMemsetAsync(ws, 0, L.keys + (size_t)batch * sizeof(unsigned long long), s));
         if (st != MTP_OK) return st;
     }
+    // after the clear, so that the GEMM's programmatic launch follows the staging kernel
+    if ((st = stage_hidden(desc, &hidden, batch, ws, L, s)) != MTP_OK) return st;
     TcGemmArgs g{};
     g.table = desc->embed_w;
     g.ld_table = desc->ld_embed;
@@ -545,6 +551,7 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
     g.ctrl = out_tokens ? (uint32_t *)ws : nullptr;
     g.out_tokens = out_tokens;
     g.out_max = out_max;
+    g.after_stage = host_hidden;
     Prof pr(MTP_KERNEL_DENSE, s);
     return cuda_status(launch_tc_gemm(g, s));
 }

@@ -39,6 +39,9 @@ __global__ void __launch_bounds__(kProjThreads) k_projection(ProjParams p)
         w1[k] = (in && v1) ? ld_stream16(p.wc + (size_t)(c0 + 1) * p.H + idx * 8) : zero;
     }
 
+    // launched behind the kernel that stages host-resident hidden rows: the centroid
+    // rows above are already streaming; the hidden rows are read only once it is done
+    if (p.after_stage) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int b0 = 0; b0 < p.B; b0 += p.rows_per_group) {
         const int nb = min(p.rows_per_group, p.B - b0);
         __syncthreads();  // previous group fully consumed
@@ -83,7 +86,8 @@ static cudaError_t run_projection(const ProjParams &p, cudaStream_t s)
         return e;
     const int rows_per_cta = (kProjThreads / kWarp) * kProjRowsPerWarp;
     const int grid = (p.C + rows_per_cta - 1) / rows_per_cta;
-    if (p.after_fill) return launch_dependent(k_projection<NCH>, dim3(grid), dim3(kProjThreads), smem, s, p);
+    if (p.after_fill || p.after_stage)
+        return launch_dependent(k_projection<NCH>, dim3(grid), dim3(kProjThreads), smem, s, p);
     k_projection<NCH><<<grid, kProjThreads, smem, s>>>(p);
     return cudaGetLastError();
 }

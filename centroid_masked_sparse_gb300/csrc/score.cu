@@ -618,6 +618,8 @@ cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, floa
 __global__ void __launch_bounds__(256) k_stage_rows(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
                                                     size_t n16)
 {
+    // the projection behind it starts now and waits for this kernel before it reads the rows
+    asm volatile("griddepcontrol.launch_dependents;");
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
         dst[i] = src[i];
 }
