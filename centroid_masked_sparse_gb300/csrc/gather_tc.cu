@@ -69,7 +69,8 @@ constexpr int kBWarps = 4;         // warps that copy the buckets' hidden rows (
 constexpr int kThreads = (7 + kBWarps) * kWarp;
 constexpr int kTileM = 128;        // MMA M: candidate positions per unit (at most)
 constexpr int kTileK = 64;         // bf16 per k-block (128-byte rows)
-constexpr int kMaxN = 128;         // bucket rows per unit (at most)
+constexpr int kMaxN = 64;          // bucket rows per unit (at most): with four accumulators a CTA
+                                   // then takes at most half the TMEM, so two CTAs fit on an SM
 constexpr int kMeta = 8;           // unit-metadata ring
 constexpr int kAcc = 4;            // TMEM accumulators: the epilogues of the last units overlap the MMAs
 constexpr int kMaxStages = 32;
@@ -119,7 +120,7 @@ struct Params {
     int chunk;      // positions per work item (<= 128; a multiple of 32 when packed)
     const uint8_t *packed;    // packed table blocks, or null (token-order gathers)
     const int32_t *poff;      // its padded cluster offsets [C+1]
-    int nmax;       // bucket rows per unit (multiple of 16, <= 128)
+    int nmax;       // bucket rows per unit (multiple of 16, <= kMaxN)
     int num_kb;
     int stages;
     uint32_t a_bytes, b_bytes;   // stage sizes

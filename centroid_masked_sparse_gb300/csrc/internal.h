@@ -56,9 +56,6 @@ cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s
 constexpr int kTcGatherChunk = 128;
 // Expected rows per selected cluster (B*K/C) from which the tensor-core gather is used.
 constexpr int kTcGatherMinReuse = 4;
-// Batch sizes up to which the tensor-core gather's accumulators take at most half an
-// SM's TMEM, so that it runs two CTAs per SM.
-constexpr int kTcGatherPairBatch = 64;
 cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s);
 // Copy `bytes` (a multiple of 16, both ends 16-byte aligned) from memory the device can
 // read (pinned host memory included) to device memory with one kernel.

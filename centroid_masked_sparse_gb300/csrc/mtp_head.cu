@@ -330,10 +330,9 @@ int choose_chunk(const mtp_head_desc *d, int B)
 // large (B*K >= 4C), where one candidate tile serves a whole bucket.  With the
 // packed embedding table it also takes calls with fewer (row, cluster) pairs: its
 // block copies stream HBM faster than the CUDA-core gather's row copies and read
-// no padding rows.  Up to batch 64 it runs two CTAs per SM, and measured on
-// GB300 it is then ahead from B*K >= C/2 at H = 1536 and 2560 (level at C/4) and
-// from B*K >= C/8 at H = 256, where the CUDA-core gather's per-row costs weigh
-// most; above batch 64 (one CTA per SM) from B*K >= C.  Smaller calls keep more
+// no padding rows.  Running two CTAs per SM, it is ahead (measured on GB300) from
+// B*K >= C/2 at H = 1536 and 2560 (level at C/4) and from B*K >= C/8 at H = 256,
+// where the CUDA-core gather's per-row costs weigh most.  Smaller calls keep more
 // SMs busy with the CUDA-core gather's finer work items.  Its chunk is the largest
 // of 128, 64, 32 positions that still gives about two work items per SM.
 bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
@@ -341,13 +340,8 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
     const long long pairs = (long long)B * d->top_k;
     const long long C = d->num_centroids;
     const bool large = pairs >= (long long)kTcGatherMinReuse * C;
-    bool packed_reuse = false;
-    if (d->embed_packed) {
-        if (B <= kTcGatherPairBatch)
-            packed_reuse = 2 * pairs >= C || (d->hidden_size <= 256 && 8 * pairs >= C);
-        else
-            packed_reuse = pairs >= C;
-    }
+    const bool packed_reuse =
+        d->embed_packed && (2 * pairs >= C || (d->hidden_size <= 256 && 8 * pairs >= C));
     if (d->embed_packed && (large || packed_reuse)) {
         const double avg = (double)d->vocab_size / d->num_centroids;
         const double clusters = (double)std::min<long long>(pairs, d->num_centroids);

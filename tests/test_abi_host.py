@@ -167,14 +167,15 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), -1) == -2
     assert L.mtp_gather_plan(ctypes.byref(d), 2000) == -6
     assert L.mtp_gather_plan(ctypes.byref(_desc(K=0)), 8) == -2
-    d.embed_packed = 0xA000                                  # packed table: from B*K >= C/2 up to batch 64
+    d.embed_packed = 0xA000                                  # packed table: from B*K >= C/2
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 31) == 0
-    d = _desc(K=16)                                          # above batch 64: from B*K >= C
+    d = _desc(K=16)                                          # the same rule above batch 64
     d.embed_packed = 0xA000
+    assert L.mtp_gather_plan(ctypes.byref(d), 63) == 0
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 65) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 65) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 128) == 1
     d = _desc(H=256)                                         # small hidden size: from B*K >= C/8
     d.embed_packed = 0xA000
