@@ -544,7 +544,7 @@ def other_workloads(ctx, args, hbm):
     m, synth, torch = ctx["m"], ctx["synth"], ctx["torch"]
     res = {}
     steps = max(10, args.steps // 8)
-    cases = (("scatter", True, False), ("variable", False, False), ("shared", False, False),
+    cases = (("scatter", True, False), ("scatter", True, True), ("variable", False, False), ("shared", False, False),
              ("shared", True, False), ("uniform", False, False), ("uniform", False, True),
              ("variable", False, True), ("shared", False, True), ("shared", True, True),
              ("draft256", False, False), ("draft256", False, True))
@@ -578,7 +578,7 @@ def other_workloads(ctx, args, hbm):
                 "tokens_per_s": round(w.batch / (pr["call_ms"] * 1e-3), 1),
                 "gather_us": round(pr["kernel_ms"] * 1e3, 2), "output_bytes": pr["out_bytes"],
                 "device_error": pr["device_error"]}
-        if name == "scatter":
+        if name == "scatter" and not packed:
             d = measure_dense(ctx, t, dh, w.batch, steps, args.warmup)
             gbs = d["bytes"] / (d["kernel_ms"] * 1e-3) / 1e9
             res[f"dense_b{w.batch}"] = {"us_per_call": round(d["call_ms"] * 1e3, 2),
