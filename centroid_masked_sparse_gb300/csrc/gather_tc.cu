@@ -310,6 +310,7 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
 {
     int stage = 0;
     uint32_t phase = 0, issued = 0;
+    const uint64_t evict_first = l2_policy_evict_first();
     for (int u = 0;; ++u) {
         const int um = u % kMeta;
         if (!mbar_wait(mfull0 + 8u * um, (uint32_t)(u / kMeta) & 1u, kWaitNs)) {
@@ -363,8 +364,11 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
             const uint32_t bar = full0 + 8u * stage;
             const uint32_t a_dst = smem_u32(a_smem + (size_t)stage * p.a_bytes);
             if (p.packed) {
+                // candidate tiles are read once per call: first out of L2, so that the
+                // scatter's output rows and the hidden rows stay there
                 if (has_pk)
-                    bulk_copy_g2s(a_dst + pk_dst_off, pk_src + (size_t)kb * kPackBlock, pk_bytes, bar);
+                    bulk_copy_g2s_hint(a_dst + pk_dst_off, pk_src + (size_t)kb * kPackBlock, pk_bytes, bar,
+                                       evict_first);
             } else if (has_a) {
                 tma_gather4(a_dst + (uint32_t)lane * 4 * kRowBytes, tmap_e, kb * kTileK, y0, y1, y2, y3, bar);
             }
