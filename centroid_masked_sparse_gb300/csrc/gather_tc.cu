@@ -502,7 +502,7 @@ __device__ bool load_b(const Params &p, const UnitMeta *meta, uint8_t *b_smem, u
 }
 
 template <bool SCATTER>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_h,
                 const Params p)
 {
@@ -753,21 +753,21 @@ size_t smem_bytes(const Params &p, int stages)
 
 namespace {
 
-// Whether two CTAs of `kfn` with `smem` bytes of dynamic shared memory fit on one SM
+// Whether `n` CTAs of `kfn` with `smem` bytes of dynamic shared memory fit on one SM
 // (shared memory with the per-block reservation, threads, registers), from the
-// device's and the kernel's attributes (cached per kernel, device and size).  The
-// runtime's occupancy query answers one CTA here where two run side by side, so
+// device's and the kernel's attributes (cached per kernel, device, size and count).
+// The runtime's occupancy query answers one CTA here where two run side by side, so
 // the fit is worked out directly; the launch asks for the largest shared-memory
-// carveout so that the driver places both.  Were the answer ever wrong, the grid
-// would run in two waves: slower, still correct (each CTA holds at most half the
-// TMEM, so no allocation waits on a CTA that is not running).
-bool two_ctas_fit(const void *kfn, size_t smem)
+// carveout so that the driver places them all.  Were the answer ever wrong, the grid
+// would run in more waves: slower, still correct (the caller keeps n CTAs' TMEM
+// within the SM's, so no allocation waits on a CTA that is not running).
+bool ctas_fit(const void *kfn, size_t smem, int n)
 {
     static std::mutex mu;
-    static std::map<std::tuple<const void *, int, size_t>, bool> cache;
+    static std::map<std::tuple<const void *, int, size_t, int>, bool> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    const auto key = std::make_tuple(kfn, dev, smem);
+    const auto key = std::make_tuple(kfn, dev, smem, n);
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
@@ -781,8 +781,8 @@ bool two_ctas_fit(const void *kfn, size_t smem)
                cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) == cudaSuccess &&
                cudaFuncGetAttributes(&fa, kfn) == cudaSuccess;
     fit = fit && fa.numRegs > 0 &&
-          2 * (smem + fa.sharedSizeBytes + (size_t)resv) <= (size_t)smem_sm && 2 * kThreads <= thr_sm &&
-          2LL * kThreads * fa.numRegs <= (long long)regs_sm &&
+          (size_t)n * (smem + fa.sharedSizeBytes + (size_t)resv) <= (size_t)smem_sm && n * kThreads <= thr_sm &&
+          (long long)n * kThreads * fa.numRegs <= (long long)regs_sm &&
           cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess;
     std::lock_guard<std::mutex> lk(mu);
@@ -826,6 +826,9 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
             g.packed + packed_poff_offset(g.V, g.H, g.C, g.packed_clusters, g.offsets != nullptr));
     }
     p.nmax = std::min(kMaxN, (g.B + 15) & ~15);
+    // at most two (row, cluster) pairs per centroid: buckets are small, and units of at
+    // most 32 rows let three CTAs share an SM (a rare larger bucket takes more units)
+    if ((long long)g.B * g.K <= 2LL * g.C) p.nmax = std::min(p.nmax, 32);
     // the A stage holds the chunk: 32, 64 or 128 rows
     const int a_rows = p.chunk <= 32 ? 32 : p.chunk <= 64 ? 64 : kTileM;
     p.a_bytes = (uint32_t)a_rows * kRowBytes;
@@ -839,18 +842,20 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
         while (st > 2 && smem_bytes(p, st) > budget) --st;
         return st;
     };
-    // Two CTAs per SM where both fit (accumulators in half the TMEM each, stages in
-    // half the shared memory): each CTA's single-thread MMA issue, TMA issue and
-    // barrier round trips cost a few hundred ns per k-block, so a second pipeline per
-    // SM is what lets short chunks and small H reach the HBM rate.
+    // Two or three CTAs per SM where they fit (their accumulators within the SM's TMEM,
+    // at least three stages each in their share of the shared memory): each CTA's
+    // single-thread MMA issue, TMA issue and barrier round trips cost a few hundred ns
+    // per k-block, so more pipelines per SM let short chunks and small H reach the HBM
+    // rate and keep SMs busy through the last round of units.
     int per_sm = 1;
     int stages = fit_stages(220 * 1024);
-    if (p.tmem_cols <= kSmTmemCols / 2) {
-        const int st2 = fit_stages(110 * 1024);
-        const size_t smem2 = smem_bytes(p, st2);
-        if (st2 >= 3 && two_ctas_fit(kfn, smem2)) {
-            per_sm = 2;
-            stages = st2;
+    for (int n = 3; n >= 2; --n) {
+        if ((uint32_t)n * p.tmem_cols > kSmTmemCols) continue;
+        const int st = fit_stages((size_t)(220 / n) * 1024);
+        if (st >= 3 && ctas_fit(kfn, smem_bytes(p, st), n)) {
+            per_sm = n;
+            stages = st;
+            break;
         }
     }
     p.stages = stages;
