@@ -330,9 +330,10 @@ int choose_chunk(const mtp_head_desc *d, int B)
 // large (B*K >= 4C), where one candidate tile serves a whole bucket.  With the
 // packed embedding table it also takes calls with fewer (row, cluster) pairs: its
 // block copies stream HBM faster than the CUDA-core gather's row copies and read
-// no padding rows.  Running two CTAs per SM, it is ahead (measured on GB300) from
-// B*K >= C/2 at H = 1536 and 2560 (level at C/4) and from B*K >= C/8 at H = 256,
-// where the CUDA-core gather's per-row costs weigh most.  Smaller calls keep more
+// no padding rows.  Running two or three CTAs per SM, it is ahead (measured on
+// GB300) from B*K >= C/4 at H = 1536 and 2560 (behind at C/8) and from B*K >= C/16
+// at H = 256, where the CUDA-core gather's per-row costs weigh most (behind at
+// C/64).  Smaller calls keep more
 // SMs busy with the CUDA-core gather's finer work items.  Its chunk is the largest
 // of 128, 64, 32 positions that still gives about two work items per SM.
 bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
@@ -341,7 +342,7 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
     const long long C = d->num_centroids;
     const bool large = pairs >= (long long)kTcGatherMinReuse * C;
     const bool packed_reuse =
-        d->embed_packed && (2 * pairs >= C || (d->hidden_size <= 256 && 8 * pairs >= C));
+        d->embed_packed && (4 * pairs >= C || (d->hidden_size <= 256 && 16 * pairs >= C));
     if (d->embed_packed && (large || packed_reuse)) {
         const double avg = (double)d->vocab_size / d->num_centroids;
         const double clusters = (double)std::min<long long>(pairs, d->num_centroids);

@@ -167,26 +167,26 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), -1) == -2
     assert L.mtp_gather_plan(ctypes.byref(d), 2000) == -6
     assert L.mtp_gather_plan(ctypes.byref(_desc(K=0)), 8) == -2
-    d.embed_packed = 0xA000                                  # packed table: from B*K >= C/2
+    d.embed_packed = 0xA000                                  # packed table: from B*K >= C/4
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 31) == 0
-    d = _desc(K=16)                                          # the same rule above batch 64
+    assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 15) == 0
+    d = _desc(K=16)                                          # the same rule at any batch size
     d.embed_packed = 0xA000
-    assert L.mtp_gather_plan(ctypes.byref(d), 63) == 0
-    assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 31) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 65) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 128) == 1
-    d = _desc(H=256)                                         # small hidden size: from B*K >= C/8
+    d = _desc(H=256)                                         # small hidden size: from B*K >= C/16
     d.embed_packed = 0xA000
-    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 7) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 4) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 3) == 0
     d = _desc(offsets=0x5000)                                # ragged clusters: the same rules
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 16) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 0
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1
 
 
