@@ -363,8 +363,8 @@ MTP_API mtp_status mtp_graph_launch(const mtp_graph *graph, void *stream);
 MTP_API mtp_status mtp_graph_destroy(mtp_graph *graph);
 
 /* Which gather kernel a masked call with this descriptor and batch runs: 1 for
- * the tensor-core gather (large buckets, or the packed table over uniform
- * clusters with at least C row-cluster pairs), 0 for the CUDA-core gather, a
+ * the tensor-core gather (large buckets, batch * K >= 4C; or a packed table with
+ * batch * K >= C/4, or >= C/16 when H <= 256), 0 for the CUDA-core gather, a
  * negative mtp_status for an invalid descriptor or batch.  Host-only; for
  * profiling and benchmarks (the calls choose by themselves). */
 MTP_API int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch);
