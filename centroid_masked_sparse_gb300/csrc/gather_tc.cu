@@ -207,15 +207,19 @@ __device__ __forceinline__ void load_item(const Params &p, int2 rec, bool have, 
 // an end-of-stream entry.  False after a timed-out wait.
 __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, uint32_t mempty0, int lane)
 {
-    const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
     const int G = (int)gridDim.x;
-    const long long packed_groups = p.packed ? __ldg(p.poff + p.C) / kPackRows : 0;
     const int2 none = make_int2(-1, 0);
+    // this CTA's first two item records are loaded together with the item count, not
+    // after it (both slots lie inside the list; a record past the count is dropped)
+    const int2 rec0 = (int)blockIdx.x < p.items_cap ? p.items[blockIdx.x] : none;
+    const int2 rec1 = (int)blockIdx.x + G < p.items_cap ? p.items[blockIdx.x + G] : none;
+    const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
+    const long long packed_groups = p.packed ? __ldg(p.poff + p.C) / kPackRows : 0;
     int u = 0;
     int it = blockIdx.x;
     ItemPre nxt;
-    load_item(p, it < n_items ? p.items[it] : none, it < n_items, lane, nxt);
-    int2 rec2 = it + G < n_items ? p.items[it + G] : none;
+    load_item(p, it < n_items ? rec0 : none, it < n_items, lane, nxt);
+    int2 rec2 = it + G < n_items ? rec1 : none;
     for (; it < n_items; it += G) {
         const ItemPre cur = nxt;
         load_item(p, rec2, it + G < n_items, lane, nxt);

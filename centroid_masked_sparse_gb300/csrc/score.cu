@@ -166,18 +166,22 @@ __device__ __forceinline__ void load_item(const GatherParams &p, int2 item, bool
 __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int consumers)
 {
     const uint32_t rb = (uint32_t)p.H * 2;
+    const int G = (int)gridDim.x;
+    int it1 = (int)blockIdx.x, it2 = it1 + G;
+    const int2 invalid_item = make_int2(-1, 0);
+    // the first two item records are loaded together with the item count, not after it
+    // (both slots lie inside the list; a record past the count is dropped)
+    const int2 rec0 = it1 < p.items_cap ? p.items[it1] : invalid_item;
+    const int2 rec1 = it2 < p.items_cap ? p.items[it2] : invalid_item;
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
     const uint64_t pol = l2_policy_evict_first();
     const int step = p.step;
     const uint32_t ring = (uint32_t)p.ring;
     uint32_t seq = 0, huse = 0;
     uint32_t seq_slot = 0, seq_par = 0;   // slot and phase parity of sequence number `seq`
-    const int G = (int)gridDim.x;
-    int it1 = (int)blockIdx.x, it2 = it1 + G;
-    const int2 invalid_item = make_int2(-1, 0);
     ItemMeta nxt;
-    load_item(p, it1 < n_items ? p.items[it1] : invalid_item, it1 < n_items, lane, nxt);
-    int2 rec2 = it2 < n_items ? p.items[it2] : invalid_item;   // record of the item after next
+    load_item(p, it1 < n_items ? rec0 : invalid_item, it1 < n_items, lane, nxt);
+    int2 rec2 = it2 < n_items ? rec1 : invalid_item;   // record of the item after next
     for (;;) {
         const ItemMeta cur = nxt;
         if (!cur.valid) break;
