@@ -1059,3 +1059,38 @@ def test_host_hidden_refuses_memory_the_device_cannot_read(build_lib):
     with pytest.raises(AssertionError):
         m.mtp_masked_topk_tokens(dh, helpers.bf16_tensor(np.zeros((2, dh.hidden_size), np.uint16)),
                                  out_tokens=torch.empty(2, dtype=torch.int32))   # pageable output
+
+
+# ---------------------------------------------------------------------------
+# buckets larger than one unit of the tensor-core gather
+
+
+@pytest.mark.parametrize("B,K,C,packed", [(64, 4, 128, True), (128, 4, 128, False), (48, 8, 192, True),
+                                         (256, 4, 512, True), (200, 16, 64, True)])
+def test_buckets_split_over_units(build_lib, B, K, C, packed):
+    """Rows that share a hidden state share their selection, so the clusters they pick get
+    buckets larger than a unit of the tensor-core gather (32 rows when B*K <= 2C, 64 above),
+    split over several units whose candidate tiles repeat: every finish must still match the
+    oracle, and the pair's rows agree with the scatter."""
+    m = build_lib
+    V, H = C * 64, 192
+    t, oh, dh = _custom(m, V, H, C, K, seed=B + 7 * K)
+    g = np.random.default_rng(B * 1000 + K)
+    base = synth.random_hidden(1, H, B + K)[0]
+    hidden = synth.random_hidden(B, H, 2 * B + K)
+    crowd = g.choice(B, size=(3 * B) // 4, replace=False)
+    hidden[crowd] = base
+    if packed:
+        dh.use_packed_table()
+    assert m.mtp_gather_plan(dh, B) == "tensor_core"
+    ref = _full_check(m, oh, dh, hidden, f"split buckets B={B} K={K} C={C}")
+    # the crowd's rows all select the same clusters: one bucket of len(crowd) rows each
+    assert len(set(tuple(r) for r in ref["sel"][crowd])) == 1
+    h = helpers.bf16_tensor(hidden)
+    plog, pids = m.mtp_select_and_score(dh, h)
+    sc = m.mtp_masked_scatter_logits(dh, h)
+    torch.cuda.synchronize()
+    pl, pi, scn = plog.cpu().numpy(), pids.cpu().numpy(), sc.cpu().numpy()
+    for b in range(B):
+        np.testing.assert_array_equal(scn[b][pi[b]], pl[b])
+    assert m.mtp_read_device_error(dh.workspace(B)) == 0
