@@ -27,8 +27,8 @@
 // Tile rows that no load wrote hold stale data, which only feeds TMEM lanes and
 // columns the epilogue ignores.
 //
-// Warp roles per CTA (352 threads; two CTAs per SM where their TMEM and shared
-// memory fit, else one):
+// Warp roles per CTA (352 threads; two or three CTAs per SM where their TMEM and
+// shared memory fit, three with units of at most 32 bucket rows, else one):
 //   warp 4   metadata: walks this CTA's items and publishes each unit's token
 //            and row lists into a ring of kMeta entries, running ahead of the
 //            loads so that its dependent global reads (item record, row mask,
@@ -71,6 +71,7 @@ constexpr int kTileM = 128;        // MMA M: candidate positions per unit (at mo
 constexpr int kTileK = 64;         // bf16 per k-block (128-byte rows)
 constexpr int kMaxN = 64;          // bucket rows per unit (at most): with four accumulators a CTA
                                    // then takes at most half the TMEM, so two CTAs fit on an SM
+                                   // (three with the 32-row units of calls with small buckets)
 constexpr int kMeta = 8;           // unit-metadata ring
 constexpr int kAcc = 4;            // TMEM accumulators: the epilogues of the last units overlap the MMAs
 constexpr int kMaxStages = 32;
