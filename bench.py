@@ -63,6 +63,8 @@ def file_sha(path):
 
 def profiled_traffic(kernel_file, workload, batch):
     """DRAM bytes per launch from a committed ncu summary, if it still matches the kernel source."""
+    if kernel_file is None:
+        return None
     prof = os.path.join(ROOT, "profiles", f"{kernel_file}_{workload}_b{batch}.md")
     src = os.path.join(ROOT, "centroid_masked_sparse_gb300", "csrc", f"{kernel_file}.cu")
     try:
@@ -461,7 +463,8 @@ def gpu_main(args):
     kern_s = res["kernel_ms"] * 1e-3
     achieved = res["bytes"]["gather"] / kern_s / 1e9
     plan = m.mtp_gather_plan(dh, B)
-    kfile, kname = ("gather_tc", "k_gather_tc") if plan == "tensor_core" else ("score", "k_gather_score")
+    kfile, kname = {"tensor_core": ("gather_tc", "k_gather_tc"),
+                    "cuda_core_direct": (None, "k_gather_direct")}.get(plan, ("score", "k_gather_score"))
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": hbm, "peak_source": f"{hbm_src} HBM copy GB/s", "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),

@@ -275,11 +275,12 @@ def mtp_pack_embeddings(head, out, workspace=None, stream=None):
 
 
 def mtp_gather_plan(head, batch: int) -> str:
-    """'tensor_core' or 'cuda_core': the gather kernel a masked call of this batch runs."""
+    """'tensor_core', 'cuda_core' or 'cuda_core_direct': the gather kernel a masked call
+    (argmax or scatter finish) of this batch runs."""
     r = int(lib().mtp_gather_plan(ctypes.byref(head.desc), int(batch)))
     if r < 0:
         check(r, "mtp_gather_plan")
-    return "tensor_core" if r == 1 else "cuda_core"
+    return {1: "tensor_core", 2: "cuda_core_direct"}.get(r, "cuda_core")
 
 
 MTP_FINISH_ARGMAX, MTP_FINISH_SCATTER, MTP_FINISH_PAIR = 0, 1, 2

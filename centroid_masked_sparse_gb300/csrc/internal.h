@@ -50,6 +50,9 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
 void gather_geometry(GatherParams &p);
 size_t gather_smem_bytes(const GatherParams &p);
 cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s);
+// Direct CUDA-core variant for batches of at most 8 rows (score.cu; no sparse pair).
+cudaError_t launch_gather_direct(const GatherParams &p, bool scatter, cudaStream_t s);
+constexpr int kDirectGatherMaxBatch = 8;
 // Tensor-core variant of the gather (gather_tc.cu); p.chunk <= 128, a multiple of 32
 // when p.packed is set.
 cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s);

@@ -359,6 +359,11 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
     return false;
 }
 
+// Small batches that the tensor-core gather does not take run the direct CUDA-core
+// gather (each warp loads candidate rows straight into registers) instead of the
+// pipelined one: its latency chain is shorter when there are few rows per SM.
+bool direct_gather(int B, bool sparse) { return !sparse && B <= kDirectGatherMaxBatch; }
+
 // The masked calls.  Finishes: the sparse argmax (out_tokens), the full-vocabulary
 // scatter (out_logits [B, V]) or, with `sparse`, the sparse pair (out_logits and
 // out_ids [B, K*S], every entry written, so no -inf fill).
@@ -422,6 +427,7 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     gp.chunk = chunk;
     Prof pr(MTP_KERNEL_GATHER_SCORE, s);
     if (tc_gather) return cuda_status(launch_gather_tc(gp, out_logits != nullptr, s));
+    if (direct_gather(B, sparse)) return cuda_status(launch_gather_direct(gp, out_logits != nullptr, s));
     gather_geometry(gp);
     return cuda_status(launch_gather(gp, out_logits != nullptr, s));
 }
@@ -628,7 +634,8 @@ int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch)
     if (st != MTP_OK) return st;
     if (batch == 0) return 0;
     int chunk = 0;
-    return tc_gather_plan(desc, batch, &chunk) ? 1 : 0;
+    if (tc_gather_plan(desc, batch, &chunk)) return 1;
+    return direct_gather(batch, false) ? 2 : 0;
 }
 
 mtp_status mtp_read_device_error(const void *workspace, uint32_t *host_word, void *stream)

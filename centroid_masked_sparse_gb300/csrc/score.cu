@@ -616,6 +616,145 @@ cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, floa
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Direct variant for small batches (at most kDirectMaxB rows): every warp takes one
+// candidate at a time, as (work item, position) pairs dealt round-robin over all
+// warps of the grid, loads its embedding row straight into registers (16 bytes per
+// lane per 256 elements, all in flight at once) and dots it with the bucket's hidden
+// rows, which each CTA keeps in shared memory.  No producer and no ring: with few
+// candidate rows per SM the pipelined gather's time is its chain of latencies (item
+// record, metadata, copy, hand-off), and here a row costs one load round trip, with
+// tens of rows in flight per SM.  Same results as the pipelined kernel up to the
+// summation order of each dot product; the sparse pair is not done here.
+// ---------------------------------------------------------------------------
+constexpr int kDirectThreads = 256;
+constexpr int kDirectMaxB = 8;
+
+template <int NCH, bool SCATTER>
+__global__ void __launch_bounds__(kDirectThreads) k_gather_direct(const GatherParams p)
+{
+    extern __shared__ uint4 hsm[];   // [B][H / 8] hidden rows
+    __shared__ unsigned long long s_best[kDirectMaxB];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid / kWarp;
+    const int hv = p.H >> 3;
+    if (!SCATTER && tid < kDirectMaxB) s_best[tid] = 0ull;
+    // the items and buckets come from the top-K kernel before this one (and the hidden
+    // rows, with host-resident input, from the staging kernel before that)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int i = tid; i < p.B * hv; i += kDirectThreads) hsm[i] = ld_ro16(p.hidden + (size_t)i * 8);
+    __syncthreads();
+
+    const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
+    const int n_cand = n_items * p.chunk;
+    const int nwarps = (int)gridDim.x * (kDirectThreads / kWarp);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    unsigned long long best[kDirectMaxB];   // this warp's best key per row (every lane the same)
+#pragma unroll
+    for (int j = 0; j < kDirectMaxB; ++j) best[j] = 0ull;
+
+    for (int cand = (int)blockIdx.x * (kDirectThreads / kWarp) + warp; cand < n_cand; cand += nwarps) {
+        const int it = cand / p.chunk, pos = cand - it * p.chunk;
+        const int2 rec = p.items[it];
+        int lo, hi;
+        if (!cluster_range(p.offsets, p.V, p.S, rec.x, &lo, &hi, p.ctrl + kCtrlError)) continue;
+        const int at = lo + rec.y + pos;
+        if (at >= hi) continue;   // past the end of a tail chunk
+        const int tok = __ldg(p.ordering + at);
+        if ((unsigned)tok >= (unsigned)p.V) {
+            if (lane == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
+            continue;
+        }
+        uint32_t mask = __ldcg(p.rowmask + (size_t)rec.x * p.W);   // B <= 32: one word
+        const uint16_t *row = p.embed + (size_t)tok * p.ld;
+        uint4 e[NCH];
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+            const int idx = k * kWarp + lane;
+            e[k] = idx < hv ? ld_stream16(row + (size_t)idx * 8) : zero;
+        }
+        while (mask) {
+            const int b = __ffs(mask) - 1;
+            mask &= mask - 1u;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < NCH; ++k) {
+                const int idx = k * kWarp + lane;
+                if (idx < hv) acc = dot8_bf16_mixed(e[k], hsm[b * hv + idx], acc);
+            }
+            acc = warp_sum(acc);
+            if (p.bf16_logits) acc = round_bf16(acc);
+            if (SCATTER) {
+                if (lane == 0) p.out_logits[(size_t)b * p.V + tok] = acc;
+            } else {
+                const unsigned long long key = argmax_key(acc, tok);
+#pragma unroll
+                for (int j = 0; j < kDirectMaxB; ++j)
+                    if (j == b && key > best[j]) best[j] = key;
+            }
+        }
+    }
+    if (SCATTER) return;
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < kDirectMaxB; ++j)
+            if (best[j]) atomicMax(&s_best[j], best[j]);
+    }
+    __syncthreads();
+    if (tid < p.B && s_best[tid]) atomicMax(p.keys + tid, s_best[tid]);
+    // the last CTA to finish turns the keys into token ids
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(p.ctrl + kCtrlTicket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (tid < p.B) {
+        const unsigned long long k = atomicAdd(p.keys + tid, 0ull);
+        int32_t t;
+        float v;
+        decode_argmax_key(k, &t, &v);
+        p.out_tokens[tid] = t;
+        if (p.out_max) p.out_max[tid] = v;
+    }
+}
+
+template <int NCH, bool SCATTER>
+cudaError_t run_gather_direct(const GatherParams &p, cudaStream_t s)
+{
+    const size_t smem = (size_t)p.B * (size_t)(p.H / 8) * sizeof(uint4);
+    const void *fn = (const void *)k_gather_direct<NCH, SCATTER>;
+    cudaError_t e = allow_smem(fn, smem);
+    if (e != cudaSuccess) return e;
+    const int per_sm = std::max(1, std::min(4, blocks_per_sm(fn, kDirectThreads, smem)));
+    return launch_dependent(k_gather_direct<NCH, SCATTER>, dim3((unsigned)(per_sm * sm_count())),
+                            dim3(kDirectThreads), smem, s, p);
+}
+
+template <bool SCATTER>
+cudaError_t dispatch_gather_direct(const GatherParams &p, cudaStream_t s)
+{
+    switch (chunks_for_hidden(p.H)) {
+    case 1: return run_gather_direct<1, SCATTER>(p, s);
+    case 2: return run_gather_direct<2, SCATTER>(p, s);
+    case 3: return run_gather_direct<3, SCATTER>(p, s);
+    case 4: return run_gather_direct<4, SCATTER>(p, s);
+    case 5: return run_gather_direct<5, SCATTER>(p, s);
+    case 6: return run_gather_direct<6, SCATTER>(p, s);
+    case 8: return run_gather_direct<8, SCATTER>(p, s);
+    case 10: return run_gather_direct<10, SCATTER>(p, s);
+    case 12: return run_gather_direct<12, SCATTER>(p, s);
+    case 16: return run_gather_direct<16, SCATTER>(p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gather_direct(const GatherParams &p, bool scatter, cudaStream_t s)
+{
+    if (p.B < 1 || p.B > kDirectMaxB || p.W != 1 || p.chunk < 1 || p.sparse_width) return cudaErrorInvalidValue;
+    return scatter ? dispatch_gather_direct<true>(p, s) : dispatch_gather_direct<false>(p, s);
+}
+
 // Copy of the batch's hidden rows from memory the device reads over the host link
 // (pinned host memory) into the workspace: one 16-byte load per thread and round,
 // all of them in flight at once, so the copy costs about one link round trip.
