@@ -17,7 +17,8 @@ int sm_count();
 // Resident CTAs per SM for a kernel (cached per kernel and shared-memory size).
 int blocks_per_sm(const void *kernel, int block, size_t smem);
 
-// Raise a kernel's dynamic shared-memory limit once.
+// Raise a kernel's dynamic shared-memory limit to at least `smem` (cached per kernel
+// and device; done for any nonzero size, since static shared memory shares the limit).
 cudaError_t allow_smem(const void *kernel, size_t smem);
 
 // Launch with programmatic stream serialization: the kernel may start while the
@@ -50,9 +51,9 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
 void gather_geometry(GatherParams &p);
 size_t gather_smem_bytes(const GatherParams &p);
 cudaError_t launch_gather(const GatherParams &p, bool scatter, cudaStream_t s);
-// Direct CUDA-core variant for batches of at most 8 rows (score.cu; no sparse pair).
+// Direct CUDA-core variant for batches of at most 32 rows (score.cu; no sparse pair);
+// its hidden rows, B x H bf16, must fit in shared memory.
 cudaError_t launch_gather_direct(const GatherParams &p, bool scatter, cudaStream_t s);
-constexpr int kDirectGatherMaxBatch = 8;
 // Tensor-core variant of the gather (gather_tc.cu); p.chunk <= 128, a multiple of 32
 // when p.packed is set.
 cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s);

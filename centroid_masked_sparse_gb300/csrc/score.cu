@@ -628,7 +628,7 @@ cudaError_t launch_decode_keys(const int64_t *keys, int B, int32_t *tokens, floa
 // summation order of each dot product; the sparse pair is not done here.
 // ---------------------------------------------------------------------------
 constexpr int kDirectThreads = 256;
-constexpr int kDirectMaxB = 8;
+constexpr int kDirectMaxB = 32;   // one row-mask word
 
 template <int NCH, bool SCATTER>
 __global__ void __launch_bounds__(kDirectThreads) k_gather_direct(const GatherParams p)
@@ -649,9 +649,6 @@ __global__ void __launch_bounds__(kDirectThreads) k_gather_direct(const GatherPa
     const int n_cand = n_items * p.chunk;
     const int nwarps = (int)gridDim.x * (kDirectThreads / kWarp);
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    unsigned long long best[kDirectMaxB];   // this warp's best key per row (every lane the same)
-#pragma unroll
-    for (int j = 0; j < kDirectMaxB; ++j) best[j] = 0ull;
 
     for (int cand = (int)blockIdx.x * (kDirectThreads / kWarp) + warp; cand < n_cand; cand += nwarps) {
         const int it = cand / p.chunk, pos = cand - it * p.chunk;
@@ -686,20 +683,12 @@ __global__ void __launch_bounds__(kDirectThreads) k_gather_direct(const GatherPa
             if (p.bf16_logits) acc = round_bf16(acc);
             if (SCATTER) {
                 if (lane == 0) p.out_logits[(size_t)b * p.V + tok] = acc;
-            } else {
-                const unsigned long long key = argmax_key(acc, tok);
-#pragma unroll
-                for (int j = 0; j < kDirectMaxB; ++j)
-                    if (j == b && key > best[j]) best[j] = key;
+            } else if (lane == 0) {
+                atomicMax(&s_best[b], argmax_key(acc, tok));   // the CTA's best per row
             }
         }
     }
     if (SCATTER) return;
-    if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < kDirectMaxB; ++j)
-            if (best[j]) atomicMax(&s_best[j], best[j]);
-    }
     __syncthreads();
     if (tid < p.B && s_best[tid]) atomicMax(p.keys + tid, s_best[tid]);
     // the last CTA to finish turns the keys into token ids

@@ -362,13 +362,14 @@ MTP_API mtp_status mtp_graph_launch(const mtp_graph *graph, void *stream);
  * replay is still in flight. */
 MTP_API mtp_status mtp_graph_destroy(mtp_graph *graph);
 
-/* Which gather kernel a masked call with this descriptor and batch runs: 1 for
- * the tensor-core gather (large buckets, batch * K >= 4C; or a packed table with
- * batch * K >= C/4, or >= C/16 when H <= 256); otherwise 2 for the direct
- * CUDA-core gather (batches of at most 8 rows; the sparse pair of such a batch
- * runs the pipelined one) and 0 for the pipelined CUDA-core gather; a negative
- * mtp_status for an invalid descriptor or batch.  Host-only; for profiling and
- * benchmarks (the calls choose by themselves). */
+/* Which gather kernel a masked argmax or scatter call with this descriptor and
+ * batch runs: 2 for the direct CUDA-core gather (batches of at most 8 rows, and of
+ * at most 12 where the tensor-core gather would not run), else 1 for the
+ * tensor-core gather (large buckets, batch * K >= 4C; or a packed table with
+ * batch * K >= C/4, or >= C/16 when H <= 256), else 0 for the pipelined CUDA-core
+ * gather; a negative mtp_status for an invalid descriptor or batch.  The sparse
+ * pair never runs the direct gather.  Host-only; for profiling and benchmarks (the
+ * calls choose by themselves). */
 MTP_API int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch);
 
 /* Enqueue an asynchronous copy of the workspace's device error word (a set of

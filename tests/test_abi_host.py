@@ -162,8 +162,8 @@ def test_packed_table_sizes_and_checks(L):
 def test_gather_plan(L):
     d = _desc()
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0      # B*K = C: CUDA-core gather
-    assert L.mtp_gather_plan(ctypes.byref(d), 9) == 0
-    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2       # small batches: the direct one
+    assert L.mtp_gather_plan(ctypes.byref(d), 13) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 12) == 2      # small batches: the direct one
     assert L.mtp_gather_plan(ctypes.byref(d), 1) == 2
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1     # B*K = 4C: large buckets
     assert L.mtp_gather_plan(ctypes.byref(d), 0) == 0
@@ -182,7 +182,8 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), 128) == 1
     d = _desc(H=256)                                         # small hidden size: from B*K >= C/16
     d.embed_packed = 0xA000
-    assert L.mtp_gather_plan(ctypes.byref(d), 4) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 9) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2       # up to 8 rows the direct one wins
     assert L.mtp_gather_plan(ctypes.byref(d), 3) == 2
     d = _desc(offsets=0x5000)                                # ragged clusters: the same rules
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
