@@ -97,7 +97,12 @@ struct TcGemmArgs {
     uint32_t *zero;         // words cleared at kernel start (may be null)
     int zero_words;
 };
-constexpr int kTcProjMinBatch = 4;  // projection on tensor cores from this batch size up
+// The projection runs on tensor cores from batch 4 up once B * H exceeds this; below,
+// the CUDA-core GEMV (whose per-row work grows with B * H while both read the table
+// once) is ahead: measured at H=1536 B=4 28.3 vs 30.3 us per call, B=8 level; at
+// H=256 B=8 27.8 vs 30.3 us; at H=2560 B=8 54.9 vs 50.8 us.
+constexpr int kTcProjMinBatch = 4;
+constexpr long long kCudaCoreProjMaxWork = 8192;
 int tc_splits(int M, int N, int K);
 cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s);
 

@@ -715,7 +715,7 @@ cudaError_t run_gather_direct(const GatherParams &p, cudaStream_t s)
     const void *fn = (const void *)k_gather_direct<NCH, SCATTER>;
     cudaError_t e = allow_smem(fn, smem);
     if (e != cudaSuccess) return e;
-    const int per_sm = std::max(1, std::min(4, blocks_per_sm(fn, kDirectThreads, smem)));
+    const int per_sm = std::max(1, std::min(8, blocks_per_sm(fn, kDirectThreads, smem)));
     return launch_dependent(k_gather_direct<NCH, SCATTER>, dim3((unsigned)(per_sm * sm_count())),
                             dim3(kDirectThreads), smem, s, p);
 }
