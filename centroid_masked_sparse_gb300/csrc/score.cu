@@ -653,9 +653,12 @@ __global__ void __launch_bounds__(kDirectThreads) k_gather_direct(const GatherPa
     for (int cand = (int)blockIdx.x * (kDirectThreads / kWarp) + warp; cand < n_cand; cand += nwarps) {
         const int it = cand / p.chunk, pos = cand - it * p.chunk;
         const int2 rec = p.items[it];
+        // a slot the top-K left unwritten (an append it dropped with overlapping offsets)
+        // holds stale data: such records are skipped, never followed
+        if ((unsigned)rec.x >= (unsigned)p.C || rec.y < 0) continue;
         int lo, hi;
         if (!cluster_range(p.offsets, p.V, p.S, rec.x, &lo, &hi, p.ctrl + kCtrlError)) continue;
-        const int at = lo + rec.y + pos;
+        const int at = (rec.y > hi - lo ? hi : lo + rec.y) + pos;
         if (at >= hi) continue;   // past the end of a tail chunk
         const int tok = __ldg(p.ordering + at);
         if ((unsigned)tok >= (unsigned)p.V) {
