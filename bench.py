@@ -21,6 +21,7 @@ host cores instead, on the same workload and metric.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -234,15 +235,22 @@ class Timer:
         torch.cuda.synchronize()
         barrier(ws)
         torch.cuda.synchronize()
-        t0 = time.time()
-        for i in range(steps):
-            self.flush_l2()
-            for k in names:
-                m.mtp_profile_events(k, kev[k][2 * i], kev[k][2 * i + 1])
-            call_ev[2 * i].record()
-            fn(i)
-            call_ev[2 * i + 1].record()
-        torch.cuda.synchronize()
+        # no garbage collection inside the loop: a collection that stalls the host long
+        # enough to drain the launch queue would leave the GPU idle inside a timed call
+        gc.collect()
+        gc.disable()
+        try:
+            t0 = time.time()
+            for i in range(steps):
+                self.flush_l2()
+                for k in names:
+                    m.mtp_profile_events(k, kev[k][2 * i], kev[k][2 * i + 1])
+                call_ev[2 * i].record()
+                fn(i)
+                call_ev[2 * i + 1].record()
+            torch.cuda.synchronize()
+        finally:
+            gc.enable()
         barrier(ws)
         torch.cuda.synchronize()
         t1 = time.time()
@@ -294,7 +302,8 @@ def measure_masked(ctx, t, dh, name, B, steps, warmup, scatter=False, rot=4, row
     kern_ms = float(np.mean(kern))
     return dict(call_ms=call_ms, kernel_ms=kern_ms, t0=t0, t1=t1, bytes=bm,
                 launches_per_call=4 if scatter else 3, kernels_us=breakdown,
-                max_call_us=round(float(np.max(call)) * 1e3, 2), device_error=dev_err)
+                max_call_us=round(float(np.max(call)) * 1e3, 2),
+                median_call_us=round(float(np.median(call)) * 1e3, 2), device_error=dev_err)
 
 
 def measure_graph(ctx, t, dh, name, B, steps, warmup, rot=4, row0=0):
@@ -488,7 +497,8 @@ def gpu_main(args):
                              "unique_clusters": res["bytes"]["unique_clusters"]},
            "roofline": roofline,
            "kernels_us": res["kernels_us"],
-           "max_call_us": res["max_call_us"], "device_error": res["device_error"],
+           "max_call_us": res["max_call_us"], "median_call_us": res["median_call_us"],
+           "device_error": res["device_error"],
            "gpu_launches": res["launches_per_call"] * args.steps,
            "clocks": clocks}
 
