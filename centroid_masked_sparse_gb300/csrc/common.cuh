@@ -42,6 +42,19 @@ __device__ __forceinline__ uint4 ld_ro16(const void *p)
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+// L2 prefetch hint for a small read-only table (token ordering, cluster offsets) that a
+// gather kernel reads on the dependent chain of every work item: issued before the
+// kernel waits for the previous kernel of the call, so the table is in L2 by the time
+// the work items arrive.  The grid's threads take one 128-byte step of the table each;
+// every address lies inside it.
+__device__ __forceinline__ void prefetch_l2_table(const void *base, size_t bytes)
+{
+    if (base == nullptr) return;
+    const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+    for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 128; off < bytes; off += nthreads * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"((const char *)base + off));
+}
+
 // ---------------------------------------------------------------------------
 // bf16 arithmetic: a bf16 is the top half of an fp32, so unpacking is a shift
 // or a mask; products of two bf16 values are exact in fp32.

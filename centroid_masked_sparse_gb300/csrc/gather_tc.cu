@@ -554,6 +554,9 @@ __global__ void __launch_bounds__(kThreads, 3)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    prefetch_l2_table(p.ordering, (size_t)p.V * sizeof(int32_t));
+    prefetch_l2_table(p.offsets, (size_t)(p.C + 1) * sizeof(int32_t));
+    if (p.packed) prefetch_l2_table(p.poff, (size_t)(p.C + 1) * sizeof(int32_t));
     // the work items and buckets come from the top-K kernel before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t acc_cols = p.tmem_cols / kAcc;

@@ -450,6 +450,8 @@ __global__ void __launch_bounds__((NW + 1) * kWarp, NW >= 16 ? 1 : 2) k_gather_s
     if (!SCATTER)
         for (int b = threadIdx.x; b < p.B; b += kThreads) sm.best[b] = 0ull;
     __syncthreads();
+    prefetch_l2_table(p.ordering, (size_t)p.V * sizeof(int32_t));
+    prefetch_l2_table(p.offsets, (size_t)(p.C + 1) * sizeof(int32_t));
     // the work items, row masks and counters come from the top-K kernel before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -639,6 +641,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_gather_direct(const GatherPa
     const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid / kWarp;
     const int hv = p.H >> 3;
     if (!SCATTER && tid < kDirectMaxB) s_best[tid] = 0ull;
+    prefetch_l2_table(p.ordering, (size_t)p.V * sizeof(int32_t));
+    prefetch_l2_table(p.offsets, (size_t)(p.C + 1) * sizeof(int32_t));
     // the items and buckets come from the top-K kernel before this one (and the hidden
     // rows, with host-resident input, from the staging kernel before that)
     asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     for (int i = tid; i < kKeyBuckets; i += kTopkThreads) hist[i] = 0u;
     if (tid == 0) s_ncand = 0;
     __syncthreads();
+    // the first selector of a cluster reads its range from the offsets table
+    if (p.rowmask) prefetch_l2_table(p.offsets, (size_t)(p.C + 1) * sizeof(int32_t));
     // the scores are written by the projection kernel that precedes this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
