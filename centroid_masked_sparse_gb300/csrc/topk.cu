@@ -68,23 +68,42 @@ __device__ __forceinline__ unsigned long long select_key(uint32_t ord, int c)
     return ((unsigned long long)ord << 32) | (unsigned long long)(0xffffffffu - (uint32_t)c);
 }
 
-// Bucketing of one selection (row b picked centroid c): see the file comment.
-__device__ __forceinline__ void bucket_selection(const TopkParams &p, int b, int c)
+// Bucketing of row b's K selections `sel` (shared memory; see the file comment), one
+// warp per 32 selections: each lane sets its row-mask bit and counts the cluster's
+// rows; the first selectors of their clusters then reserve their work items with one
+// atomicAdd per warp on the item count (a warp-wide prefix sum of their item counts),
+// not one per cluster on the same word.
+__device__ __forceinline__ void bucket_selections(const TopkParams &p, int b, const int32_t *sel)
 {
-    if (c < p.c_begin || c >= p.c_end) return;   // another shard's cluster
-    atomicOr(&p.rowmask[(size_t)c * p.W + (b >> 5)], 1u << (b & 31));
-    if (atomicAdd(&p.ccount[c], 1) == 0) {
-        int lo, hi;
-        if (cluster_range(p.offsets, p.V, p.S, c, &lo, &hi, p.ctrl + kCtrlError) && hi > lo) {
-            const int n = (hi - lo + p.chunk - 1) / p.chunk;
-            const uint32_t base = atomicAdd(p.ctrl + kCtrlItems, (uint32_t)n);
-            // Ascending offsets cannot overflow the list (it is sized for V / chunk + C
-            // items); overlapping ranges can, so they are reported and dropped.
-            if (base + (uint32_t)n > (uint32_t)p.items_cap) {
-                atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
-            } else {
-                for (int j = 0; j < n; ++j) p.items[base + j] = make_int2(c, j * p.chunk);
-            }
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x / kWarp;
+    for (int i0 = warp * kWarp; i0 < p.K; i0 += kTopkThreads) {
+        const int c = i0 + lane < p.K ? sel[i0 + lane] : -1;
+        int n = 0;
+        if (c >= p.c_begin && c < p.c_end) {   // else another shard's cluster (or no lane)
+            atomicOr(&p.rowmask[(size_t)c * p.W + (b >> 5)], 1u << (b & 31));
+            int lo, hi;
+            if (atomicAdd(&p.ccount[c], 1) == 0 &&
+                cluster_range(p.offsets, p.V, p.S, c, &lo, &hi, p.ctrl + kCtrlError) && hi > lo)
+                n = (hi - lo + p.chunk - 1) / p.chunk;
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
+        if (total == 0) continue;
+        uint32_t base = 0;
+        if (lane == kWarp - 1) base = atomicAdd(p.ctrl + kCtrlItems, (uint32_t)total);
+        base = __shfl_sync(0xffffffffu, base, kWarp - 1) + (uint32_t)(incl - n);
+        if (n == 0) continue;
+        // Ascending offsets cannot overflow the list (it is sized for V / chunk + C items);
+        // overlapping ranges can, so a cluster that does not fit is reported and dropped.
+        if (base + (uint32_t)n > (uint32_t)p.items_cap) {
+            atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
+        } else {
+            for (int j = 0; j < n; ++j) p.items[base + j] = make_int2(c, j * p.chunk);
         }
     }
 }
@@ -99,11 +118,9 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     unsigned long long *s_cand = reinterpret_cast<unsigned long long *>(hist);
     __shared__ int s_scan[kWarp + 1];
     __shared__ uint32_t s_digit, s_above;
-    __shared__ int s_ncand;
 
     const int b = blockIdx.x, tid = threadIdx.x;
     for (int i = tid; i < kKeyBuckets; i += kTopkThreads) hist[i] = 0u;
-    if (tid == 0) s_ncand = 0;
     __syncthreads();
     // the first selector of a cluster reads its range from the offsets table
     if (p.rowmask) prefetch_l2_table(p.offsets, (size_t)(p.C + 1) * sizeof(int32_t));
@@ -153,20 +170,27 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
     const uint32_t kbucket = s_digit;
     const int ncand = (int)s_above;
     if (ncand <= kCandCap) {
-        // compaction: one shared atomic per warp and pass (the candidates of a warp take
-        // consecutive slots), not one per candidate on a single counter
-        const int lane = tid & (kWarp - 1);
+        // compaction without atomics: each warp counts its hits over its columns (ballots),
+        // one prefix over the warps gives each warp its first slot, and a second pass
+        // writes the candidates (their order does not matter to the ranking)
+        const int lane = tid & (kWarp - 1), warp = tid / kWarp;
+        int whits = 0;
+        for (int c0 = 0; c0 < p.C; c0 += kTopkThreads) {
+            const int c = c0 + tid;
+            const bool hit = c < p.C && (keys[c] >> kKeyShift) >= kbucket;
+            whits += __popc(__ballot_sync(0xffffffffu, hit));
+        }
+        if (lane == 0) s_scan[warp] = whits;
+        __syncthreads();
+        int slot = 0;
+        for (int w = 0; w < warp; ++w) slot += s_scan[w];
         for (int c0 = 0; c0 < p.C; c0 += kTopkThreads) {
             const int c = c0 + tid;
             const uint32_t k = c < p.C ? keys[c] : 0u;
             const bool hit = c < p.C && (k >> kKeyShift) >= kbucket;
             const unsigned bal = __ballot_sync(0xffffffffu, hit);
-            if (bal) {
-                int base = 0;
-                if (lane == __ffs(bal) - 1) base = atomicAdd(&s_ncand, __popc(bal));
-                base = __shfl_sync(0xffffffffu, base, __ffs(bal) - 1);
-                if (hit) s_cand[base + __popc(bal & ((1u << lane) - 1u))] = select_key(k, c);
-            }
+            if (hit) s_cand[slot + __popc(bal & ((1u << lane) - 1u))] = select_key(k, c);
+            slot += __popc(bal);
         }
         __syncthreads();
         // rank of each candidate = candidates with a larger key; with few candidates four
@@ -187,9 +211,12 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
             if (q == 0 && rank < p.K) {
                 const int c = (int)(0xffffffffu - (uint32_t)(ki & 0xffffffffull));
                 p.topk[(size_t)b * p.K + rank] = c;
-                if (p.rowmask) bucket_selection(p, b, c);
+                sel[rank] = c;
             }
         }
+        if (p.rowmask == nullptr) return;
+        __syncthreads();
+        bucket_selections(p, b, sel);
         return;
     }
 
@@ -291,7 +318,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkParams p)
 
     if (p.rowmask == nullptr)
         return;
-    for (int i = tid; i < p.K; i += kTopkThreads) bucket_selection(p, b, sel[i]);
+    bucket_selections(p, b, sel);
 }
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s)
