@@ -420,6 +420,33 @@ def test_corrupt_offsets_set_device_error(build_lib):
     assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_OFFSETS
 
 
+def test_overlapping_offsets_overflow_the_item_list(build_lib):
+    """Cluster ranges that overlap (possible only beside an invalid range: clusters 0, 2, 4
+    and 6 below each own all of V, 1, 3, 5 and 7 are reversed) ask for 4 x 32 work items of
+    8 positions, more than the list holds (V/8 + C + 1 = 41).  The top-K drops every cluster
+    whose items do not fit instead of writing past the list, the call reports
+    MTP_DEVERR_OFFSETS, and a clean call on the same workspace runs clean."""
+    m = build_lib
+    V, H, C, K = 256, 8, 8, 8
+    t, oh, dh = _custom(m, V, H, C, K, seed=11, sizes=[32] * C)
+    off = np.array([0, V, 0, V, 0, V, 0, V, 0], dtype=np.int32)
+    dbad = m.MaskedHead(dh.centroid_w, dh.embed_w, dh.token_ordering, K, torch.from_numpy(off).cuda(),
+                        vocab_size=V)
+    h = helpers.bf16_tensor(synth.random_hidden(1, H, 12))
+    ws = dbad.workspace(1)
+    assert m.mtp_gather_plan(dbad, 1) == "cuda_core_direct"
+    tok, _ = m.mtp_masked_topk_tokens(dbad, h, workspace=ws)
+    torch.cuda.synchronize()
+    assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_OFFSETS
+    assert 0 <= int(tok.cpu()[0]) < V
+    ref = oracle.masked_topk_tokens(oh, synth.random_hidden(1, H, 12))
+    tok, _ = m.mtp_masked_topk_tokens(dh, h, workspace=ws)
+    torch.cuda.synchronize()
+    assert m.mtp_read_device_error(ws) == 0
+    if ref["score_margin"][0] > helpers.MARGIN and ref["logit_margin"][0] > helpers.MARGIN:
+        assert int(tok.cpu()[0]) == int(ref["tokens"][0])
+
+
 def test_repeat_calls_are_deterministic(build_lib):
     m = build_lib
     oh, dh = device_head(m, "uniform")
