@@ -37,6 +37,23 @@ def test_every_declared_symbol_is_exported(L):
         assert n in _lib.SIGNATURES, f"{n} has no ctypes signature in the binding"
 
 
+def test_exports_nothing_beyond_the_header(L):
+    """The library's dynamic symbols are the header's entry points; everything else is
+    hidden (built with -fvisibility=hidden), apart from the C++ standard library's own
+    template instantiations, which the toolchain exports as weak symbols."""
+    import shutil
+    import subprocess
+    from centroid_masked_sparse_gb300 import _lib
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    names = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    extra = {n for n in names - _declared() if not re.match(r"_Z(NK?)?St", n)}
+    assert not extra, sorted(extra)
+
+
 def test_status_strings_and_version(L):
     for code in range(-6, 1):
         assert L.mtp_status_string(code)
