@@ -44,6 +44,13 @@ MUTATIONS = [
      "*hi = off[c + 1];", "*hi = off[c + 1] + (c + 2 < C ? 1 : 0);"),
     ("bf16 decoded with the wrong shift",
      "uint32_t u = ((uint32_t)bits) << 16;", "uint32_t u = ((uint32_t)bits) << 15;"),
+    ("sparse pair lists a cluster's positions in reverse",
+     "        for (int64_t p = lo; p < hi; ++p) {\n            int32_t t = ordering[p];\n            tokens[j] = t;",
+     "        for (int64_t p = hi - 1; p >= lo; --p) {\n            int32_t t = ordering[p];\n            tokens[j] = t;"),
+    ("sparse pair reports ordered positions as token ids",
+     "            tokens[j] = t;\n            logits[j] =", "            tokens[j] = (int32_t)p;\n            logits[j] ="),
+    ("sparse pair reports one candidate fewer than it lists",
+     "        *n = candidate_count(sel, K, V, C, off);", "        *n = candidate_count(sel, K, V, C, off) - 1;"),
     ("centroid table read transposed",
      "scores[c] = dot_bf16(h_row, centroid_w + c * H, H);",
      "{ scores[c] = 0; for (int64_t i = 0; i < H; ++i) scores[c] += bf16_value(h_row[i]) * "
