@@ -51,6 +51,10 @@ MUTATIONS = [
      "            tokens[j] = t;\n            logits[j] =", "            tokens[j] = (int32_t)p;\n            logits[j] ="),
     ("sparse pair reports one candidate fewer than it lists",
      "        *n = candidate_count(sel, K, V, C, off);", "        *n = candidate_count(sel, K, V, C, off) - 1;"),
+    ("full-vocab scatter stores at the candidate's list index, not its token id",
+     "row[cand_tok[j]] = cand_log[j];", "row[j] = cand_log[j];"),
+    ("finite-minimum fill takes fp32's minimum instead of bf16's",
+     "? -ORC_BF16_MAX : -INFINITY;", "? -3.4028234663852886e38 : -INFINITY;"),
     ("centroid table read transposed",
      "scores[c] = dot_bf16(h_row, centroid_w + c * H, H);",
      "{ scores[c] = 0; for (int64_t i = 0; i < H; ++i) scores[c] += bf16_value(h_row[i]) * "
