@@ -55,6 +55,11 @@ MUTATIONS = [
      "row[cand_tok[j]] = cand_log[j];", "row[j] = cand_log[j];"),
     ("finite-minimum fill takes fp32's minimum instead of bf16's",
      "? -ORC_BF16_MAX : -INFINITY;", "? -3.4028234663852886e38 : -INFINITY;"),
+    ("score margin taken between the (K-1)-th and K-th picks",
+     "all[K - 1].score - all[K].score", "all[K > 1 ? K - 2 : 0].score - all[K - 1].score"),
+    ("logit margin forgets the best it displaces",
+     "                if (best_t >= 0)\n                    second = best;",
+     "                if (0)\n                    second = best;"),
     ("centroid table read transposed",
      "scores[c] = dot_bf16(h_row, centroid_w + c * H, H);",
      "{ scores[c] = 0; for (int64_t i = 0; i < H; ++i) scores[c] += bf16_value(h_row[i]) * "
