@@ -247,6 +247,42 @@ def test_select_and_score_rejects_bad_arguments(L):
     assert L.mtp_select_and_score(ctypes.byref(d), None, 0, None, None, None, 0, None) == 0
 
 
+def test_key_exchange_rejects_bad_arguments(L):
+    """The sharded head's key export and decode check their arguments on the host, in the
+    header's order, before any device work; an empty batch is a no-op."""
+    d = _desc()
+    keys = ctypes.c_void_p(0x8000)
+    tok = ctypes.c_void_p(0xA000)
+    big = 1 << 30
+    assert L.mtp_masked_topk_keys(None, FAKE, 4, keys, WS, big, None) == -1
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), None, 4, keys, WS, big, None) == -1
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, 4, None, WS, big, None) == -1
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), ctypes.c_void_p(0x7001), 4, keys, WS, big, None) == -3
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, 4, keys, None, 0, None) == -4
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, 4, keys, WS, 16, None) == -4
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, -1, keys, WS, big, None) == -2
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), FAKE, 1025, keys, WS, big, None) == -6
+    assert L.mtp_masked_topk_keys(ctypes.byref(d), None, 0, None, None, 0, None) == 0
+    assert L.mtp_decode_keys(None, 4, tok, None, None) == -1
+    assert L.mtp_decode_keys(keys, 4, None, None, None) == -1
+    assert L.mtp_decode_keys(keys, -3, tok, None, None) == -2
+    assert L.mtp_decode_keys(keys, 1025, tok, None, None) == -6
+    assert L.mtp_decode_keys(None, 0, None, None, None) == 0
+
+
+def test_noalloc_host_checks(L):
+    """The allocation-free entry point refuses, before any device work, requests whose
+    workspace would exceed its fixed 8 MiB scratch: 943 rows of the V=262144, C=2048, K=32
+    head fit, 944 do not; empty and negative batches behave as in the workspace call."""
+    d = _desc()
+    out = ctypes.c_void_p(0x8000)
+    assert L.mtp_workspace_bytes(ctypes.byref(d), 943) <= 8 << 20 < L.mtp_workspace_bytes(ctypes.byref(d), 944)
+    assert L.mtp_masked_topk_tokens_noalloc(None, FAKE, 4, out, None, None) == -1
+    assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), FAKE, 0, out, None, None) == 0
+    assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), FAKE, -1, out, None, None) == -2
+    assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), FAKE, 944, out, None, None) == -6
+
+
 def test_cluster_range_checks_and_packed_size(L):
     out = ctypes.c_void_p(0x8000)
     for b, e in ((5, 3), (-1, 4), (0, 2049)):
