@@ -60,6 +60,10 @@ MUTATIONS = [
     ("logit margin forgets the best it displaces",
      "                if (best_t >= 0)\n                    second = best;",
      "                if (0)\n                    second = best;"),
+    ("sampled dense logits read the table row of the batch row, not of the token",
+     "embed_w + tokens[i] * ld_embed", "embed_w + rows[i] * ld_embed"),
+    ("permutation check accepts repeated token ids",
+     "if (t < 0 || t >= V || seen[t])", "if (t < 0 || t >= V)"),
     ("centroid table read transposed",
      "scores[c] = dot_bf16(h_row, centroid_w + c * H, H);",
      "{ scores[c] = 0; for (int64_t i = 0; i < H; ++i) scores[c] += bf16_value(h_row[i]) * "
@@ -79,7 +83,8 @@ def _pin_calls():
               ("variable", pins.test_variable_cluster_candidate_counts),
               ("round_bf16", pins.test_round_bf16_values),
               ("flags", pins.test_fidelity_flags_hand_example),
-              ("softcap", pins.test_dense_softcap_hand_example)]
+              ("softcap", pins.test_dense_softcap_hand_example),
+              ("permutation", pins.test_permutation_check)]
     return calls
 
 
