@@ -222,12 +222,14 @@ class Timer:
             e.record()
         return evs
 
-    def run(self, fn, steps, warmup, kernel=None, ws=1, extra_kernels=()):
+    def run(self, fn, steps, warmup, kernel=None, ws=1, extra_kernels=(), flush=True):
         """Per-step device times (ms) of fn(i) and of library kernels (events the library
-        records around each launch on the call's stream)."""
+        records around each launch on the call's stream).  flush=False: L2 keeps what the
+        previous call left (the warm figure)."""
         torch, m = self.torch, self.m
         for i in range(warmup):
-            self.flush_l2()
+            if flush:
+                self.flush_l2()
             fn(i)
         names = ([kernel] if kernel else []) + [k for k in extra_kernels if k != kernel]
         call_ev = self.events(2 * steps)
@@ -242,7 +244,8 @@ class Timer:
         try:
             t0 = time.time()
             for i in range(steps):
-                self.flush_l2()
+                if flush:
+                    self.flush_l2()
                 for k in names:
                     m.mtp_profile_events(k, kev[k][2 * i], kev[k][2 * i + 1])
                 call_ev[2 * i].record()
@@ -285,8 +288,14 @@ def measure_masked(ctx, t, dh, name, B, steps, warmup, scatter=False, rot=4, row
     # the headline: whole calls, no library events between the kernels (events recorded
     # between launches would also stop the dependent-launch overlap)
     call, _, t0, t1 = timer.run(fn, steps, warmup, ws=ctx["ws"])
-    # the per-kernel breakdown, in a separate shorter loop with the library's events
-    extra = ("projection", "topk") + (("fill",) if scatter else ())
+    # secondary: the same calls back to back without the flush (the batch's rows and the
+    # tables' hot lines may still be in L2 from the previous call; at small batches the
+    # whole working set fits)
+    warm, _, _, _ = timer.run(fn, max(20, steps // 4), 2, ws=ctx["ws"], flush=False)
+    # the per-kernel breakdown, in a separate shorter loop with the library's events (the
+    # fused small-batch kernel selects the top-K itself: no top-K launch then)
+    fused = m.mtp_gather_plan(dh, B) == "fused"
+    extra = ("projection",) + (() if fused else ("topk",)) + (("fill",) if scatter else ())
     _, kern, _, _ = timer.run(fn, max(20, steps // 4), 2, kernel="gather_score", ws=ctx["ws"],
                               extra_kernels=extra)
     breakdown = {k: round(v * 1e3, 2) for k, v in timer.last_breakdown.items()}
@@ -301,8 +310,9 @@ def measure_masked(ctx, t, dh, name, B, steps, warmup, scatter=False, rot=4, row
     call_ms = float(np.mean(call))
     kern_ms = float(np.mean(kern))
     return dict(call_ms=call_ms, kernel_ms=kern_ms, t0=t0, t1=t1, bytes=bm,
-                launches_per_call=4 if scatter else 3, kernels_us=breakdown,
+                launches_per_call=(2 if fused else 3) + (1 if scatter else 0), kernels_us=breakdown,
                 max_call_us=round(float(np.max(call)) * 1e3, 2),
+                warm_l2_us_per_call=round(float(np.mean(warm)) * 1e3, 2),
                 median_call_us=round(float(np.median(call)) * 1e3, 2), device_error=dev_err)
 
 
@@ -419,6 +429,17 @@ def cpu_baseline(t, name, B, budget_s=10.0, threads=None):
                 us_per_call=dt / passes * 1e6)
 
 
+def run_config(args, w, B, ws):
+    """The `config` object of the JSON line: the same for the library's arm and the
+    reference arm on the same workload."""
+    return {"workload": workload_label(w, B), "finish": "sparse argmax",
+            "embedding_layout": ("packed tiles (built once at load, outside the timing)"
+                                 if args.layout == "packed" else "token order"),
+            "batch_per_gpu": B, "parallelism": "replicas" if ws > 1 else "single",
+            "l2": "flushed before every timed call, outside the events: 256 MB written, "
+                  "then 512 MB read so the written lines are evicted before the call"}
+
+
 def workload_label(w, B):
     layout = "lognormal clusters" if w.variable_clusters else f"{w.centroids}x{w.vocab // w.centroids} clusters"
     return (f"{w.name}: V={w.vocab} ({layout}), H={w.hidden}, C={w.centroids}, K={w.top_k}, B={B}")
@@ -472,7 +493,7 @@ def gpu_main(args):
     kern_s = res["kernel_ms"] * 1e-3
     achieved = res["bytes"]["gather"] / kern_s / 1e9
     plan = m.mtp_gather_plan(dh, B)
-    kfile, kname = {"tensor_core": ("gather_tc", "k_gather_tc"),
+    kfile, kname = {"tensor_core": ("gather_tc", "k_gather_tc"), "fused": ("select_gather", "k_select_gather"),
                     "cuda_core_direct": (None, "k_gather_direct")}.get(plan, ("score", "k_gather_score"))
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": hbm, "peak_source": f"{hbm_src} HBM copy GB/s", "unit": "GB/s",
@@ -485,12 +506,7 @@ def gpu_main(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(call_ms, 5),
            "us_per_call": round(call_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": workload_label(w, B), "finish": "sparse argmax",
-                      "embedding_layout": ("packed tiles (built once at load, outside the timing)"
-                                           if args.layout == "packed" else "token order"),
-                      "batch_per_gpu": B, "parallelism": "replicas" if ws > 1 else "single",
-                      "l2": "flushed before every timed call, outside the events: 256 MB written, "
-                            "then 512 MB read so the written lines are evicted before the call"},
+           "config": run_config(args, w, B, ws),
            "call_roofline": {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
                              "frac": round(call_gbs / hbm, 4),
                              "algorithmic_bytes": int(res["bytes"]["call"]),
@@ -498,6 +514,7 @@ def gpu_main(args):
            "roofline": roofline,
            "kernels_us": res["kernels_us"],
            "max_call_us": res["max_call_us"], "median_call_us": res["median_call_us"],
+           "warm_l2_us_per_call": res["warm_l2_us_per_call"],
            "device_error": res["device_error"],
            "gpu_launches": res["launches_per_call"] * args.steps,
            "clocks": clocks}
@@ -531,6 +548,7 @@ def gpu_main(args):
                              "call_gbs": round(cg, 1), "call_frac": round(cg / hbm, 4),
                              "unique_clusters": r["bytes"]["unique_clusters"],
                              "kernels_us": r["kernels_us"], "max_call_us": r["max_call_us"],
+                             "warm_l2_us_per_call": r["warm_l2_us_per_call"],
                              "device_error": r["device_error"]}
         out["sweep"] = sweep
         if args.layout == "packed":
@@ -545,6 +563,9 @@ def gpu_main(args):
         if not args.no_extra:
             out["other_workloads"] = other_workloads(ctx, args, hbm)
         out["cpu_baseline"] = cpu_baseline(t, name, B, budget_s=args.cpu_seconds)
+        one = cpu_baseline(t, name, B, budget_s=max(2.0, args.cpu_seconds / 2), threads=1)
+        out["cpu_baseline"]["one_thread"] = {"value": one["value"], "unit": UNIT, "cores": 1,
+                                             "us_per_call": one["us_per_call"], "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
@@ -633,10 +654,7 @@ def reference_main(args):
            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": workload_label(w, B), "finish": "sparse argmax",
-                      "embedding_layout": ("packed tiles (built once at load, outside the timing)"
-                                           if args.layout == "packed" else "token order"),
-                      "batch_per_gpu": B},
+           "config": run_config(args, w, B, ws),
            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads,
                             "kind": "oracle",
                             "sample": f"each step: one {B}-row batch of the '{name}' workload, "
@@ -646,7 +664,7 @@ def reference_main(args):
     print(json.dumps(out), flush=True)
 
 
-def parse():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1500)
@@ -662,13 +680,28 @@ def parse():
                          "the timing) or the token-order table alone")
     ap.add_argument("--finish", default="argmax", choices=["argmax", "scatter", "dense"],
                     help="profiling aid: time only this finish on the workload's tables")
-    a = ap.parse_args()
+    a = ap.parse_args(argv)
     a.warmup = max(3, a.warmup)
     return a
 
 
+def spawn_ranks(n):
+    """`--gpus N` (N > 1) outside a launcher: start N ranks of this same command line on
+    this node with torch.distributed.run (one process per GPU, rendezvous on 127.0.0.1)
+    and return their exit status; rank 0 prints the JSON line."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 if __name__ == "__main__":
-    args = parse()
+    args = parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_ranks(args.gpus))
     if args.impl == "reference":
         reference_main(args)
     else:

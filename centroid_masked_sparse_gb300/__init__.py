@@ -17,16 +17,16 @@ from __future__ import annotations
 
 import ctypes
 
-from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TOKEN_RANGE, MTP_MAX_BATCH,
+from ._lib import (KERNEL_IDS, MTP_DEVERR_OFFSETS, MTP_DEVERR_TIMEOUT, MTP_DEVERR_TOKEN_RANGE, MTP_MAX_BATCH,
                    MtpError, MtpHeadDesc, check, lib)
 
 __all__ = ["MaskedHead", "MtpError", "CapturedCalls", "MTP_FINISH_ARGMAX", "MTP_FINISH_SCATTER", "MTP_FINISH_PAIR",
            "MTP_FLAG_FILL_FINFO_MIN", "MTP_FLAG_BF16_SCORES", "MTP_FLAG_BF16_LOGITS", "MTP_FLAG_HOST_HIDDEN", "mtp_workspace_bytes", "mtp_centroid_scores",
            "mtp_masked_topk_tokens", "mtp_masked_scatter_logits", "mtp_select_and_score", "mtp_dense_lm_head",
-           "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan",
+           "mtp_read_device_error", "mtp_profile_events", "mtp_packed_embeddings_bytes", "mtp_pack_embeddings", "mtp_gather_plan", "mtp_force_gather", "mtp_wait_test", "GATHER_KINDS",
            "mtp_masked_topk_keys", "mtp_decode_keys", "combine_keys", "sharded_topk_tokens",
            "MTP_DEVERR_TOKEN_RANGE",
-           "MTP_DEVERR_OFFSETS", "lib"]
+           "MTP_DEVERR_OFFSETS", "MTP_DEVERR_TIMEOUT", "lib"]
 
 
 def _torch():
@@ -274,13 +274,28 @@ def mtp_pack_embeddings(head, out, workspace=None, stream=None):
     return out
 
 
+GATHER_KINDS = {0: "cuda_core", 1: "tensor_core", 2: "cuda_core_direct", 3: "fused"}
+
+
 def mtp_gather_plan(head, batch: int) -> str:
-    """'tensor_core', 'cuda_core' or 'cuda_core_direct': the gather kernel a masked call
-    (argmax or scatter finish) of this batch runs."""
+    """'fused', 'cuda_core_direct', 'tensor_core' or 'cuda_core': the gather kernel a
+    masked call (argmax or scatter finish) of this batch runs."""
     r = int(lib().mtp_gather_plan(ctypes.byref(head.desc), int(batch)))
     if r < 0:
         check(r, "mtp_gather_plan")
-    return {1: "tensor_core", 2: "cuda_core_direct"}.get(r, "cuda_core")
+    return GATHER_KINDS[r]
+
+
+def mtp_force_gather(kind):
+    """Testing and profiling aid: run gather `kind` (a name of GATHER_KINDS, or None for
+    the library's own choice) in every masked call of this process."""
+    code = -1 if kind is None else {v: k for k, v in GATHER_KINDS.items()}[kind]
+    check(lib().mtp_force_gather(code), "mtp_force_gather")
+
+
+def mtp_wait_test(limit_ns: int = 0, stall: bool = False):
+    """Testing aid: the pipelined gather's wait limit (0 = the default 2 s) and its stall."""
+    check(lib().mtp_wait_test(int(limit_ns), 1 if stall else 0), "mtp_wait_test")
 
 
 MTP_FINISH_ARGMAX, MTP_FINISH_SCATTER, MTP_FINISH_PAIR = 0, 1, 2
@@ -415,7 +430,14 @@ def combine_keys(keys, group=None):
     """The shards' exchange step: an elementwise max of the int64 keys over the ranks of
     `group` (in place).  Nothing to do without an initialised process group."""
     import torch.distributed as dist
-    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+    if not (dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1):
+        return keys
+    if keys.is_cuda and dist.get_backend(group) == "gloo":
+        # gloo reduces host tensors: the B x 8 bytes go through host memory
+        host = keys.cpu()
+        dist.all_reduce(host, op=dist.ReduceOp.MAX, group=group)
+        keys.copy_(host)
+    else:
         dist.all_reduce(keys, op=dist.ReduceOp.MAX, group=group)
     return keys
 

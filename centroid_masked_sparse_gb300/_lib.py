@@ -16,6 +16,7 @@ STATUS_NAMES = {0: "MTP_OK", -1: "MTP_ERR_NULL", -2: "MTP_ERR_SHAPE", -3: "MTP_E
                 -4: "MTP_ERR_WORKSPACE", -5: "MTP_ERR_CUDA", -6: "MTP_ERR_UNSUPPORTED"}
 MTP_DEVERR_TOKEN_RANGE = 0x1
 MTP_DEVERR_OFFSETS = 0x2
+MTP_DEVERR_TIMEOUT = 0x4
 MTP_MAX_HIDDEN = 4096
 MTP_MAX_CENTROIDS = 16384
 MTP_MAX_BATCH = 1024
@@ -57,6 +58,7 @@ SIGNATURES = {
     "mtp_masked_scatter_logits": (_i32, [_DP, _p, _i32, _p, _p, _sz, _p]),
     "mtp_dense_lm_head": (_i32, [_DP, _p, _i32, _p, _p, _p, _p, _sz, _p]),
     "mtp_masked_topk_tokens_noalloc": (_i32, [_DP, _p, _i32, _p, _p, _p]),
+    "mtp_noalloc_read_device_error": (_i32, [_i32, ctypes.POINTER(ctypes.c_uint32), _p]),
     "mtp_packed_embeddings_bytes": (ctypes.c_size_t, [_DP]),
     "mtp_pack_embeddings": (_i32, [_DP, _p, ctypes.c_size_t, _p, _p]),
     "mtp_gather_plan": (_i32, [_DP, _i32]),
@@ -71,6 +73,8 @@ SIGNATURES = {
     "mtp_status_string": (ctypes.c_char_p, [_i32]),
     "mtp_version": (_i32, []),
     "mtp_profile_events": (_i32, [_i32, _p, _p]),
+    "mtp_force_gather": (_i32, [_i32]),
+    "mtp_wait_test": (_i32, [ctypes.c_int64, _i32]),
 }
 
 _lib = None

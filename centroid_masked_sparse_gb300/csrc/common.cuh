@@ -151,6 +151,23 @@ __device__ __forceinline__ void decode_argmax_key(unsigned long long k, int32_t 
     }
 }
 
+// Fire-and-forget 64-bit max at device scope (no ordering of its own; a later release
+// operation of the same thread orders it).
+__device__ __forceinline__ void red_max_u64(unsigned long long *addr, unsigned long long v)
+{
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
+// atomicAdd with acquire-release semantics at device scope: the thread's earlier writes
+// (and reductions) are visible to whoever acquires a later value of *addr, and this
+// thread sees what the earlier adders released.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *addr, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // Ordered positions [lo, hi) of centroid c; false (and the error bit) when the
 // offsets are malformed.
 __device__ __forceinline__ bool cluster_range(const int32_t *offsets, int32_t V, int32_t S, int c,
@@ -236,6 +253,14 @@ struct GatherParams {
     int step;                       // slots the producer warp publishes per batch (<= 32, <= ring)
     int consumer_warps;             // 8 or 16
     int ctas_per_sm;                // gather CTAs per SM (1 or 2)
+    // the fused small-batch kernel selects each row's top-K itself
+    const float *scores;            // [B, C] centroid scores
+    int bf16_scores;                // select on the scores rounded to bf16
+    int c_begin, c_end;             // clusters this shard gathers
+    // bounded waits of the pipelined gather: wall-clock limit, and the wait test (its
+    // first h-buffer wait waits for a barrier phase that nothing completes)
+    unsigned long long wait_ns;
+    int stall_test;
 };
 
 }  // namespace mtp

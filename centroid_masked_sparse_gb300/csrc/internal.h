@@ -21,6 +21,29 @@ int blocks_per_sm(const void *kernel, int block, size_t smem);
 // and device; done for any nonzero size, since static shared memory shares the limit).
 cudaError_t allow_smem(const void *kernel, size_t smem);
 
+// Host-side argument checks of the sparse-argmax call (descriptor, batch, pointers,
+// alignment), shared by its workspace and allocation-free entry points.
+mtp_status check_topk_call(const mtp_head_desc *desc, const void *hidden, int32_t batch, const int32_t *out_tokens);
+
+// Makes `dev` current for the rest of a call and gives the calling thread back its
+// own current device when the call returns (ok == false: either step failed).
+struct DeviceScope {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceScope(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = prev == dev || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceScope()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+    DeviceScope(const DeviceScope &) = delete;
+    DeviceScope &operator=(const DeviceScope &) = delete;
+};
+
 // Launch with programmatic stream serialization: the kernel may start while the
 // previous kernel on the stream is still running and must execute
 // griddepcontrol.wait before it reads that kernel's results.
@@ -60,6 +83,15 @@ cudaError_t launch_gather_tc(const GatherParams &p, bool scatter, cudaStream_t s
 constexpr int kTcGatherChunk = 128;
 // Expected rows per selected cluster (B*K/C) from which the tensor-core gather is used.
 constexpr int kTcGatherMinReuse = 4;
+// Fused top-K + gather + finish for small batches (select_gather.cu): every CTA
+// selects its row's top-K from p.scores itself; no buckets or work items.  K at most
+// kSelectGatherMaxK; no sparse pair.
+cudaError_t launch_select_gather(const GatherParams &p, bool scatter, cudaStream_t s);
+constexpr int kSelectGatherMaxK = 1024;
+// Wall-clock limit of a bounded mbarrier wait in the pipelined gather (mtp_wait_test
+// can change it for a test).
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+constexpr int kSelectGatherCtasPerSm = 2;
 cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s);
 // Copy `bytes` (a multiple of 16, both ends 16-byte aligned) from memory the device can
 // read (pinned host memory included) to device memory with one kernel.

@@ -12,6 +12,7 @@
 struct mtp_graph {
     cudaGraph_t graph;
     cudaGraphExec_t exec;
+    int device;   // the descriptor's device, current while the graph is launched
 };
 
 namespace {
@@ -44,6 +45,8 @@ mtp_status mtp_graph_capture(const mtp_head_desc *desc, int32_t finish, const vo
     // (kernel attributes, occupancy queries, tensor-map encoder lookup) outside the capture
     mtp_status st = run_call(desc, finish, hidden, batch, out0, out1, workspace, workspace_bytes, stream);
     if (st != MTP_OK) return st;
+    const mtp::DeviceScope dev(desc->device);
+    if (!dev.ok) return MTP_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return MTP_ERR_CUDA;
     st = run_call(desc, finish, hidden, batch, out0, out1, workspace, workspace_bytes, stream);
@@ -60,7 +63,7 @@ mtp_status mtp_graph_capture(const mtp_head_desc *desc, int32_t finish, const vo
         cudaGetLastError();
         return MTP_ERR_CUDA;
     }
-    mtp_graph *h = new (std::nothrow) mtp_graph{g, x};
+    mtp_graph *h = new (std::nothrow) mtp_graph{g, x, desc->device};
     if (!h) {
         cudaGraphExecDestroy(x);
         cudaGraphDestroy(g);
@@ -73,6 +76,8 @@ mtp_status mtp_graph_capture(const mtp_head_desc *desc, int32_t finish, const vo
 mtp_status mtp_graph_launch(const mtp_graph *graph, void *stream)
 {
     if (!graph) return MTP_ERR_NULL;
+    const mtp::DeviceScope dev(graph->device);
+    if (!dev.ok) return MTP_ERR_CUDA;
     return cudaGraphLaunch(graph->exec, (cudaStream_t)stream) == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
 }
 

@@ -2,6 +2,7 @@
 // layout and the launch sequence of each call.  Declarations and the contract
 // of every entry point are in include/mtp_head.h.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <unordered_map>
@@ -190,14 +191,6 @@ mtp_status check_batch(int32_t B)
     return MTP_OK;
 }
 
-mtp_status use_device(int dev)
-{
-    int cur = -1;
-    if (cudaGetDevice(&cur) != cudaSuccess) return MTP_ERR_CUDA;
-    if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return MTP_ERR_CUDA;
-    return MTP_OK;
-}
-
 int proj_rows_per_group(int B, int H)
 {
     int r = 49152 / (2 * H);
@@ -361,20 +354,56 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
     return false;
 }
 
-enum GatherKind { kGatherPipelined = 0, kGatherTensorCore = 1, kGatherDirect = 2 };
+enum GatherKind { kGatherNone = -1, kGatherPipelined = 0, kGatherTensorCore = 1, kGatherDirect = 2, kGatherFused = 3 };
 
-// The gather a masked call runs.  Small batches take the direct CUDA-core gather
-// (each warp loads candidate rows straight into registers; no producer, ring or
-// hand-off, so its latency chain is short): every call of at most 8 rows, and up
-// to 12 rows where the tensor-core gather would not run.  Measured on GB300 against
-// the alternatives: uniform clusters B=12 ~46 vs ~47.5 us (pipelined), B=16 ~56.5 vs
-// ~54.5 us (tensor cores); H=256 B=4 26 vs 30 us and B=8 30 vs 31 us (tensor cores),
-// B=16 38.5 vs 32.4 us.  The sparse pair keeps the other kernels.
+// Testing and profiling controls (mtp_force_gather, mtp_wait_test): process-wide.
+std::atomic<int> g_force_kind{-1};
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_stall_test{0};
+
+// Batches that run the fused top-K + gather kernel (select_gather.cu) behind the
+// projection instead of the top-K kernel and a gather.
+constexpr int kFusedMaxBatch = 8;
+
+// Whether a gather kernel can run a masked call of this shape.
+bool gather_can_run(const mtp_head_desc *d, int B, bool sparse, GatherKind k)
+{
+    switch (k) {
+    case kGatherPipelined:
+    case kGatherTensorCore: return true;
+    case kGatherDirect: return !sparse && B <= 32 && (size_t)B * d->hidden_size * 2 <= 200u * 1024u;
+    case kGatherFused: return !sparse && d->top_k <= kSelectGatherMaxK;
+    default: return false;
+    }
+}
+
+// The gather a masked call runs.  Batches of at most kFusedMaxBatch rows take the
+// fused kernel, which selects each row's top-K in the gather CTAs themselves.  The
+// direct CUDA-core gather (each warp loads candidate rows straight into registers; no
+// producer, ring or hand-off, so its latency chain is short) takes up to 12 rows
+// where the tensor-core gather would not run.  Measured on GB300 against the
+// alternatives: uniform clusters B=12 ~46 vs ~47.5 us (pipelined), B=16 ~56.5 vs
+// ~54.5 us (tensor cores); H=256 B=16 38.5 vs 32.4 us (tensor cores).  The sparse
+// pair keeps the pipelined and tensor-core gathers.  A kind forced by
+// mtp_force_gather that cannot run the call gives kGatherNone.
 GatherKind gather_kind(const mtp_head_desc *d, int B, bool sparse, int *chunk)
 {
-    const bool tc = tc_gather_plan(d, B, chunk);
-    if (!sparse && (B <= 8 || (!tc && B <= 12))) return kGatherDirect;
-    return tc ? kGatherTensorCore : kGatherPipelined;
+    int tc_chunk = 0;
+    const bool tc = tc_gather_plan(d, B, &tc_chunk);
+    const int forced = g_force_kind.load(std::memory_order_relaxed);
+    GatherKind k;
+    if (forced >= 0) {
+        k = (GatherKind)forced;
+        if (!gather_can_run(d, B, sparse, k)) return kGatherNone;
+    } else if (!sparse && B <= kFusedMaxBatch && gather_can_run(d, B, sparse, kGatherFused)) {
+        k = kGatherFused;
+    } else if (!sparse && !tc && B <= 12) {
+        k = kGatherDirect;
+    } else {
+        k = tc ? kGatherTensorCore : kGatherPipelined;
+    }
+    *chunk = k == kGatherTensorCore ? (tc ? tc_chunk : kTcGatherChunk) : choose_chunk(d, B);
+    return k;
 }
 
 // The masked calls.  Finishes: the sparse argmax (out_tokens), the full-vocabulary
@@ -387,8 +416,12 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     const Layout L = layout_for(d, B);
     if (!workspace || ws_bytes < L.total) return MTP_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MTP_ERR_ALIGN;
-    mtp_status st = use_device(d->device);
-    if (st != MTP_OK) return st;
+    int chunk = 0;
+    const GatherKind kind = gather_kind(d, B, sparse, &chunk);
+    if (kind == kGatherNone) return MTP_ERR_UNSUPPORTED;
+    const DeviceScope dev(d->device);
+    if (!dev.ok) return MTP_ERR_CUDA;
+    mtp_status st = MTP_OK;
     char *ws = (char *)workspace;
     if ((st = stage_hidden(d, &hidden, B, ws, L, s)) != MTP_OK) return st;
     if (out_logits && !sparse) {
@@ -397,14 +430,14 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
         st = cuda_status(launch_fill(out_logits, (size_t)B * d->vocab_size, fill, s));
         if (st != MTP_OK) return st;
     }
-    int chunk = 0;
-    const GatherKind kind = gather_kind(d, B, sparse, &chunk);
     const bool tc_gather = kind == kGatherTensorCore;
+    const bool fused = kind == kGatherFused;
     // the projection starts behind the staging kernel (programmatic launch) when it is the
-    // next kernel; behind the scatter's fill it is ordered by the fill's own launch
+    // next kernel; behind the scatter's fill it is ordered by the fill's own launch.  The
+    // fused kernel selects the top-K itself, so only the projection runs here then.
     const bool fill = out_logits && !sparse;
-    st = run_select(d, hidden, B, (float *)(ws + L.scores), (int32_t *)(ws + L.topk), ws, &L, chunk, s, fill,
-                    (d->flags & MTP_FLAG_HOST_HIDDEN) && !fill);
+    st = run_select(d, hidden, B, (float *)(ws + L.scores), fused ? nullptr : (int32_t *)(ws + L.topk), ws, &L,
+                    chunk, s, fill, (d->flags & MTP_FLAG_HOST_HIDDEN) && !fill);
     if (st != MTP_OK) return st;
 
     GatherParams gp{};
@@ -439,7 +472,13 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
     gp.W = L.W;
     gp.C = d->num_centroids;
     gp.chunk = chunk;
+    gp.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    gp.stall_test = g_stall_test.load(std::memory_order_relaxed);
+    gp.scores = (const float *)(ws + L.scores);
+    gp.bf16_scores = (d->flags & MTP_FLAG_BF16_SCORES) ? 1 : 0;
+    cluster_span(d, &gp.c_begin, &gp.c_end);
     Prof pr(MTP_KERNEL_GATHER_SCORE, s);
+    if (fused) return cuda_status(launch_select_gather(gp, out_logits != nullptr, s));
     if (tc_gather) return cuda_status(launch_gather_tc(gp, out_logits != nullptr, s));
     if (kind == kGatherDirect) return cuda_status(launch_gather_direct(gp, out_logits != nullptr, s));
     gather_geometry(gp);
@@ -447,6 +486,21 @@ mtp_status run_masked(const mtp_head_desc *d, const void *hidden, int B, int32_t
 }
 
 }  // namespace
+
+namespace mtp {
+
+mtp_status check_topk_call(const mtp_head_desc *desc, const void *hidden, int32_t batch, const int32_t *out_tokens)
+{
+    mtp_status st = check_desc(desc, true, true, true);
+    if (st != MTP_OK) return st;
+    if ((st = check_batch(batch)) != MTP_OK) return st;
+    if (batch == 0) return MTP_OK;
+    if (!hidden || !out_tokens) return MTP_ERR_NULL;
+    if (!aligned16(hidden)) return MTP_ERR_ALIGN;
+    return MTP_OK;
+}
+
+}  // namespace mtp
 
 extern "C" {
 
@@ -469,7 +523,8 @@ mtp_status mtp_centroid_scores(const mtp_head_desc *desc, const void *hidden, in
     if (desc->flags & MTP_FLAG_HOST_HIDDEN) return MTP_ERR_UNSUPPORTED;   // no workspace to stage into
     if (!hidden || !scores) return MTP_ERR_NULL;
     if (!aligned16(hidden)) return MTP_ERR_ALIGN;
-    if ((st = use_device(desc->device)) != MTP_OK) return st;
+    const DeviceScope dev(desc->device);
+    if (!dev.ok) return MTP_ERR_CUDA;
     return run_select(desc, hidden, batch, scores, topk_idx, nullptr, nullptr, kMinChunk,
                       (cudaStream_t)stream);
 }
@@ -478,12 +533,8 @@ mtp_status mtp_masked_topk_tokens(const mtp_head_desc *desc, const void *hidden,
                                   int32_t *out_tokens, float *out_max, void *workspace,
                                   size_t workspace_bytes, void *stream)
 {
-    mtp_status st = check_desc(desc, true, true, true);
-    if (st != MTP_OK) return st;
-    if ((st = check_batch(batch)) != MTP_OK) return st;
-    if (batch == 0) return MTP_OK;
-    if (!hidden || !out_tokens) return MTP_ERR_NULL;
-    if (!aligned16(hidden)) return MTP_ERR_ALIGN;
+    const mtp_status st = mtp::check_topk_call(desc, hidden, batch, out_tokens);
+    if (st != MTP_OK || batch == 0) return st;
     return run_masked(desc, hidden, batch, out_tokens, out_max, nullptr, nullptr, false, workspace, workspace_bytes,
                       (cudaStream_t)stream);
 }
@@ -543,7 +594,8 @@ mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidden, int3
         if (!ws || workspace_bytes < need) return MTP_ERR_WORKSPACE;
         if (!aligned16(ws)) return MTP_ERR_ALIGN;
     }
-    if ((st = use_device(desc->device)) != MTP_OK) return st;
+    const DeviceScope dev(desc->device);
+    if (!dev.ok) return MTP_ERR_CUDA;
     if (out_tokens) {
         st = cuda_status(cudaMemsetAsync(ws, 0, L.keys + (size_t)batch * sizeof(unsigned long long), s));
         if (st != MTP_OK) return st;
@@ -602,8 +654,8 @@ mtp_status mtp_pack_embeddings(const mtp_head_desc *desc, void *packed, size_t p
     const char *src = (const char *)desc->embed_w, *dst = (const char *)packed;
     const size_t src_bytes = (size_t)desc->vocab_size * desc->ld_embed * 2;
     if (src < dst + need && dst < src + src_bytes) return MTP_ERR_SHAPE;   // overlapping tables
-    st = use_device(desc->device);
-    if (st != MTP_OK) return st;
+    const DeviceScope dev(desc->device);
+    if (!dev.ok) return MTP_ERR_CUDA;
     return cuda_status(launch_pack_embeddings((const uint16_t *)desc->embed_w, desc->ld_embed,
                                               desc->token_ordering, desc->cluster_offsets, desc->vocab_size,
                                               desc->hidden_size, desc->num_centroids, c0, c1, (uint8_t *)packed,
@@ -623,6 +675,8 @@ mtp_status mtp_masked_topk_keys(const mtp_head_desc *desc, const void *hidden, i
     // the call's decoded tokens go to the scores region, which nothing reads after the
     // top-K; the keys it leaves in the workspace are exported
     const Layout L = layout_for(desc, batch);
+    const DeviceScope dev(desc->device);
+    if (!dev.ok) return MTP_ERR_CUDA;
     char *ws = (char *)workspace;
     st = run_masked(desc, hidden, batch, (int32_t *)(ws + L.scores), nullptr, nullptr, nullptr, false, workspace,
                     workspace_bytes, (cudaStream_t)stream);
@@ -648,7 +702,23 @@ int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch)
     if (st != MTP_OK) return st;
     if (batch == 0) return 0;
     int chunk = 0;
-    return (int32_t)gather_kind(desc, batch, false, &chunk);
+    const GatherKind k = gather_kind(desc, batch, false, &chunk);
+    return k == kGatherNone ? (int32_t)MTP_ERR_UNSUPPORTED : (int32_t)k;
+}
+
+mtp_status mtp_force_gather(int32_t kind)
+{
+    if (kind < -1 || kind > kGatherFused) return MTP_ERR_SHAPE;
+    g_force_kind.store(kind);
+    return MTP_OK;
+}
+
+mtp_status mtp_wait_test(int64_t limit_ns, int32_t stall)
+{
+    if (limit_ns < 0) return MTP_ERR_SHAPE;
+    g_wait_ns.store(limit_ns == 0 ? kDefaultWaitNs : (unsigned long long)limit_ns);
+    g_stall_test.store(stall != 0 ? 1 : 0);
+    return MTP_OK;
 }
 
 mtp_status mtp_read_device_error(const void *workspace, uint32_t *host_word, void *stream)

@@ -14,7 +14,9 @@
 // not a device address, so its device address is looked up once per device
 // with cudaGetSymbolAddress (with that device current) and cached.  The call
 // then runs the same kernels as mtp_masked_topk_tokens with that address as
-// the workspace.  Nothing here allocates or frees memory.
+// the workspace, whose first word is the device error word of the last call
+// (mtp_noalloc_read_device_error reads it).  Nothing here allocates or frees
+// memory.
 #include <mutex>
 
 #include "internal.h"
@@ -28,14 +30,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[MTP_NOALLOC_SCR
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on `dev` (made current), looked up on the
-// first call for that device.
+// Device address of g_noalloc_scratch on `dev` (current while it is looked up, on the
+// first call for that device).
 mtp_status scratch_address(int dev, void **addr)
 {
     if (dev < 0 || dev >= kMaxDevices) return MTP_ERR_SHAPE;
-    int cur = -1;
-    if (cudaGetDevice(&cur) != cudaSuccess) return MTP_ERR_CUDA;
-    if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return MTP_ERR_CUDA;
+    const mtp::DeviceScope scope(dev);
+    if (!scope.ok) return MTP_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_addr[dev]) {
         void *p = nullptr;
@@ -53,16 +54,27 @@ extern "C" MTP_API mtp_status mtp_masked_topk_tokens_noalloc(const mtp_head_desc
                                                              int32_t *out_tokens, float *out_max,
                                                              void *stream)
 {
-    if (!desc) return MTP_ERR_NULL;
-    const size_t need = batch > 0 ? mtp_workspace_bytes(desc, batch) : 0;
-    if (batch <= 0 || need == 0) {
-        // empty batch, or sizes the regular entry point rejects: let it return the status
-        return mtp_masked_topk_tokens(desc, hidden, batch, out_tokens, out_max, nullptr, 0, stream);
-    }
+    // the same checks, in the same order, as the workspace entry point; only then the
+    // size limit and the scratch address
+    const mtp_status st = mtp::check_topk_call(desc, hidden, batch, out_tokens);
+    if (st != MTP_OK || batch == 0) return st;
+    const size_t need = mtp_workspace_bytes(desc, batch);
+    if (need == 0) return MTP_ERR_SHAPE;
     if (need > (size_t)MTP_NOALLOC_SCRATCH_BYTES) return MTP_ERR_UNSUPPORTED;
     void *scratch = nullptr;
-    const mtp_status st = scratch_address(desc->device, &scratch);
-    if (st != MTP_OK) return st;
+    const mtp_status sa = scratch_address(desc->device, &scratch);
+    if (sa != MTP_OK) return sa;
     return mtp_masked_topk_tokens(desc, hidden, batch, out_tokens, out_max, scratch,
                                   (size_t)MTP_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" MTP_API mtp_status mtp_noalloc_read_device_error(int32_t device, uint32_t *host_word, void *stream)
+{
+    if (!host_word) return MTP_ERR_NULL;
+    void *scratch = nullptr;
+    const mtp_status st = scratch_address(device, &scratch);
+    if (st != MTP_OK) return st;
+    const mtp::DeviceScope scope(device);
+    if (!scope.ok) return MTP_ERR_CUDA;
+    return mtp_read_device_error(scratch, host_word, stream);
 }

@@ -54,7 +54,6 @@ namespace {
 
 constexpr int kHBuffers = 4;
 constexpr int kMaxRowGroup = 8;
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kTokDone = -2;
 
 // Sites of a wait that gave up, recorded once per call for diagnosis.
@@ -221,7 +220,10 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
             const uint32_t hpar = (huse / kHBuffers) & 1u;
             int ok = 1;
             if (lane == 0) {
-                ok = mbar_wait(sm.hempty0 + 8u * hb, hpar ^ 1u, kWaitNs);
+                // (the wait test makes the first use wait for the phase that nothing
+                // completes: no copy has been issued yet, so the CTA leaves clean)
+                const uint32_t stall = (p.stall_test && huse == 0u) ? 1u : 0u;
+                ok = mbar_wait(sm.hempty0 + 8u * hb, hpar ^ 1u ^ stall, p.wait_ns);
                 if (!ok) record_timeout(p, kSiteProducerHEmpty, huse);
                 if (ok) {
                     HMeta &hm = sm.hmeta[hb];
@@ -261,7 +263,7 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
                         slot -= ring;
                         par ^= 1u;
                     }
-                    lok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, kWaitNs);
+                    lok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, p.wait_ns);
                     if (!lok) record_timeout(p, kSiteProducerEmpty, sq);
                     if (lok) {
                         sm.meta[slot].tok = tok;
@@ -296,7 +298,7 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
             slot -= ring;
             par ^= 1u;
         }
-        ok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, kWaitNs);
+        ok = mbar_wait(sm.empty0 + 8u * slot, par ^ 1u, p.wait_ns);
         if (!ok) record_timeout(p, kSiteProducerDone, sq);
         if (ok) {
             sm.meta[slot].tok = kTokDone;
@@ -327,7 +329,7 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
             par ^= 1u;
         }
         const uint32_t seq = (uint32_t)warp + k * NW;
-        if (!mbar_wait(sm.full0 + 8u * slot, par, kWaitNs)) {
+        if (!mbar_wait(sm.full0 + 8u * slot, par, p.wait_ns)) {
             if (lane == 0) record_timeout(p, kSiteConsumerFull, seq);
             ok = false;
             break;
@@ -358,7 +360,7 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
         if (lane == 0) mbar_arrive(sm.empty0 + 8u * slot);
         if (m.tok >= 0) {
             if (m.use != ready_use) {
-                if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, kWaitNs)) {
+                if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, p.wait_ns)) {
                     if (lane == 0) record_timeout(p, kSiteConsumerHFull, m.use);
                     ok = false;
                     break;
@@ -410,7 +412,7 @@ __device__ bool consume(const GatherParams &p, const Smem &sm, int warp, int lan
         // (a skipped slot never waited for them)
         __syncwarp();
         if (lane == 0 && atomicSub(&sm.hmeta[hb].left, 1) == 1) {
-            if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, kWaitNs)) {
+            if (!mbar_wait(sm.hfull0 + 8u * hb, hpar, p.wait_ns)) {
                 record_timeout(p, kSiteConsumerLastHFull, m.use);
                 ok = false;
             }

@@ -80,8 +80,8 @@ typedef enum mtp_status {
 /* Bits of the device error word (OR-ed together over one call). */
 #define MTP_DEVERR_TOKEN_RANGE 0x1u  /* token_ordering held an id outside [0, V) */
 #define MTP_DEVERR_OFFSETS 0x2u      /* cluster_offsets not ascending in [0, V]  */
-#define MTP_DEVERR_TIMEOUT 0x4u      /* a tensor-core pipeline wait gave up (its
-                                        results are invalid; nothing hung)        */
+#define MTP_DEVERR_TIMEOUT 0x4u      /* a bounded wait of a pipelined kernel gave
+                                        up (its results are invalid; nothing hung) */
 
 /* The head's tables.  Plain data: the struct is read on the host at each call
  * and may live anywhere on the host.
@@ -268,11 +268,25 @@ MTP_API mtp_status mtp_dense_lm_head(const mtp_head_desc *desc, const void *hidd
  *   - Sharing: every call on a device uses the same array, and the array keeps
  *     the last call's contents (each call clears what must start at zero).
  *     Calls whose kernels overlap on the GPU (different streams without
- *     ordering between them) race on the array and give undefined results. */
+ *     ordering between them) race on the array and give undefined results.
+ *   - Checks: the same host-side checks as mtp_masked_topk_tokens run first,
+ *     with the same statuses, before the size limit and the set-up.
+ *   - Device reset: the cached address belongs to the device's context; after
+ *     cudaDeviceReset on that device the entry point must not be used again in
+ *     this process.
+ *   - Errors found on the device (the device error word) go to the array's
+ *     first word: read them with mtp_noalloc_read_device_error on the same
+ *     device and stream after the call; the next call on the device resets it. */
 #define MTP_NOALLOC_SCRATCH_BYTES (8u << 20)
 MTP_API mtp_status mtp_masked_topk_tokens_noalloc(const mtp_head_desc *desc, const void *hidden,
                                                   int32_t batch, int32_t *out_tokens,
                                                   float *out_max, void *stream);
+
+/* The device error word of the last mtp_masked_topk_tokens_noalloc call on
+ * `device`, copied asynchronously into *host_word on `stream` (valid once the
+ * stream has been synchronised); see mtp_read_device_error.  Allocates
+ * nothing. */
+MTP_API mtp_status mtp_noalloc_read_device_error(int32_t device, uint32_t *host_word, void *stream);
 
 /* The packed embedding table: the rows of each cluster in ordered-position
  * order, cut into the operand tiles of the tensor-core gather.  This is a
@@ -363,14 +377,40 @@ MTP_API mtp_status mtp_graph_launch(const mtp_graph *graph, void *stream);
 MTP_API mtp_status mtp_graph_destroy(mtp_graph *graph);
 
 /* Which gather kernel a masked argmax or scatter call with this descriptor and
- * batch runs: 2 for the direct CUDA-core gather (batches of at most 8 rows, and of
- * at most 12 where the tensor-core gather would not run), else 1 for the
- * tensor-core gather (large buckets, batch * K >= 4C; or a packed table with
- * batch * K >= C/4, or >= C/16 when H <= 256), else 0 for the pipelined CUDA-core
- * gather; a negative mtp_status for an invalid descriptor or batch.  The sparse
- * pair never runs the direct gather.  Host-only; for profiling and benchmarks (the
- * calls choose by themselves). */
+ * batch runs: 3 for the fused small-batch kernel, which selects each row's top-K
+ * itself right behind the projection (batches of at most 8 rows with K <= 1024),
+ * else 2 for the direct CUDA-core gather (at most 12 rows where the tensor-core
+ * gather would not run), else 1 for the tensor-core gather (large buckets,
+ * batch * K >= 4C; or a packed table with batch * K >= C/4, or >= C/16 when
+ * H <= 256), else 0 for the pipelined CUDA-core gather; a negative mtp_status for
+ * an invalid descriptor or batch, or MTP_ERR_UNSUPPORTED when mtp_force_gather
+ * forces a kernel that cannot run this call.  The sparse pair runs only kernels 0
+ * and 1.  Host-only; for profiling and benchmarks (the calls choose by
+ * themselves). */
 MTP_API int32_t mtp_gather_plan(const mtp_head_desc *desc, int32_t batch);
+
+/* Testing and profiling aid (not part of the head): make the masked argmax and
+ * scatter calls (and the sparse pair) run gather kernel `kind` (the numbers of
+ * mtp_gather_plan) whatever the batch; -1 restores the library's own choice.
+ * Calls that the forced kernel cannot run (the fused and direct kernels do not
+ * produce the sparse pair; the direct one takes at most 32 rows and
+ * batch * H * 2 <= 200 KB; the fused one K <= 1024) return MTP_ERR_UNSUPPORTED
+ * and launch nothing.  Results do not depend on the kernel beyond fp32 rounding
+ * of the summation order.  Process-wide, not thread-safe.  Out-of-range kind:
+ * MTP_ERR_SHAPE. */
+MTP_API mtp_status mtp_force_gather(int32_t kind);
+
+/* Testing aid for the bounded waits (not part of the head).  Every mbarrier wait
+ * of the pipelined CUDA-core gather (kernel 0 of mtp_gather_plan) gives up after
+ * a wall-clock limit, sets MTP_DEVERR_TIMEOUT in the device error word and lets
+ * its CTA finish; the call's results are then invalid but nothing hangs, and the
+ * next call starts clean.  limit_ns > 0 sets that limit (default 2 s; 0 restores
+ * the default).  stall != 0 makes the first hidden-row buffer wait of every CTA
+ * that has work wait for a barrier phase that nothing completes, before the CTA
+ * has issued any copy: the wait runs out after limit_ns, and so do the waits of
+ * the CTA's consumer warps, which then have nothing to consume.  Process-wide,
+ * not thread-safe; a negative limit gives MTP_ERR_SHAPE. */
+MTP_API mtp_status mtp_wait_test(int64_t limit_ns, int32_t stall);
 
 /* Enqueue an asynchronous copy of the workspace's device error word (a set of
  * MTP_DEVERR_* bits, reset by each masked call) into *host_word; the value is

@@ -180,8 +180,11 @@ def test_gather_plan(L):
     d = _desc()
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0      # B*K = C: CUDA-core gather
     assert L.mtp_gather_plan(ctypes.byref(d), 13) == 0
-    assert L.mtp_gather_plan(ctypes.byref(d), 12) == 2      # small batches: the direct one
-    assert L.mtp_gather_plan(ctypes.byref(d), 1) == 2
+    assert L.mtp_gather_plan(ctypes.byref(d), 12) == 2      # a dozen rows: the direct one
+    assert L.mtp_gather_plan(ctypes.byref(d), 9) == 2
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 3       # up to 8 rows: the fused kernel
+    assert L.mtp_gather_plan(ctypes.byref(d), 1) == 3
+    assert L.mtp_gather_plan(ctypes.byref(_desc(K=1025, C=2048)), 1) == 2   # fused: K <= 1024
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1     # B*K = 4C: large buckets
     assert L.mtp_gather_plan(ctypes.byref(d), 0) == 0
     assert L.mtp_gather_plan(ctypes.byref(d), -1) == -2
@@ -200,15 +203,38 @@ def test_gather_plan(L):
     d = _desc(H=256)                                         # small hidden size: from B*K >= C/16
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 9) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2       # up to 8 rows the direct one wins
-    assert L.mtp_gather_plan(ctypes.byref(d), 3) == 2
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 3       # up to 8 rows the fused kernel
+    assert L.mtp_gather_plan(ctypes.byref(d), 3) == 3
     d = _desc(offsets=0x5000)                                # ragged clusters: the same rules
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 3
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1
+
+
+def test_forced_gather(L):
+    d = _desc()
+    try:
+        for kind in (0, 1, 2, 3):
+            assert L.mtp_force_gather(kind) == 0
+            assert L.mtp_gather_plan(ctypes.byref(d), 4) == kind
+        assert L.mtp_force_gather(2) == 0                   # the direct kernel: at most 32 rows
+        assert L.mtp_gather_plan(ctypes.byref(d), 33) == -6
+        assert L.mtp_force_gather(3) == 0                   # the fused kernel: K <= 1024
+        assert L.mtp_gather_plan(ctypes.byref(_desc(K=1025, C=2048)), 4) == -6
+        assert L.mtp_force_gather(4) == -2
+        assert L.mtp_force_gather(-2) == -2
+    finally:
+        assert L.mtp_force_gather(-1) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 4) == 3
+
+
+def test_wait_test_control(L):
+    assert L.mtp_wait_test(-1, 0) == -2
+    assert L.mtp_wait_test(1000000, 1) == 0
+    assert L.mtp_wait_test(0, 0) == 0                       # back to the default
 
 
 def test_graph_capture_rejects_bad_arguments(L):
@@ -281,6 +307,15 @@ def test_noalloc_host_checks(L):
     assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), FAKE, 0, out, None, None) == 0
     assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), FAKE, -1, out, None, None) == -2
     assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), FAKE, 944, out, None, None) == -6
+    # the workspace call's checks come first, with its statuses, whatever the size
+    assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(_desc(ew=0)), FAKE, 944, out, None, None) == -1
+    assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), ctypes.c_void_p(0x7008), 944, out, None,
+                                            None) == -3
+    assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(d), FAKE, 4, None, None, None) == -1
+    assert L.mtp_masked_topk_tokens_noalloc(ctypes.byref(_desc(K=0)), FAKE, 944, out, None, None) == -2
+    word = ctypes.c_uint32(0)
+    assert L.mtp_noalloc_read_device_error(0, None, None) == -1
+    assert L.mtp_noalloc_read_device_error(-1, ctypes.byref(word), None) == -2
 
 
 def test_cluster_range_checks_and_packed_size(L):

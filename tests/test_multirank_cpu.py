@@ -79,6 +79,26 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
+def test_gpus_flag_starts_its_own_ranks():
+    """`bench.py --gpus 2` outside a launcher starts two ranks itself (torch.distributed.run
+    on 127.0.0.1): the reference arm's line, printed by rank 0 alone, reports both ranks,
+    with the same `config` object as the library's arm."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--workload", "tiny", "--steps", "2", "--warmup", "3"]
+    r = subprocess.run(cmd, env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    sys.path.insert(0, ROOT)
+    import bench
+    from centroid_masked_sparse_gb300 import synth
+    args = bench.parse_args(["--workload", "tiny", "--gpus", "2"])
+    assert line["config"] == bench.run_config(args, synth.WORKLOADS["tiny"], 1, 2)
+
+
 def _key(logit, token):
     """A key in the order the library's keys follow: larger logit, then lower token id,
     as a signed 64-bit integer (used here only to feed the exchange step)."""

@@ -434,17 +434,115 @@ def test_overlapping_offsets_overflow_the_item_list(build_lib):
                         vocab_size=V)
     h = helpers.bf16_tensor(synth.random_hidden(1, H, 12))
     ws = dbad.workspace(1)
-    assert m.mtp_gather_plan(dbad, 1) == "cuda_core_direct"
-    tok, _ = m.mtp_masked_topk_tokens(dbad, h, workspace=ws)
-    torch.cuda.synchronize()
-    assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_OFFSETS
-    assert 0 <= int(tok.cpu()[0]) < V
     ref = oracle.masked_topk_tokens(oh, synth.random_hidden(1, H, 12))
-    tok, _ = m.mtp_masked_topk_tokens(dh, h, workspace=ws)
-    torch.cuda.synchronize()
+    # the work-item list belongs to the top-K kernel + gather path; the fused kernel has none
+    # (it only reports the reversed ranges)
+    for kind in ("cuda_core_direct", "fused"):
+        m.mtp_force_gather(kind)
+        try:
+            tok, _ = m.mtp_masked_topk_tokens(dbad, h, workspace=ws)
+            torch.cuda.synchronize()
+            assert m.mtp_read_device_error(ws) & m.MTP_DEVERR_OFFSETS
+            assert 0 <= int(tok.cpu()[0]) < V
+            tok, _ = m.mtp_masked_topk_tokens(dh, h, workspace=ws)
+            torch.cuda.synchronize()
+        finally:
+            m.mtp_force_gather(None)
+        assert m.mtp_read_device_error(ws) == 0
+        if ref["score_margin"][0] > helpers.MARGIN and ref["logit_margin"][0] > helpers.MARGIN:
+            assert int(tok.cpu()[0]) == int(ref["tokens"][0])
+
+
+# ---------------------------------------------------------------------------
+# every gather kernel at the drafter's small batches; the fused small-batch kernel
+
+
+@pytest.mark.parametrize("B", [1, 3, 8])
+@pytest.mark.parametrize("kind", ["fused", "cuda_core_direct", "cuda_core", "tensor_core"])
+def test_every_gather_kernel_small_batches(build_lib, B, kind):
+    """The uniform workload at small batches through each gather kernel (forced): token
+    ids equal the oracle's, max logits and full-vocabulary rows within the tolerance."""
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    hidden, ref, _ = helpers.clean_batch("uniform", oh, B, row0=7000 + B)
+    h = helpers.bf16_tensor(hidden)
+    ws = dh.workspace(B)
+    m.mtp_force_gather(kind)
+    try:
+        assert m.mtp_gather_plan(dh, B) == kind
+        tok, mx = m.mtp_masked_topk_tokens(dh, h, workspace=ws)
+        sc = m.mtp_masked_scatter_logits(dh, h, workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        m.mtp_force_gather(None)
     assert m.mtp_read_device_error(ws) == 0
-    if ref["score_margin"][0] > helpers.MARGIN and ref["logit_margin"][0] > helpers.MARGIN:
-        assert int(tok.cpu()[0]) == int(ref["tokens"][0])
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+    helpers.assert_close(mx.cpu().numpy(), ref["max_logit"], f"{kind} B={B} max")
+    sc_np = sc.cpu().numpy()
+    helpers.assert_close(sc_np, oracle.masked_scatter_logits(oh, hidden), f"{kind} B={B} scatter")
+    assert (np.isfinite(sc_np).sum(axis=1) == 32 * 128).all()
+
+
+@pytest.mark.parametrize("name,B", [("variable", 1), ("variable", 8), ("shared", 8), ("draft256", 4)])
+def test_fused_kernel_other_workloads(build_lib, name, B):
+    """The fused kernel (every batch of at most 8 rows) on lognormal clusters, on K=128 of
+    4096 small clusters and at H=256, both finishes, against the oracle."""
+    m = build_lib
+    oh, dh = device_head(m, name)
+    assert m.mtp_gather_plan(dh, B) == "fused"
+    hidden, ref = check_topk(m, name, B, row0=6100)
+    sc = m.mtp_masked_scatter_logits(dh, helpers.bf16_tensor(hidden))
+    torch.cuda.synchronize()
+    helpers.assert_close(sc.cpu().numpy(), oracle.masked_scatter_logits(oh, hidden), f"fused {name} scatter")
+
+
+@pytest.mark.parametrize("K", [1024, 1025])
+def test_fused_kernel_at_its_k_limit(build_lib, K):
+    """K up to 1024 selections per row run the fused kernel (here K of C = 1100 centroids,
+    most of the vocabulary a candidate); one more falls back to the direct gather."""
+    m = build_lib
+    t, oh, dh = _custom(m, 1100 * 8, 64, 1100, K, seed=K)
+    assert m.mtp_gather_plan(dh, 3) == ("fused" if K <= 1024 else "cuda_core_direct")
+    hidden = synth.random_hidden(3, 64, K + 1)
+    _full_check(m, oh, dh, hidden, f"K={K}")
+
+
+def test_bounded_wait_gives_up_cleanly(build_lib):
+    """A wait that runs out: the pipelined gather's first hidden-row buffer wait is made to
+    wait for a barrier phase that nothing completes, with a 20 ms limit (the wait test).
+    The producer gives up before it has issued any copy, the consumer warps' waits run out
+    next, and the call finishes with MTP_DEVERR_TIMEOUT and the site of the first wait that
+    gave up in the workspace; the next call on the same workspace runs clean and right."""
+    import time
+    m = build_lib
+    oh, dh = device_head(m, "uniform")
+    hidden, ref, _ = helpers.clean_batch("uniform", oh, 8, row0=8800)
+    h = helpers.bf16_tensor(hidden)
+    ws = dh.workspace(8)
+    m.mtp_force_gather("cuda_core")
+    try:
+        m.mtp_masked_topk_tokens(dh, h, workspace=ws)     # module loaded, nothing pending
+        torch.cuda.synchronize()
+        m.mtp_wait_test(20_000_000, stall=True)
+        try:
+            t0 = time.time()
+            m.mtp_masked_topk_tokens(dh, h, workspace=ws)
+            torch.cuda.synchronize()
+            elapsed = time.time() - t0
+        finally:
+            m.mtp_wait_test(0, stall=False)
+        word = m.mtp_read_device_error(ws)
+        ctrl = ws[:32].view(torch.int32).cpu().tolist()
+        assert word & m.MTP_DEVERR_TIMEOUT, f"error word {word:#x}"
+        assert ctrl[4] in (1, 4), f"wait site {ctrl[4]}"     # consumer slot / producer h buffer
+        assert elapsed < 1.0, f"{elapsed:.3f} s: the waits did not give up after 20 ms"
+        tok, mx = m.mtp_masked_topk_tokens(dh, h, workspace=ws)
+        torch.cuda.synchronize()
+        assert m.mtp_read_device_error(ws) == 0
+    finally:
+        m.mtp_force_gather(None)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+    helpers.assert_close(mx.cpu().numpy(), ref["max_logit"], "after the wait test")
 
 
 def test_repeat_calls_are_deterministic(build_lib):
@@ -847,10 +945,11 @@ def test_draft256_full_size(build_lib, B, packed):
 def test_sharded_head_equals_unsharded(build_lib, name, B, packed, shards):
     """Each shard gathers only its clusters; the max of the shards' keys decodes to the
     unsharded argmax and the max of their scatter rows is the unsharded scatter, bit
-    for bit (every candidate's logit is computed by one shard, with the same arithmetic)."""
+    for bit (every candidate's logit is computed by one shard, with the same arithmetic),
+    and both equal the oracle (token ids exactly, logits within the tolerance)."""
     m = build_lib
     oh, dh = device_head(m, name)
-    hidden = synth.hidden_batch(name, B, None, helpers.tables(name).prototypes, row0=123)
+    hidden, oref, _ = helpers.clean_batch(name, oh, B, row0=123)
     h = helpers.bf16_tensor(hidden)
     C = oh.C
     cuts = [round(i * C / shards) for i in range(shards + 1)]
@@ -877,6 +976,12 @@ def test_sharded_head_equals_unsharded(build_lib, name, B, packed, shards):
         torch.cuda.synchronize()
         assert torch.equal(tok, ref_tok) and torch.equal(mx, ref_max)
         assert torch.equal(sc, ref_sc)
+        # and the combined shards against the oracle: token ids, max logits, scatter rows
+        np.testing.assert_array_equal(tok.cpu().numpy(), oref["tokens"])
+        helpers.assert_close(mx.cpu().numpy(), oref["max_logit"], f"sharded {name} max")
+        rows = [0, B // 2, B - 1]
+        helpers.assert_close(sc.cpu().numpy()[rows], oracle.masked_scatter_logits(oh, hidden[rows]),
+                             f"sharded {name} scatter rows")
         # each shard wrote only its own clusters' tokens
         finite = [torch.isfinite(x).sum().item() for x in scs]
         assert sum(finite) == torch.isfinite(ref_sc).sum().item()
