@@ -19,14 +19,10 @@
 //           write fp32 results; for the dense head they also fold each row's
 //           (logit, lower token id) argmax key into a 64-bit atomicMax.
 // Split-K (for the projection, whose M is only C): the splits of one output
-// tile run as one thread-block cluster, and each rank adds up a slice of the
-// tile's columns over the ranks in rank order, so results are deterministic and
-// no partial ever goes to HBM.  Where a receive buffer fits beside the stage
-// ring, every CTA's epilogue stores its partial of each column straight from the
-// accumulator registers into the owning rank's receive buffer (distributed
-// shared memory stores need no round trip) and one cluster barrier makes them
-// visible; otherwise each CTA parks its partial tile in its own (idle) ring and
-// the owners load the partials from every rank between two cluster barriers.  Every mbarrier wait gives up after a wall-clock limit and records
+// tile run as one thread-block cluster; each CTA parks its partial tile in its
+// own shared memory and rank 0 adds the partials through distributed shared
+// memory in rank order, so results are deterministic and no partial ever goes
+// to HBM.  Every mbarrier wait gives up after a wall-clock limit and records
 // MTP_DEVERR_TIMEOUT instead of hanging.
 #include <cudaTypedefs.h>
 
@@ -61,9 +57,7 @@ struct TcParams {
     uint32_t *err;          // timeout reports (may be null)
     uint32_t *zero;         // cleared at kernel start (the next kernels' workspace words)
     int zero_words;
-    int cluster_reduce;     // splits > 1: one cluster per output tile, summed through DSMEM:
-                            // 1 = partials pushed into the owners' receive buffers,
-                            // 2 = parked in each CTA's ring and pulled by the owners
+    int cluster_reduce;     // splits > 1: one cluster per output tile, summed through DSMEM
     int round_bf16;         // dense head: logits rounded to bf16 before they are stored or compared
     float softcap;          // dense head: final logit softcap (cap * tanh(v / cap)), 0 = none
     int after_stage;        // launched behind the staging of the hidden rows: the producer
@@ -103,21 +97,8 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
     return v;
 }
 
-// Columns of the partial tile that one pull step loads at once (from every rank).
+// Columns of the partial tile that one reduction step loads at once (from every rank).
 constexpr int kRedCols = 4;
-
-// Store into another CTA's shared memory (no round trip); the cluster barrier's
-// release orders it before the owner reads it.
-__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v)
-{
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// Columns of a split-K output tile that each cluster rank owns and adds up.
-__host__ __device__ __forceinline__ int red_cols_per_rank(int n_pad, int splits)
-{
-    return (n_pad + splits - 1) / splits;
-}
 
 __device__ __forceinline__ void report_timeout(const TcParams &p)
 {
@@ -136,8 +117,6 @@ __global__ void __launch_bounds__(kTcThreads)
     uint8_t *b_smem = smem + (size_t)S * kABytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(b_smem + (size_t)S * b_bytes);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
-    // split-K receive buffer: recv[source rank][owned column][128 rows] fp32
-    float *recv = reinterpret_cast<float *>(bars + 2 * S + 6);
     __shared__ int s_last;
 
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x & (kWarp - 1);
@@ -263,31 +242,18 @@ __global__ void __launch_bounds__(kTcThreads)
             const bool m_ok = m < p.M;
             const uint32_t trow = tmem_base + ((uint32_t)(warp * kWarp) << 16) + (uint32_t)(acc * p.n_pad);
             float *outp = p.out ? p.out + (size_t)sp * p.split_stride : nullptr;
-            const int m_local = warp * kWarp + lane;
-            // push mode: column j of the partial tile goes to rank j / per, into its
-            // recv[this rank][j mod per][m] (a warp's 32 lanes store one 128-byte line);
-            // pull mode: the ring is idle now (every MMA of this CTA's only unit has
-            // completed), so it holds the partial tile as red[n][128]
-            const int per = red_cols_per_rank(p.n_pad, p.splits);
+            // cluster mode: the stage ring is idle now (every MMA of this CTA's only
+            // unit has completed), so it holds the partial tile as red[n][128]: a warp
+            // reads one column of it as one contiguous 128-byte line
             float *red = reinterpret_cast<float *>(smem);
+            const int m_local = warp * kWarp + lane;
             for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
                 uint32_t r[16];
                 tmem_load_16(trow + (uint32_t)c0, r);
                 tmem_wait_load();
-                if (p.cluster_reduce == 2) {
+                if (p.cluster_reduce) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) red[(c0 + j) * kTileM + m_local] = __uint_as_float(r[j]);
-                    continue;
-                }
-                if (p.cluster_reduce == 1) {
-                    const uint32_t recv0 = smem_u32(recv);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = c0 + j;
-                        const int owner = col / per, jl = col - owner * per;
-                        const uint32_t off = (uint32_t)(((sp * per + jl) * kTileM + m_local) * 4);
-                        st_dsmem_f32(dsmem_addr(recv0 + off, (uint32_t)owner), __uint_as_float(r[j]));
-                    }
                     continue;
                 }
                 // the dense head's options act on the 16 loaded values before any
@@ -332,36 +298,10 @@ __global__ void __launch_bounds__(kTcThreads)
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
-    if (p.cluster_reduce == 1) {
-        // split-K, push: every rank has stored its partials of this rank's columns into
-        // recv; the barrier (release / acquire at cluster scope) makes them visible, then
-        // each rank adds its columns over the ranks in rank order (deterministic) and
-        // stores them.  Nothing reads another CTA's shared memory after the barrier, so a
-        // CTA may leave as soon as it is done.
-        cluster_sync_all();
-        uint32_t rank;
-        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-        if (warp < 4) {
-            int mt, sp, nb;
-            decode_unit(p, blockIdx.x, &mt, &sp, &nb);
-            const int m_local = warp * kWarp + lane;
-            const int m = mt * kTileM + m_local;
-            const int per = red_cols_per_rank(p.n_pad, p.splits);
-            if (m < p.M) {
-                for (int jl = 0; jl < per; ++jl) {
-                    const int j = (int)rank * per + jl;
-                    const int n = nb * p.n_pad + j;
-                    if (j >= p.n_pad || n >= p.N) break;
-                    float v = 0.f;
-                    for (int r = 0; r < p.splits; ++r) v += recv[(r * per + jl) * kTileM + m_local];
-                    p.out[(size_t)n * p.ldo + m] = v;
-                }
-            }
-        }
-    } else if (p.cluster_reduce == 2) {
-        // split-K, pull: the cluster's CTAs hold the partial tiles of one output tile.
-        // Each rank sums its slice of the columns over all ranks, in rank order, and
-        // stores it; it loads kRedCols columns from every rank at once (all loads
+    if (p.cluster_reduce) {
+        // split-K: the cluster's CTAs hold the partial tiles of one output tile.  Each
+        // rank sums a slice of the columns over all ranks, in rank order (deterministic),
+        // and stores it; it loads kRedCols columns from every rank at once (all loads
         // independent, each warp-wide load one 128-byte line), so the remote latency is
         // paid once per group of columns, not once per column.
         cluster_sync_all();
@@ -372,7 +312,7 @@ __global__ void __launch_bounds__(kTcThreads)
             decode_unit(p, blockIdx.x, &mt, &sp, &nb);
             const int m_local = warp * kWarp + lane;
             const int m = mt * kTileM + m_local;
-            const int per = red_cols_per_rank(p.n_pad, p.splits);
+            const int per = (p.n_pad + p.splits - 1) / p.splits;
             const int j0 = (int)rank * per, j1 = min(p.n_pad, j0 + per);
             const uint32_t red0 = smem_u32(smem);
             uint32_t base[8];
@@ -495,26 +435,15 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     const size_t budget = 220 * 1024 - 1024 - 256;
     int stages = (int)(budget / stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
-    int reduce_mode = 0;
-    size_t recv_bytes = 0;
     if (p.splits > 1) {
-        // one unit per CTA: enough stages for its k-blocks; less shared memory lets several
-        // CTAs share an SM, so every cluster of the grid is resident at once
+        // one unit per CTA: enough stages for its k-blocks and for the partial tile that the
+        // cluster reduction parks in the ring; less shared memory lets several CTAs share an
+        // SM, so every cluster of the grid is resident at once
+        const size_t red = (size_t)p.n_pad * kTileM * 4;
         int need = p.kb_per_split;
+        while ((size_t)need * stage_bytes < red) ++need;
         if (need < 2) need = 2;
         if (need < stages) stages = need;
-        // push into a receive buffer beside the ring where both fit, else park the partial
-        // tile in the ring (which must then hold it) and pull
-        recv_bytes = (size_t)p.splits * red_cols_per_rank(p.n_pad, p.splits) * kTileM * 4;
-        if ((size_t)stages * stage_bytes + recv_bytes <= budget) {
-            reduce_mode = 1;
-        } else {
-            reduce_mode = 2;
-            recv_bytes = 0;
-            const size_t red = (size_t)p.n_pad * kTileM * 4;
-            while ((size_t)stages * stage_bytes < red && (size_t)(stages + 1) * stage_bytes <= budget) ++stages;
-            if ((size_t)stages * stage_bytes < red) return cudaErrorInvalidValue;
-        }
     }
     if (stages < 2) return cudaErrorInvalidValue;
     p.stages = stages;
@@ -528,10 +457,12 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     p.err = a.ctrl ? a.ctrl + kCtrlError : nullptr;
     p.zero = a.zero;
     p.zero_words = a.zero ? a.zero_words : 0;
-    p.cluster_reduce = reduce_mode;
+    p.cluster_reduce = p.splits > 1;
     p.round_bf16 = a.round_bf16 ? 1 : 0;
     p.softcap = a.softcap;
     p.after_stage = a.after_stage ? 1 : 0;
+    if (p.cluster_reduce && (size_t)stages * stage_bytes < (size_t)p.n_pad * kTileM * 4)
+        return cudaErrorInvalidValue;
     if (p.cluster_reduce && (p.keys || p.splits > 8 || p.units > 65535)) return cudaErrorInvalidValue;
 
     alignas(64) CUtensorMap map_a;
@@ -539,7 +470,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s)
     if (!encode_map(&map_a, a.table, a.K, a.M, a.ld_table, kTileM)) return cudaErrorInvalidValue;
     if (!encode_map(&map_b, a.hidden, a.K, a.N, a.K, p.n_pad)) return cudaErrorInvalidValue;
 
-    const size_t smem = 1024 + (size_t)stages * stage_bytes + (size_t)(2 * stages + 6) * 8 + recv_bytes;
+    const size_t smem = 1024 + (size_t)stages * stage_bytes + (size_t)(2 * stages + 4) * 8 + 16;
     cudaError_t e = allow_smem((const void *)k_tc_gemm, smem);
     if (e != cudaSuccess) return e;
     if (!p.cluster_reduce) {
