@@ -215,6 +215,15 @@ class Timer:
         self.flush.zero_()
         self.evict.sum()
 
+    def before_call(self, flush):
+        """Outside the timed events: the L2 flush, or (warm figure) a ~25 us spin kernel,
+        so that in both cases the GPU is busy while the host enqueues the call and the
+        call's launches are queued before it starts (no host launch gap inside it)."""
+        if flush:
+            self.flush_l2()
+        else:
+            self.torch.cuda._sleep(50000)
+
     def events(self, n):
         torch = self.torch
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -228,8 +237,7 @@ class Timer:
         previous call left (the warm figure)."""
         torch, m = self.torch, self.m
         for i in range(warmup):
-            if flush:
-                self.flush_l2()
+            self.before_call(flush)
             fn(i)
         names = ([kernel] if kernel else []) + [k for k in extra_kernels if k != kernel]
         call_ev = self.events(2 * steps)
@@ -244,8 +252,7 @@ class Timer:
         try:
             t0 = time.time()
             for i in range(steps):
-                if flush:
-                    self.flush_l2()
+                self.before_call(flush)
                 for k in names:
                     m.mtp_profile_events(k, kev[k][2 * i], kev[k][2 * i + 1])
                 call_ev[2 * i].record()

@@ -36,6 +36,8 @@
  *   device error word (see mtp_read_device_error).
  * - A workspace serves one call at a time: concurrent calls on different
  *   streams need different workspaces.  Tables may be shared freely.
+ * - A call makes desc->device current while it launches and gives the calling
+ *   thread back its own current device before it returns.
  *
  * Readings of the source that this library takes (where the page is silent or
  * inconsistent): token ids are int32 (the page uses int64); scores and logits
