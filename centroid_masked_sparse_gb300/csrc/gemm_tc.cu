@@ -409,6 +409,10 @@ int tc_splits(int M, int N, int K)
     const int num_kb = (K + kTileK - 1) / kTileK;
     int splits = 128 / (m_tiles * n_blocks);
     if (splits > 8) splits = 8;
+    // long contractions keep longer splits: at K = 2560 (40 k-blocks), M = 2048, N = 64 four
+    // splits of 10 k-blocks measured faster than eight of 5 (projection + top-K 19.4 vs
+    // 25.3 us on GB300); at K = 1536 eight splits of 3 stay ahead (17.4 vs 18.2 us)
+    if (num_kb >= 32 && splits > 4) splits = 4;
     if (splits > num_kb) splits = num_kb;
     if (splits < 1) splits = 1;
     const int per = (num_kb + splits - 1) / splits;  // no empty split
