@@ -15,7 +15,7 @@ constexpr int kWarp = 32;
 constexpr int kCtrlError = 0;    // MTP_DEVERR_* bits
 constexpr int kCtrlItems = 1;    // number of gather work items built by the top-K kernel
 constexpr int kCtrlTicket = 2;   // CTAs of the gather-score kernel that have finished
-constexpr int kCtrlNext = 3;     // reserved (cleared with the others)
+constexpr int kCtrlNext = 3;     // the gathers' item counter: items handed out after the first round
 constexpr int kCtrlWaitSite = 4; // first wait that gave up: site code (see score.cu)
 constexpr int kCtrlWaitCta = 5;  //   its CTA
 constexpr int kCtrlWaitSeq = 6;  //   its slot sequence number or h-buffer use

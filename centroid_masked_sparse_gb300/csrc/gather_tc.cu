@@ -95,8 +95,11 @@ struct UnitMeta {
     int npad, nvalid;
     int p0;             // token-order table: first ordered position; packed: first group
     int local0;         // position of the chunk's first candidate inside its cluster
-    int pad[2];
+    int g1, nvalid1;    // a paired unit's second chunk (packed: first group, candidates)
     int ranks[kMaxN];   // sparse pair: rank of the cluster in each row's top-K
+    // per row: bit 0 = a row of the first chunk's bucket, bit 1 = of the second chunk's
+    // (the candidates in tile rows 64..127 of a paired unit); 3 for an unpaired unit
+    uint8_t half[kMaxN];
 };
 
 struct Params {
@@ -163,6 +166,36 @@ __device__ int bucket_rows(const Params &p, uint32_t w, int blk, int lane, int *
     return max(0, min(p.nmax, total - lo));
 }
 
+// Rows of the union of two buckets (row-mask words wa, wb of this lane) in row order
+// (at most nmax), and for each which bucket holds it (bit 0: a, bit 1: b).
+__device__ int union_rows(const Params &p, uint32_t wa, uint32_t wb, int lane, int *rows, uint8_t *half)
+{
+    const uint32_t w = wa | wb;
+    const int cnt = __popc(w);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int pos = incl - cnt;
+    for (uint32_t m = w; m; m &= m - 1u, ++pos) {
+        if (pos >= p.nmax) break;
+        const int bit = __ffs(m) - 1;
+        rows[pos] = lane * kWarp + bit;
+        half[pos] = (uint8_t)(((wa >> bit) & 1u) | (((wb >> bit) & 1u) << 1));
+    }
+    return min(p.nmax, __shfl_sync(0xffffffffu, incl, kWarp - 1));
+}
+
+__device__ __forceinline__ int warp_count(uint32_t w)
+{
+    int c = __popc(w);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    return c;
+}
+
 // The metadata warp's view of one work item: its range and the loads its units
 // need (this lane's row-mask word and token ids, the packed group), issued one
 // item before they are used so that their latency overlaps the current item.
@@ -203,28 +236,110 @@ __device__ __forceinline__ void load_item(const Params &p, int2 rec, bool have, 
     if (p.packed) m.g0 = (__ldg(p.poff + rec.x) + rec.y) / kPackRows;
 }
 
-// Metadata warp: publishes the units of this CTA's items (items blockIdx.x,
-// blockIdx.x + G, ...; records two items ahead, their loads one item ahead), then
-// an end-of-stream entry.  False after a timed-out wait.
+// Candidate token ids of an item for the unit's tile rows lane, lane+32, ... (the item's
+// position j*32+lane), -1 past its chunk or for an id outside [0, V) (reported).
+__device__ __forceinline__ int unit_token(const Params &p, int tok)
+{
+    if (tok == kNoPos) return -1;
+    if ((unsigned)tok >= (unsigned)p.V) {
+        atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
+        return -1;
+    }
+    return tok;
+}
+
+// A chunk of at most 64 candidates as the pairing needs it (per lane: row-mask word
+// `lane`, token ids of positions lane and 32 + lane).
+struct ShortChunk {
+    uint32_t w;
+    int tok0, tok1, nvalid, g0;
+};
+
+__device__ __forceinline__ ShortChunk short_chunk(const ItemPre &m)
+{
+    return ShortChunk{m.w, m.tok[0], m.tok[1], m.nvalid, m.g0};
+}
+
+// Publishes one unit holding chunk a and its whole bucket (at most nmax rows) or, with
+// b, chunks a and b together: a's candidates in tile rows 0..63, b's in 64..127, the
+// union of their buckets as the unit's rows.  Both chunks are at most 64 candidates
+// and the union at most nmax rows (the caller checks).  Packed table only (no sparse
+// pair).  False after a timed-out wait.
+__device__ bool publish_joint(const Params &p, UnitMeta *meta, uint32_t mfull0, uint32_t mempty0, int &u,
+                              int lane, const ShortChunk &a, const ShortChunk *b)
+{
+    const int um = u % kMeta;
+    if (!mbar_wait(mempty0 + 8u * um, ((uint32_t)(u / kMeta) & 1u) ^ 1u, kWaitNs)) return false;
+    UnitMeta &m = meta[um];
+    const int n = union_rows(p, a.w, b ? b->w : a.w, lane, m.rows, m.half);
+    const int npad = (n + 15) & ~15;
+    for (int r = n + lane; r < npad; r += kWarp) {
+        m.rows[r] = p.B;   // zero rows
+        m.half[r] = 0;
+    }
+    m.tok[lane] = unit_token(p, a.tok0);
+    m.tok[kWarp + lane] = unit_token(p, a.tok1);
+    m.tok[2 * kWarp + lane] = unit_token(p, b ? b->tok0 : kNoPos);
+    m.tok[3 * kWarp + lane] = unit_token(p, b ? b->tok1 : kNoPos);
+    if (lane == 0) {
+        m.n = n;
+        m.npad = npad;
+        m.nvalid = a.nvalid;
+        m.local0 = 0;
+        m.p0 = a.g0;
+        m.g1 = b ? b->g0 : 0;
+        m.nvalid1 = b ? b->nvalid : 0;
+    }
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence_block();
+        mbar_arrive(mfull0 + 8u * um);
+    }
+    ++u;
+    return true;
+}
+
+// The next item a CTA takes after its first: a ticket on the call's item counter
+// (cleared with the other control words by the projection), offset by the grid, so
+// every item past the first round goes to whichever CTA asks first.  Items differ in
+// cost (a large bucket is several units), so CTAs that finish early take more.  The
+// ticket is taken when the item is about to be needed (taking it earlier, to hide the
+// atomic's round trip, measured worse: it leaves fewer items to even out the tail).
+__device__ __forceinline__ int grab_item(const Params &p, int lane)
+{
+    int it = 0;
+    if (lane == 0) it = (int)gridDim.x + (int)atomicAdd(p.ctrl + kCtrlNext, 1u);
+    return __shfl_sync(0xffffffffu, it, 0);
+}
+
+// Metadata warp: publishes the units of this CTA's items (item blockIdx.x, then the
+// items it grabs; item records two items ahead, their loads one item ahead), pairing
+// short chunks where the call allows it, then an end-of-stream entry.  False after a
+// timed-out wait.
+template <bool PAIR>
 __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, uint32_t mempty0, int lane)
 {
-    const int G = (int)gridDim.x;
     const int2 none = make_int2(-1, 0);
-    // this CTA's first two item records are loaded together with the item count, not
-    // after it (both slots lie inside the list; a record past the count is dropped)
-    const int2 rec0 = (int)blockIdx.x < p.items_cap ? p.items[blockIdx.x] : none;
-    const int2 rec1 = (int)blockIdx.x + G < p.items_cap ? p.items[blockIdx.x + G] : none;
+    int it = blockIdx.x;
+    // this CTA's first item record is loaded together with the item count, not after it
+    // (the slot lies inside the list; a record past the count is dropped), and the
+    // ticket for the second item is taken while both are in flight
+    const int2 rec0 = it < p.items_cap ? p.items[it] : none;
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
+    int it1 = grab_item(p, lane);
+    const int2 rec1 = it1 < p.items_cap ? p.items[it1] : none;
     const long long packed_groups = p.packed ? __ldg(p.poff + p.C) / kPackRows : 0;
     int u = 0;
-    int it = blockIdx.x;
     ItemPre nxt;
     load_item(p, it < n_items ? rec0 : none, it < n_items, lane, nxt);
-    int2 rec2 = it + G < n_items ? rec1 : none;
-    for (; it < n_items; it += G) {
+    int2 rec2 = it1 < n_items ? rec1 : none;
+    ShortChunk pend{};         // a chunk of at most 64 candidates waiting for a partner
+    bool have_pend = false;
+    int it2 = it1 < n_items ? grab_item(p, lane) : n_items;   // the item after it1
+    for (; it < n_items; it = it1, it1 = it2, it2 = it2 < n_items ? grab_item(p, lane) : n_items) {
         const ItemPre cur = nxt;
-        load_item(p, rec2, it + G < n_items, lane, nxt);
-        rec2 = it + 2 * G < n_items ? p.items[it + 2 * G] : none;
+        load_item(p, rec2, it1 < n_items, lane, nxt);
+        rec2 = it2 < n_items ? p.items[it2] : none;
         if (!cur.valid) continue;
         const int nvalid = cur.nvalid, p0 = cur.p0, g0 = cur.g0;
         // a chunk reaching past the packed table's last group (a table packed from other
@@ -232,6 +347,30 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
         if (p.packed && (long long)g0 + (nvalid + kPackRows - 1) / kPackRows > packed_groups) {
             if (lane == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
             continue;
+        }
+        if (PAIR) {
+            // two chunks of at most 64 candidates whose buckets together fit a unit share
+            // it: the next such item waits here for a partner
+            if (nvalid <= kTileM / 2 && warp_count(cur.w) <= p.nmax) {
+                const ShortChunk sc = short_chunk(cur);
+                if (!have_pend) {
+                    pend = sc;
+                    have_pend = true;
+                    continue;
+                }
+                const bool fits = warp_count(pend.w | sc.w) <= p.nmax;
+                if (!publish_joint(p, meta, mfull0, mempty0, u, lane, pend, fits ? &sc : nullptr)) return false;
+                if (fits) {
+                    have_pend = false;
+                } else {
+                    pend = sc;
+                }
+                continue;
+            }
+            if (have_pend) {
+                if (!publish_joint(p, meta, mfull0, mempty0, u, lane, pend, nullptr)) return false;
+                have_pend = false;
+            }
         }
         for (int blk = 0;; ++blk) {
             const int um = u % kMeta;
@@ -243,17 +382,10 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
             if (n == 0) break;
             const int npad = (n + 15) & ~15;
             for (int r = n + lane; r < npad; r += kWarp) m.rows[r] = p.B;   // zero rows
+            if (PAIR)
+                for (int r = lane; r < npad; r += kWarp) m.half[r] = r < n ? 3 : 0;
 #pragma unroll
-            for (int j = 0; j < kTileM / kWarp; ++j) {
-                int tok = cur.tok[j];
-                if (tok == kNoPos) {
-                    tok = -1;
-                } else if ((unsigned)tok >= (unsigned)p.V) {
-                    atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_TOKEN_RANGE);
-                    tok = -1;
-                }
-                m.tok[j * kWarp + lane] = tok;
-            }
+            for (int j = 0; j < kTileM / kWarp; ++j) m.tok[j * kWarp + lane] = unit_token(p, cur.tok[j]);
             if (p.sparse_width) {
                 // the sparse pair's column block of each row: the cluster's rank in its top-K
                 __syncwarp();   // every lane's row entries are written
@@ -274,6 +406,10 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                 m.nvalid = nvalid;
                 m.local0 = p0 - cur.lo;
                 m.p0 = p.packed ? g0 : p0;
+                if (PAIR) {
+                    m.g1 = 0;
+                    m.nvalid1 = 0;
+                }
             }
             __syncwarp();
             if (lane == 0) {
@@ -284,6 +420,7 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
             if (n < p.nmax) break;   // the bucket ended in this block
         }
     }
+    if (PAIR && have_pend && !publish_joint(p, meta, mfull0, mempty0, u, lane, pend, nullptr)) return false;
     // end of stream
     const int um = u % kMeta;
     int ok = 1;
@@ -309,6 +446,7 @@ __device__ void drain_loads(const Params &p, uint32_t full0, uint32_t issued, in
         mbar_wait(full0 + 8u * (q % S), (q / S) & 1u, kWaitNs);
 }
 
+template <bool PAIR>
 __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtensorMap *tmap_e,
                             const CUtensorMap *tmap_h, uint8_t *a_smem, uint8_t *b_smem, uint32_t full0,
                             uint32_t empty0, uint32_t mfull0, uint32_t mempty0, int lane)
@@ -338,22 +476,26 @@ __device__ bool issue_loads(const Params &p, const UnitMeta *meta, const CUtenso
         __syncwarp();
         if (lane == 0) mbar_arrive(mempty0 + 8u * um);   // the entry is in registers now
         const bool has_a = 4 * lane < nvalid;
-        const uint32_t a_tx = p.packed ? (uint32_t)nvalid * kRowBytes
+        const int nvalid1 = PAIR ? m.nvalid1 : 0, g1 = PAIR ? m.g1 : 0;
+        const uint32_t a_tx = p.packed ? (uint32_t)(nvalid + nvalid1) * kRowBytes
                                        : (uint32_t)((nvalid + 3) / 4) * 4 * kRowBytes;
         // packed: rows [pp0, pp0 + nvalid) of the padded table, pp0 = 32*g0 (the cluster's
         // padding rows are not read; the tile rows past nvalid keep stale data, which only
         // reaches accumulator rows the epilogue skips); the run is in block pp0/128 from
         // row pp0%128 on, and continues at row 0 of the next block if it crosses the
-        // block's end (lane 0 copies the first part, lane 1 the rest)
-        const int prow0 = g0 * kPackRows, nrows = nvalid;
+        // block's end.  A paired unit's second chunk is a second run into tile rows 64..
+        // Lanes 0-1 copy the two parts of the first run, lanes 2-3 those of the second.
+        const int run = PAIR ? lane >> 1 : 0, piece = lane & 1;
+        const int prow0 = (run ? g1 : g0) * kPackRows, nrows = run ? nvalid1 : nvalid;
         const int blk0 = prow0 / kPackSuper, r0 = prow0 % kPackSuper;
         const int first = min(nrows, kPackSuper - r0);
-        const bool has_pk = lane == 0 || (lane == 1 && nrows > first);
-        const uint32_t pk_bytes = (uint32_t)(lane == 0 ? first : nrows - first) * kRowBytes;
-        const uint32_t pk_dst_off = lane == 0 ? 0u : (uint32_t)first * kRowBytes;
-        const uint8_t *pk_src = p.packed ? p.packed + (size_t)(blk0 + lane) * p.num_kb * kPackBlock +
-                                               (lane == 0 ? (size_t)r0 * kRowBytes : 0)
-                                         : nullptr;
+        const bool has_pk = lane < (PAIR ? 4 : 2) && nrows > 0 && (piece == 0 || nrows > first);
+        const uint32_t pk_bytes = (uint32_t)(piece == 0 ? first : nrows - first) * kRowBytes;
+        const uint32_t pk_dst_off =
+            (run ? (uint32_t)(kTileM / 2) * kRowBytes : 0u) + (piece == 0 ? 0u : (uint32_t)first * kRowBytes);
+        const uint8_t *pk_src = p.packed && has_pk ? p.packed + (size_t)(blk0 + piece) * p.num_kb * kPackBlock +
+                                                         (piece == 0 ? (size_t)r0 * kRowBytes : 0)
+                                                   : nullptr;
         const uint32_t tx = a_tx + (n <= kGatherRowsMax ? (uint32_t)((n + 3) / 4) * 4 * kRowBytes : 0u);
         for (int kb = 0; kb < p.num_kb; ++kb) {
             int wok = 1;
@@ -506,7 +648,7 @@ __device__ bool load_b(const Params &p, const UnitMeta *meta, uint8_t *b_smem, u
     return ok;
 }
 
-template <bool SCATTER>
+template <bool SCATTER, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 3)
     k_gather_tc(const __grid_constant__ CUtensorMap tmap_e, const __grid_constant__ CUtensorMap tmap_h,
                 const Params p)
@@ -562,9 +704,9 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint32_t acc_cols = p.tmem_cols / kAcc;
 
     if (warp == 4) {
-        if (!publish_units(p, meta, mfull0, mempty0, lane) && lane == 0) timeout(p);
+        if (!publish_units<PAIR>(p, meta, mfull0, mempty0, lane) && lane == 0) timeout(p);
     } else if (warp == 6) {
-        if (!issue_loads(p, meta, &tmap_e, &tmap_h, a_smem, b_smem, full0, empty0, mfull0, mempty0, lane) &&
+        if (!issue_loads<PAIR>(p, meta, &tmap_e, &tmap_h, a_smem, b_smem, full0, empty0, mfull0, mempty0, lane) &&
             lane == 0)
             timeout(p);
     } else if (warp >= 7) {
@@ -644,39 +786,68 @@ __global__ void __launch_bounds__(kThreads, 3)
             tc_fence_after();
             const int t = warp * kWarp + lane;
             const int tok = m.tok[t];
+            // the bucket rows that belong to this candidate's chunk (both in an unpaired unit)
+            const uint8_t hbit = t >= kTileM / 2 ? 2 : 1;
             const uint32_t trow = tmem_base + ((uint32_t)(warp * kWarp) << 16) + (uint32_t)acc * acc_cols;
             for (int c0 = 0; c0 < m.npad; c0 += 16) {
                 uint32_t r[16];
                 tmem_load_16(trow + (uint32_t)c0, r);
                 tmem_wait_load();
+                if constexpr (!SCATTER) {
+                    // argmax: the warp's best (logit, lower id) key of each column (bucket
+                    // row) over its 32 candidates, 8 columns at a time, by a reduce-scatter
+                    // butterfly: at each step a lane keeps half of its columns and takes its
+                    // partner's copies of them, so after three steps the four lanes 4c..4c+3
+                    // hold column c's maximum over 8 lanes each, and two more exchanges
+                    // complete it; lane 4c folds it into the row's shared maximum
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = c0 + j;
-                    if (col >= n) break;
-                    const float v = p.bf16_logits ? round_bf16(__uint_as_float(r[j])) : __uint_as_float(r[j]);
-                    const int row = m.rows[col];
-                    if (SCATTER) {
-                        if (tok >= 0) {
-                            if (p.sparse_width) {
-                                const int rank = m.ranks[col];
-                                if (rank >= 0) {
-                                    const size_t o = (size_t)row * p.sparse_width + (size_t)rank * p.S +
-                                                     (size_t)(m.local0 + t);
-                                    p.out_logits[o] = v;
-                                    if (p.out_ids) p.out_ids[o] = tok;
-                                }
-                            } else {
-                                p.out_logits[(size_t)row * p.V + tok] = v;
+                    for (int h8 = 0; h8 < 16; h8 += 8) {
+                        unsigned long long k[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int col = c0 + h8 + j;
+                            const float v = p.bf16_logits ? round_bf16(__uint_as_float(r[h8 + j]))
+                                                          : __uint_as_float(r[h8 + j]);
+                            k[j] = (col < n && tok >= 0 && (!PAIR || (m.half[col] & hbit))) ? argmax_key(v, tok) : 0ull;
+                        }
+#pragma unroll
+                        for (int h = 4, o = 16; h >= 1; h >>= 1, o >>= 1) {
+                            const bool up = (lane & o) != 0;
+#pragma unroll
+                            for (int i = 0; i < h; ++i) {
+                                const unsigned long long send = up ? k[i] : k[i + h];
+                                const unsigned long long keep = up ? k[i + h] : k[i];
+                                const unsigned long long recv = __shfl_xor_sync(0xffffffffu, send, o);
+                                k[i] = keep > recv ? keep : recv;
                             }
                         }
-                    } else {
-                        unsigned long long key = tok >= 0 ? argmax_key(v, tok) : 0ull;
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-                            key = other > key ? other : key;
+                        for (int o = 2; o >= 1; o >>= 1) {
+                            const unsigned long long other = __shfl_xor_sync(0xffffffffu, k[0], o);
+                            k[0] = k[0] > other ? k[0] : other;
                         }
-                        if (lane == 0 && key) atomicMax(best + row, key);
+                        const int col = c0 + h8 + (((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1));
+                        if (!(lane & 3) && col < n && k[0]) atomicMax(best + m.rows[col], k[0]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = c0 + j;
+                        if (col >= n) break;
+                        if (tok < 0 || (PAIR && !(m.half[col] & hbit))) continue;
+                        const float v = p.bf16_logits ? round_bf16(__uint_as_float(r[j])) : __uint_as_float(r[j]);
+                        const int row = m.rows[col];
+                        if (p.sparse_width) {
+                            const int rank = m.ranks[col];
+                            if (rank >= 0) {
+                                const size_t o = (size_t)row * p.sparse_width + (size_t)rank * p.S +
+                                                 (size_t)(m.local0 + t);
+                                p.out_logits[o] = v;
+                                if (p.out_ids) p.out_ids[o] = tok;
+                            }
+                        } else {
+                            p.out_logits[(size_t)row * p.V + tok] = v;
+                        }
                     }
                 }
             }
@@ -699,24 +870,25 @@ __global__ void __launch_bounds__(kThreads, 3)
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
-    if (SCATTER) return;
-    for (int b = threadIdx.x; b < p.B; b += kThreads) {
-        const unsigned long long k = best[b];
-        if (k) atomicMax(p.keys + b, k);
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(p.ctrl + kCtrlTicket, 1u) == gridDim.x - 1);
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    for (int b = threadIdx.x; b < p.B; b += kThreads) {
-        const unsigned long long k = atomicAdd(p.keys + b, 0ull);
-        int32_t tok;
-        float v;
-        decode_argmax_key(k, &tok, &v);
-        p.out_tokens[b] = tok;
-        if (p.out_max) p.out_max[b] = v;
+    if constexpr (!SCATTER) {
+        for (int b = threadIdx.x; b < p.B; b += kThreads) {
+            const unsigned long long k = best[b];
+            if (k) atomicMax(p.keys + b, k);
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = (atomicAdd(p.ctrl + kCtrlTicket, 1u) == gridDim.x - 1);
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        for (int b = threadIdx.x; b < p.B; b += kThreads) {
+            const unsigned long long k = atomicAdd(p.keys + b, 0ull);
+            int32_t tok;
+            float v;
+            decode_argmax_key(k, &tok, &v);
+            p.out_tokens[b] = tok;
+            if (p.out_max) p.out_max[b] = v;
+        }
     }
 }
 
@@ -839,12 +1011,22 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     if ((long long)g.B * g.K <= 2LL * g.C) p.nmax = std::min(p.nmax, 32);
     // the A stage holds the chunk: 32, 64 or 128 rows
     const int a_rows = p.chunk <= 32 ? 32 : p.chunk <= 64 ? 64 : kTileM;
+    // With 128-row tiles and the packed table, two chunks of at most 64 candidates may
+    // share a unit (not for the sparse pair, whose column blocks follow one cluster per
+    // unit).  Pairing is compiled into its own kernel and chosen only where clusters
+    // average at most 64 positions: with larger clusters short chunks are rare, and the
+    // pairing's per-item work and registers measured ~2% slower on 128-position clusters.
+    const bool pair = g.packed && a_rows == kTileM && !g.sparse_width && 2LL * g.V <= (long long)kTileM * g.C;
     p.a_bytes = (uint32_t)a_rows * kRowBytes;
     p.b_bytes = (uint32_t)p.nmax * kRowBytes;
     uint32_t cols = 32;
     while (cols < (uint32_t)kAcc * (uint32_t)p.nmax) cols <<= 1;
     p.tmem_cols = cols;
-    const void *kfn = scatter ? (const void *)k_gather_tc<true> : (const void *)k_gather_tc<false>;
+    auto kernel = [&]() {
+        if (scatter) return pair ? k_gather_tc<true, true> : k_gather_tc<true, false>;
+        return pair ? k_gather_tc<false, true> : k_gather_tc<false, false>;
+    }();
+    const void *kfn = (const void *)kernel;
     auto fit_stages = [&](size_t budget) {
         int st = kMaxStages;
         while (st > 2 && smem_bytes(p, st) > budget) --st;
@@ -879,8 +1061,7 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     cudaError_t e = allow_smem(kfn, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(per_sm * sm_count()));
-    if (scatter) return launch_dependent(k_gather_tc<true>, grid, dim3(kThreads), smem, s, map_e, map_h, p);
-    return launch_dependent(k_gather_tc<false>, grid, dim3(kThreads), smem, s, map_e, map_h, p);
+    return launch_dependent(kernel, grid, dim3(kThreads), smem, s, map_e, map_h, p);
 }
 
 // ---------------------------------------------------------------------------

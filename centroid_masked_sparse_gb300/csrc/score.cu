@@ -156,23 +156,35 @@ __device__ __forceinline__ void load_item(const GatherParams &p, int2 item, bool
     if (lane < p.W) m.mask = __ldcg(p.rowmask + (size_t)item.x * p.W + lane);
 }
 
-// Producer warp: walks the items of this CTA (CTA j takes items j, j + G, j + 2G, ...
-// for a grid of G CTAs; items are chunks of randomly chosen clusters, so the
-// interleaved split is balanced and needs no atomic hand-out) and publishes, per
+// The next item of a CTA after item it.  Uniform clusters make equal items, so CTA j
+// takes j, j + G, j + 2G, ... (an even split without atomics; a hand-out by atomics
+// measured slower there).  Ragged clusters make items of unequal cost: after its
+// first item a CTA takes a ticket on the call's item counter (cleared with the other
+// control words by the projection), so CTAs that finish early take more.
+__device__ __forceinline__ int next_item(const GatherParams &p, int it, int lane)
+{
+    if (p.offsets == nullptr) return it + (int)gridDim.x;
+    int nx = 0;
+    if (lane == 0) nx = (int)gridDim.x + (int)atomicAdd(p.ctrl + kCtrlNext, 1u);
+    return __shfl_sync(0xffffffffu, nx, 0);
+}
+
+// Producer warp: walks the items of this CTA (item blockIdx.x, then next_item's) and
+// publishes, per
 // row group, the hidden rows into an h buffer and one ring slot per candidate
 // position (each lane issues its own slot's bulk copy).  The item records and
 // their metadata are loaded two and one items ahead.  False after a timed-out wait.
 __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int consumers)
 {
     const uint32_t rb = (uint32_t)p.H * 2;
-    const int G = (int)gridDim.x;
-    int it1 = (int)blockIdx.x, it2 = it1 + G;
+    int it1 = (int)blockIdx.x;
     const int2 invalid_item = make_int2(-1, 0);
     // the first two item records are loaded together with the item count, not after it
     // (both slots lie inside the list; a record past the count is dropped)
     const int2 rec0 = it1 < p.items_cap ? p.items[it1] : invalid_item;
-    const int2 rec1 = it2 < p.items_cap ? p.items[it2] : invalid_item;
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
+    int it2 = next_item(p, it1, lane);
+    const int2 rec1 = it2 < p.items_cap ? p.items[it2] : invalid_item;
     const uint64_t pol = l2_policy_evict_first();
     const int step = p.step;
     const uint32_t ring = (uint32_t)p.ring;
@@ -185,7 +197,7 @@ __device__ bool produce(const GatherParams &p, const Smem &sm, int lane, int con
         const ItemMeta cur = nxt;
         if (!cur.valid) break;
         load_item(p, rec2, it2 < n_items, lane, nxt);
-        it2 += G;
+        if (it2 < n_items) it2 = next_item(p, it2, lane);
         rec2 = it2 < n_items ? p.items[it2] : invalid_item;
         if (cur.nvalid == 0) continue;
         // the bucket's batch rows, in row order
