@@ -125,6 +125,7 @@ struct Params {
     const uint8_t *packed;    // packed table blocks, or null (token-order gathers)
     const int32_t *poff;      // its padded cluster offsets [C+1]
     int nmax;       // bucket rows per unit (multiple of 16, <= kMaxN)
+    int handout;    // items past the first round by ticket (large buckets), else round-robin
     int num_kb;
     int stages;
     uint32_t a_bytes, b_bytes;   // stage sizes
@@ -299,14 +300,18 @@ __device__ bool publish_joint(const Params &p, UnitMeta *meta, uint32_t mfull0, 
     return true;
 }
 
-// The next item a CTA takes after its first: a ticket on the call's item counter
-// (cleared with the other control words by the projection), offset by the grid, so
-// every item past the first round goes to whichever CTA asks first.  Items differ in
-// cost (a large bucket is several units), so CTAs that finish early take more.  The
-// ticket is taken when the item is about to be needed (taking it earlier, to hide the
-// atomic's round trip, measured worse: it leaves fewer items to even out the tail).
-__device__ __forceinline__ int grab_item(const Params &p, int lane)
+// The item a CTA takes after item `prev`.  With large buckets (p.handout): a ticket on
+// the call's item counter (cleared with the other control words by the projection),
+// offset by the grid, so every item past the first round goes to whichever CTA asks
+// first; such items differ in cost (a large bucket is several units), so CTAs that
+// finish early take more.  The ticket is taken when the item is about to be needed
+// (taking it earlier, to hide the atomic's round trip, measured worse: it leaves fewer
+// items to even out the tail).  Otherwise every item is about one unit and the CTAs
+// take items prev + G, prev + 2G, ... with no atomic (with tickets, every CTA asking at
+// once, the launch took 88.9 instead of 82.9 us on uniform clusters at B=64).
+__device__ __forceinline__ int grab_item(const Params &p, int prev, int lane)
 {
+    if (!p.handout) return prev + (int)gridDim.x;
     int it = 0;
     if (lane == 0) it = (int)gridDim.x + (int)atomicAdd(p.ctrl + kCtrlNext, 1u);
     return __shfl_sync(0xffffffffu, it, 0);
@@ -326,7 +331,7 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
     // ticket for the second item is taken while both are in flight
     const int2 rec0 = it < p.items_cap ? p.items[it] : none;
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
-    int it1 = grab_item(p, lane);
+    int it1 = grab_item(p, it, lane);
     const int2 rec1 = it1 < p.items_cap ? p.items[it1] : none;
     const long long packed_groups = p.packed ? __ldg(p.poff + p.C) / kPackRows : 0;
     int u = 0;
@@ -335,8 +340,8 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
     int2 rec2 = it1 < n_items ? rec1 : none;
     ShortChunk pend{};         // a chunk of at most 64 candidates waiting for a partner
     bool have_pend = false;
-    int it2 = it1 < n_items ? grab_item(p, lane) : n_items;   // the item after it1
-    for (; it < n_items; it = it1, it1 = it2, it2 = it2 < n_items ? grab_item(p, lane) : n_items) {
+    int it2 = it1 < n_items ? grab_item(p, it1, lane) : n_items;   // the item after it1
+    for (; it < n_items; it = it1, it1 = it2, it2 = it2 < n_items ? grab_item(p, it2, lane) : n_items) {
         const ItemPre cur = nxt;
         load_item(p, rec2, it1 < n_items, lane, nxt);
         rec2 = it2 < n_items ? p.items[it2] : none;
@@ -1017,6 +1022,7 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     // average at most 64 positions: with larger clusters short chunks are rare, and the
     // pairing's per-item work and registers measured ~2% slower on 128-position clusters.
     const bool pair = g.packed && a_rows == kTileM && !g.sparse_width && 2LL * g.V <= (long long)kTileM * g.C;
+    p.handout = (long long)g.B * g.K >= 4LL * g.C ? 1 : 0;
     p.a_bytes = (uint32_t)a_rows * kRowBytes;
     p.b_bytes = (uint32_t)p.nmax * kRowBytes;
     uint32_t cols = 32;

@@ -321,9 +321,15 @@ int choose_chunk(const mtp_head_desc *d, int B)
     return ch;
 }
 
+// Hidden sizes whose 512-byte (or smaller) rows make per-row costs weigh most.
+constexpr int kSmallHidden = 256;
+
 // Which gather a call runs.  The tensor-core gather takes calls whose buckets are
-// large (B*K >= 4C), where one candidate tile serves a whole bucket.  With the
-// packed embedding table it also takes calls with fewer (row, cluster) pairs: its
+// large (B*K >= 4C), where one candidate tile serves a whole bucket, and at
+// H <= 256 calls from B*K >= C/4 on the token-order table too (its gathered tiles
+// against the CUDA-core gather's row copies, measured on GB300 at H=256: B=64 52.3
+// vs 93.9 us, B=16 33.2 vs 47.4 us; at H=1536 the CUDA-core gather stays ahead).
+// With the packed embedding table it also takes calls with fewer (row, cluster) pairs: its
 // block copies stream HBM faster than the CUDA-core gather's row copies and read
 // no padding rows.  Running two or three CTAs per SM, it is ahead (measured on
 // GB300) from B*K >= C/4 at H = 1536 and 2560 (behind at C/8) and from B*K >= C/16
@@ -337,7 +343,7 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
     const long long C = d->num_centroids;
     const bool large = pairs >= (long long)kTcGatherMinReuse * C;
     const bool packed_reuse =
-        d->embed_packed && (4 * pairs >= C || (d->hidden_size <= 256 && 16 * pairs >= C));
+        d->embed_packed && (4 * pairs >= C || (d->hidden_size <= kSmallHidden && 16 * pairs >= C));
     if (d->embed_packed && (large || packed_reuse)) {
         const double avg = (double)d->vocab_size / d->num_centroids;
         const double clusters = (double)std::min<long long>(pairs, d->num_centroids);
@@ -346,7 +352,7 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
         *chunk = ch;
         return true;
     }
-    if (large) {
+    if (large || (d->hidden_size <= kSmallHidden && 4 * pairs >= C)) {
         *chunk = kTcGatherChunk;
         return true;
     }
@@ -362,7 +368,8 @@ std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 std::atomic<int> g_stall_test{0};
 
 // Batches that run the fused top-K + gather kernel (select_gather.cu) behind the
-// projection instead of the top-K kernel and a gather.
+// projection instead of the top-K kernel and a gather, for hidden sizes above
+// kSmallHidden; at or below it the same batches take the direct gather.
 constexpr int kFusedMaxBatch = 8;
 
 // Whether a gather kernel can run a masked call of this shape.
@@ -381,9 +388,13 @@ bool gather_can_run(const mtp_head_desc *d, int B, bool sparse, GatherKind k)
 // fused kernel, which selects each row's top-K in the gather CTAs themselves.  The
 // direct CUDA-core gather (each warp loads candidate rows straight into registers; no
 // producer, ring or hand-off, so its latency chain is short) takes up to 12 rows
-// where the tensor-core gather would not run.  Measured on GB300 against the
-// alternatives: uniform clusters B=12 ~46 vs ~47.5 us (pipelined), B=16 ~56.5 vs
-// ~54.5 us (tensor cores); H=256 B=16 38.5 vs 32.4 us (tensor cores).  The sparse
+// where the tensor-core gather would not run, and the fused kernel's batches at
+// H <= 256, whose 512-byte rows make the fused kernel's row stream (every row's
+// candidates, no dedup) the slower one.  Measured on GB300 against the alternatives:
+// uniform clusters B=12 ~46 vs ~47.5 us (pipelined), B=16 ~56.5 vs ~54.5 us (tensor
+// cores); H=256 B=16 38.5 vs 32.4 us (tensor cores); H=256 with the packed table,
+// direct against fused (and tensor cores): B=1 18.1 vs 19.2, B=2 18.3 vs 19.9, B=4
+// 21.1 vs 20.4, B=6 22.8 vs 26.6 (24.4), B=8 24.7 vs 26.9 (26.9) us.  The sparse
 // pair keeps the pipelined and tensor-core gathers.  A kind forced by
 // mtp_force_gather that cannot run the call gives kGatherNone.
 GatherKind gather_kind(const mtp_head_desc *d, int B, bool sparse, int *chunk)
@@ -395,8 +406,11 @@ GatherKind gather_kind(const mtp_head_desc *d, int B, bool sparse, int *chunk)
     if (forced >= 0) {
         k = (GatherKind)forced;
         if (!gather_can_run(d, B, sparse, k)) return kGatherNone;
-    } else if (!sparse && B <= kFusedMaxBatch && gather_can_run(d, B, sparse, kGatherFused)) {
+    } else if (!sparse && B <= kFusedMaxBatch && d->hidden_size > kSmallHidden &&
+               gather_can_run(d, B, sparse, kGatherFused)) {
         k = kGatherFused;
+    } else if (!sparse && B <= kFusedMaxBatch && gather_can_run(d, B, sparse, kGatherDirect)) {
+        k = kGatherDirect;
     } else if (!sparse && !tc && B <= 12) {
         k = kGatherDirect;
     } else {

@@ -200,11 +200,16 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 65) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 128) == 1
-    d = _desc(H=256)                                         # small hidden size: from B*K >= C/16
+    d = _desc(H=256)                                         # small hidden size, token order:
+    assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1       # tensor cores from B*K >= C/4
+    assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 15) == 0
+    d = _desc(H=256)                                         # and packed: from B*K >= C/16
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 9) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 3       # up to 8 rows the fused kernel
-    assert L.mtp_gather_plan(ctypes.byref(d), 3) == 3
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2       # up to 8 rows of 512 bytes: direct
+    assert L.mtp_gather_plan(ctypes.byref(d), 3) == 2
+    assert L.mtp_gather_plan(ctypes.byref(_desc(H=512)), 8) == 3   # above H=256: fused
     d = _desc(offsets=0x5000)                                # ragged clusters: the same rules
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
     d.embed_packed = 0xA000

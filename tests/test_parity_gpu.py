@@ -485,25 +485,34 @@ def test_every_gather_kernel_small_batches(build_lib, B, kind):
 
 @pytest.mark.parametrize("name,B", [("variable", 1), ("variable", 8), ("shared", 8), ("draft256", 4)])
 def test_fused_kernel_other_workloads(build_lib, name, B):
-    """The fused kernel (every batch of at most 8 rows) on lognormal clusters, on K=128 of
-    4096 small clusters and at H=256, both finishes, against the oracle."""
+    """The fused kernel on lognormal clusters, on K=128 of 4096 small clusters and at H=256
+    (where the library runs the direct gather instead, so the kernel is forced), both
+    finishes, against the oracle."""
     m = build_lib
     oh, dh = device_head(m, name)
-    assert m.mtp_gather_plan(dh, B) == "fused"
-    hidden, ref = check_topk(m, name, B, row0=6100)
-    sc = m.mtp_masked_scatter_logits(dh, helpers.bf16_tensor(hidden))
-    torch.cuda.synchronize()
+    small_h = oh.H <= 256
+    assert m.mtp_gather_plan(dh, B) == ("cuda_core_direct" if small_h else "fused")
+    if small_h:
+        m.mtp_force_gather("fused")
+    try:
+        assert m.mtp_gather_plan(dh, B) == "fused"
+        hidden, ref = check_topk(m, name, B, row0=6100)
+        sc = m.mtp_masked_scatter_logits(dh, helpers.bf16_tensor(hidden))
+        torch.cuda.synchronize()
+    finally:
+        m.mtp_force_gather(None)
     helpers.assert_close(sc.cpu().numpy(), oracle.masked_scatter_logits(oh, hidden), f"fused {name} scatter")
 
 
 @pytest.mark.parametrize("K", [1024, 1025])
 def test_fused_kernel_at_its_k_limit(build_lib, K):
     """K up to 1024 selections per row run the fused kernel (here K of C = 1100 centroids,
-    most of the vocabulary a candidate); one more falls back to the direct gather."""
+    most of the vocabulary a candidate; H = 512, above the sizes that take the direct
+    gather instead); one more falls back to the direct gather."""
     m = build_lib
-    t, oh, dh = _custom(m, 1100 * 8, 64, 1100, K, seed=K)
+    t, oh, dh = _custom(m, 1100 * 8, 512, 1100, K, seed=K)
     assert m.mtp_gather_plan(dh, 3) == ("fused" if K <= 1024 else "cuda_core_direct")
-    hidden = synth.random_hidden(3, 64, K + 1)
+    hidden = synth.random_hidden(3, 512, K + 1)
     _full_check(m, oh, dh, hidden, f"K={K}")
 
 
