@@ -317,9 +317,14 @@ __device__ __forceinline__ int grab_item(const Params &p, int prev, int lane)
     return __shfl_sync(0xffffffffu, it, 0);
 }
 
-// Metadata warp: publishes the units of this CTA's items (item blockIdx.x, then the
-// items it grabs; item records two items ahead, their loads one item ahead), pairing
-// short chunks where the call allows it, then an end-of-stream entry.  False after a
+// Metadata warp: publishes the units of this CTA's items, pairing short chunks where the
+// call allows it, then an end-of-stream entry.  Round-robin (item blockIdx.x, then + G,
+// + 2G, ...): item records two items ahead, their loads one item ahead.  Ticketed
+// (p.handout): the CTA claims its next item only once the units before the current
+// item's are consumed, so it holds at most one item beyond the one in flight; the
+// claim, its record and its loads (~2 us) overlap the current item's units.  (Claiming
+// as far ahead as the 8-entry metadata ring allowed left CTAs with 2 to 5 units of the
+// shared-centroid workload, the slowest ~30 us behind the fastest.)  False after a
 // timed-out wait.
 template <bool PAIR>
 __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, uint32_t mempty0, int lane)
@@ -327,31 +332,22 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
     const int2 none = make_int2(-1, 0);
     int it = blockIdx.x;
     // this CTA's first item record is loaded together with the item count, not after it
-    // (the slot lies inside the list; a record past the count is dropped), and the
-    // ticket for the second item is taken while both are in flight
+    // (the slot lies inside the list; a record past the count is dropped)
     const int2 rec0 = it < p.items_cap ? p.items[it] : none;
     const int n_items = (int)min(p.ctrl[kCtrlItems], (uint32_t)p.items_cap);
-    int it1 = grab_item(p, it, lane);
-    const int2 rec1 = it1 < p.items_cap ? p.items[it1] : none;
     const long long packed_groups = p.packed ? __ldg(p.poff + p.C) / kPackRows : 0;
     int u = 0;
-    ItemPre nxt;
-    load_item(p, it < n_items ? rec0 : none, it < n_items, lane, nxt);
-    int2 rec2 = it1 < n_items ? rec1 : none;
     ShortChunk pend{};         // a chunk of at most 64 candidates waiting for a partner
     bool have_pend = false;
-    int it2 = it1 < n_items ? grab_item(p, it1, lane) : n_items;   // the item after it1
-    for (; it < n_items; it = it1, it1 = it2, it2 = it2 < n_items ? grab_item(p, it2, lane) : n_items) {
-        const ItemPre cur = nxt;
-        load_item(p, rec2, it1 < n_items, lane, nxt);
-        rec2 = it2 < n_items ? p.items[it2] : none;
-        if (!cur.valid) continue;
+    // publishes the units of one item (or holds a short chunk for a partner)
+    auto publish_item = [&](const ItemPre &cur) -> bool {
+        if (!cur.valid) return true;
         const int nvalid = cur.nvalid, p0 = cur.p0, g0 = cur.g0;
         // a chunk reaching past the packed table's last group (a table packed from other
         // offsets) is skipped and flagged instead of read
         if (p.packed && (long long)g0 + (nvalid + kPackRows - 1) / kPackRows > packed_groups) {
             if (lane == 0) atomicOr(p.ctrl + kCtrlError, MTP_DEVERR_OFFSETS);
-            continue;
+            return true;
         }
         if (PAIR) {
             // two chunks of at most 64 candidates whose buckets together fit a unit share
@@ -361,7 +357,7 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                 if (!have_pend) {
                     pend = sc;
                     have_pend = true;
-                    continue;
+                    return true;
                 }
                 const bool fits = warp_count(pend.w | sc.w) <= p.nmax;
                 if (!publish_joint(p, meta, mfull0, mempty0, u, lane, pend, fits ? &sc : nullptr)) return false;
@@ -370,7 +366,7 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
                 } else {
                     pend = sc;
                 }
-                continue;
+                return true;
             }
             if (have_pend) {
                 if (!publish_joint(p, meta, mfull0, mempty0, u, lane, pend, nullptr)) return false;
@@ -423,6 +419,35 @@ __device__ bool publish_units(const Params &p, UnitMeta *meta, uint32_t mfull0, 
             }
             ++u;
             if (n < p.nmax) break;   // the bucket ended in this block
+        }
+        return true;
+    };
+    if (p.handout) {
+        ItemPre cur;
+        load_item(p, it < n_items ? rec0 : none, it < n_items, lane, cur);
+        while (it < n_items) {
+            const int u0 = u;
+            if (!publish_item(cur)) return false;
+            // the units before this item's are consumed (unit u0 - 1's slot is not reused
+            // before unit u0 - 1 + kMeta, so its phase is unambiguous)
+            if (u0 > 0 && u > u0 && u - u0 < kMeta &&
+                !mbar_wait(mempty0 + 8u * ((u0 - 1) % kMeta), (uint32_t)((u0 - 1) / kMeta) & 1u, kWaitNs))
+                return false;
+            it = grab_item(p, it, lane);
+            load_item(p, it < n_items ? p.items[it] : none, it < n_items, lane, cur);
+        }
+    } else {
+        int it1 = grab_item(p, it, lane);
+        const int2 rec1 = it1 < p.items_cap ? p.items[it1] : none;
+        ItemPre nxt;
+        load_item(p, it < n_items ? rec0 : none, it < n_items, lane, nxt);
+        int2 rec2 = it1 < n_items ? rec1 : none;
+        int it2 = it1 < n_items ? grab_item(p, it1, lane) : n_items;   // the item after it1
+        for (; it < n_items; it = it1, it1 = it2, it2 = it2 < n_items ? grab_item(p, it2, lane) : n_items) {
+            const ItemPre cur = nxt;
+            load_item(p, rec2, it1 < n_items, lane, nxt);
+            rec2 = it2 < n_items ? p.items[it2] : none;
+            if (!publish_item(cur)) return false;
         }
     }
     if (PAIR && have_pend && !publish_joint(p, meta, mfull0, mempty0, u, lane, pend, nullptr)) return false;
