@@ -326,7 +326,7 @@ def measure_masked(ctx, t, dh, name, B, steps, warmup, scatter=False, rot=4, row
 def measure_graph(ctx, t, dh, name, B, steps, warmup, rot=4, row0=0):
     """µs per call replaying a CUDA graph of the call (the batch copied into the graph's
     static input inside the timed region), on a side stream: the legacy stream cannot be
-    captured."""
+    captured.  Medians: the loops are short, and one host stall would dominate a mean."""
     torch, m, synth, timer = ctx["torch"], ctx["m"], ctx["synth"], ctx["timer"]
     hb = make_batches(synth, t, name, B, rot, row0)
     hs = [torch.from_numpy(h.view(np.int16)).to(ctx["device"]).view(torch.bfloat16) for h in hb]
@@ -344,7 +344,7 @@ def measure_graph(ctx, t, dh, name, B, steps, warmup, rot=4, row0=0):
             gs.synchronize()
             g.close()
     torch.cuda.current_stream(ctx["device"]).wait_stream(gs)
-    return float(np.mean(call)), float(np.mean(bare)), err
+    return float(np.median(call)), float(np.median(bare)), err
 
 
 def measure_pair(ctx, t, dh, name, B, steps, warmup, rot=4, row0=0):
