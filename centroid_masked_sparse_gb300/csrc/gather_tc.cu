@@ -9,7 +9,11 @@
 // One unit = (work item, block of at most nmax bucket rows).  The candidate
 // embedding rows are the MMA's M side (one token per TMEM lane, M = 128 with the
 // lanes past the chunk ignored), the bucket's hidden rows its N side (padded to
-// a multiple of 16), K = H in 64-element blocks.  Operands reach shared memory
+// a multiple of 16), K = H in 64-element blocks.  With the packed table and
+// clusters of at most 64 positions on average, two chunks of at most 64
+// candidates whose buckets together fit share a unit (tile rows 0-63 and 64-127,
+// the union of the buckets as N; the epilogue keeps a pair only where the row
+// selected that candidate's cluster): a separate instantiation (PAIR).  Operands reach shared memory
 // by TMA in the 128-byte-swizzled layout the MMA descriptors expect:
 //   * with the packed embedding table (below) the chunk's candidate rows are one
 //     or two contiguous, pre-swizzled runs of a 16 KB block per k-block, fetched
@@ -29,17 +33,20 @@
 //
 // Warp roles per CTA (352 threads; two or three CTAs per SM where their TMEM and
 // shared memory fit, three with units of at most 32 bucket rows, else one):
-//   warp 4   metadata: walks this CTA's items and publishes each unit's token
-//            and row lists into a ring of kMeta entries, running ahead of the
-//            loads so that its dependent global reads (item record, row mask,
-//            token ids) never stall the stream;
+//   warp 4   metadata: walks this CTA's items (round-robin; with large buckets
+//            by ticket, the next item claimed once the previous one's units are
+//            consumed) and publishes each unit's token and row lists into a ring
+//            of kMeta entries, running ahead of the loads so that its dependent
+//            global reads (item record, row mask, token ids) never stall the
+//            stream;
 //   warp 6   TMA issue: per unit and k-block, one stage of A loads (and B for a
 //            small bucket);
 //   warps 7-10 B: the hidden rows of larger buckets, by cp.async (see load_b);
 //   warp 5   one thread issues tcgen05.mma (kind::f16, fp32 in TMEM, four
 //            accumulators so the epilogues of the last units overlap the next);
 //   warps 0-3 epilogue: tcgen05.ld of the unit's logits (thread = candidate),
-//            then the scatter store or the per-row argmax fold.
+//            then the scatter store or the per-row argmax fold (a reduce-scatter
+//            butterfly over the warp's candidates for each group of columns).
 // Every mbarrier wait is bounded and records MTP_DEVERR_TIMEOUT if it gives up.
 //
 // The packed table (its layout is specified with mtp_pack_embeddings in the C
