@@ -58,6 +58,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <climits>
 #include <mutex>
 #include <map>
@@ -1075,9 +1076,29 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     // single-thread MMA issue, TMA issue and barrier round trips cost a few hundred ns
     // per k-block, so more pipelines per SM let short chunks and small H reach the HBM
     // rate and keep SMs busy through the last round of units.
+    //
+    // The last round of units decides the end: when few CTAs are left with a unit each,
+    // each runs at its own pipeline's pace and HBM idles (at uniform B=16, ~459 units
+    // over 456 CTAs, three units ran alone for ~9 us).  With uniform clusters, one item
+    // per selected cluster and small buckets, the unit count is the number of distinct
+    // selected clusters, expected C(1 - (1 - K/C)^B) for independent rows; where three
+    // CTAs per SM would leave a thin last round and two would not, two run (measured on
+    // GB300: B=16 53.1 vs 55.3 us, B=20 57.7 vs 61.7 us per call; B=12, 24 and 64, where
+    // three leave a full last round, 47.1, 64.6 and 98.6 against 51.7, 68.3 and 101.5 us
+    // with two).  A misprediction (rows that share clusters) costs only speed.
+    int max_per_sm = 3;
+    if (!p.handout && g.offsets == nullptr && (long long)g.V <= (long long)p.chunk * g.C && p.nmax >= g.B) {
+        const double units = g.C * (1.0 - std::pow(1.0 - (double)g.K / g.C, (double)g.B));
+        auto thin_tail = [&](int n) {
+            const double rounds = units / ((double)n * sm_count());
+            const double frac = rounds - std::floor(rounds + 0.05);
+            return rounds >= 0.95 && frac > -0.05 && frac < 1.0 / 3.0;
+        };
+        if (thin_tail(3) && !thin_tail(2)) max_per_sm = 2;
+    }
     int per_sm = 1;
     int stages = fit_stages(220 * 1024);
-    for (int n = 3; n >= 2; --n) {
+    for (int n = max_per_sm; n >= 2; --n) {
         if ((uint32_t)n * p.tmem_cols > kSmTmemCols) continue;
         const int st = fit_stages((size_t)(220 / n) * 1024);
         if (st >= 3 && ctas_fit(kfn, smem_bytes(p, st), n)) {
