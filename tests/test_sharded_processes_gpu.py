@@ -67,7 +67,7 @@ def test_two_process_sharded_head_matches_the_oracle():
     t = helpers.tables(NAME)
     oh = oracle.Head.from_tables(t, synth.WORKLOADS[NAME].top_k)
     batches, refs = [], []
-    for B, row0 in ((8, 4100), (64, 4200)):   # the fused kernel and the pipelined gather per shard
+    for B, row0 in ((8, 4100), (64, 4200)):   # the direct and the tensor-core gather per shard (H=256)
         hidden, ref, _ = helpers.clean_batch(NAME, oh, B, row0=row0)
         batches.append(hidden)
         refs.append(ref)
