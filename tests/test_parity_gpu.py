@@ -765,12 +765,14 @@ def test_packed_table_parity(build_lib, H, B, sizes):
         dh.drop_packed_table()
 
 
-@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64), ("uniform", 32), ("uniform", 8),
-                                    ("variable", 64), ("variable", 32)])
+@pytest.mark.parametrize("name,B", [("shared", 256), ("uniform", 64), ("uniform", 32), ("uniform", 20),
+                                    ("uniform", 16), ("uniform", 8), ("variable", 64), ("variable", 32)])
 def test_packed_table_full_size(build_lib, name, B):
     """Full-size tables with the packed table: token ids match the oracle and the
     token-order path exactly, logits within the fp32 tolerance (the packed call may run
-    the tensor-core gather where the token-order call runs the CUDA-core one)."""
+    the tensor-core gather where the token-order call runs the CUDA-core one).  Uniform
+    B=16 and 20 run the tensor-core gather with two CTAs per SM (a full last round of
+    units), the other uniform batches with three."""
     m = build_lib
     oh, dh = device_head(m, name)
     hidden, ref, _ = helpers.clean_batch(name, oh, B)
