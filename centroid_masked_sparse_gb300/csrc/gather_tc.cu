@@ -618,7 +618,23 @@ __device__ bool load_b(const Params &p, const UnitMeta *meta, uint8_t *b_smem, u
     };
     for (int u = 0; ok; ++u) {
         const int um = u % kMeta;
-        if (!warp_wait(mfull0 + 8u * um, (uint32_t)(u / kMeta) & 1u)) {
+        const uint32_t mbar = mfull0 + 8u * um, mpar = (uint32_t)(u / kMeta) & 1u;
+        // The next unit may be published only once the unit before the last one is
+        // consumed (with the ticketed hand-out the metadata warp claims its next item
+        // then).  A unit of fewer k-blocks than the signal lag leaves stages of that
+        // earlier unit unsignalled here (more than num_kb stages owed: the last unit has
+        // num_kb, each with one copy group): settle those before blocking on the next
+        // unit, or their MMAs, and so the publication, could never complete.  (Units of
+        // more k-blocks than the lag have signalled their predecessors by now.)
+        if (filled - signalled > (uint32_t)p.num_kb) {
+            int ready = lane == 0 ? (int)mbar_test_wait(mbar, mpar) : 0;
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) {
+                cp_async_wait(p.num_kb);   // < b_lag groups: those of the last unit
+                while (filled - signalled > (uint32_t)p.num_kb) signal_one();
+            }
+        }
+        if (!warp_wait(mbar, mpar)) {
             ok = false;
             break;
         }

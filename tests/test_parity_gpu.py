@@ -1248,3 +1248,36 @@ def test_buckets_split_over_units(build_lib, B, K, C, packed):
     for b in range(B):
         np.testing.assert_array_equal(scn[b][pi[b]], pl[b])
     assert m.mtp_read_device_error(dh.workspace(B)) == 0
+
+
+@pytest.mark.parametrize("B", [64, 128])
+def test_tensor_core_gather_one_k_block_large_buckets(build_lib, B):
+    """H = 64: every unit of the tensor-core gather is one k-block, and B*K >= 4C makes the
+    item hand-out ticketed (the next item claimed once the previous one is consumed).  The
+    B warps must settle the stages they still owe a signal before they block on the next
+    unit, or the claim never comes (the call then ended in the bounded waits' timeout).
+    Argmax and sparse pair against the oracle, the device error word clear."""
+    m = build_lib
+    g = np.random.default_rng(300 + B)
+    V, C, H, K = 65536, 256, 64, 32
+    cw = synth.bf16_bits(g.integers(-8, 9, size=(C, H)).astype(np.float32))
+    ew = synth.bf16_bits(g.integers(-8, 9, size=(V, H)).astype(np.float32))
+    perm = g.permutation(V).astype(np.int32)
+    hid = synth.bf16_bits(g.integers(-16, 17, size=(B, H)).astype(np.float32))
+    oh = oracle.Head(cw, ew, perm, None, K)
+    dh = m.MaskedHead(helpers.bf16_tensor(cw), helpers.bf16_tensor(ew), torch.from_numpy(perm).cuda(), K)
+    assert m.mtp_gather_plan(dh, B) == "tensor_core"
+    h = helpers.bf16_tensor(hid)
+    tok, mx = m.mtp_masked_topk_tokens(dh, h)
+    torch.cuda.synchronize()
+    assert m.mtp_read_device_error(dh.workspace(B)) == 0
+    ref = oracle.masked_topk_tokens(oh, hid)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+    np.testing.assert_array_equal(mx.cpu().numpy(), ref["max_logit"].astype(np.float32))
+    plog, pids = m.mtp_select_and_score(dh, h)
+    torch.cuda.synchronize()
+    assert m.mtp_read_device_error(dh.workspace(B)) == 0
+    for b in range(0, B, 17):
+        rl, rt = oracle.select_and_score_row(oh, hid, b)
+        np.testing.assert_array_equal(pids[b].cpu().numpy(), rt)
+        np.testing.assert_array_equal(plog[b].cpu().numpy(), rl.astype(np.float32))
