@@ -216,13 +216,13 @@ class Timer:
         self.evict.sum()
 
     def before_call(self, flush):
-        """Outside the timed events: the L2 flush, or (warm figure) a ~25 us spin kernel,
+        """Outside the timed events: the L2 flush, or (warm figure) a ~100 us spin kernel,
         so that in both cases the GPU is busy while the host enqueues the call and the
         call's launches are queued before it starts (no host launch gap inside it)."""
         if flush:
             self.flush_l2()
         else:
-            self.torch.cuda._sleep(50000)
+            self.torch.cuda._sleep(200000)
 
     def events(self, n):
         torch = self.torch

@@ -1281,3 +1281,62 @@ def test_tensor_core_gather_one_k_block_large_buckets(build_lib, B):
         rl, rt = oracle.select_and_score_row(oh, hid, b)
         np.testing.assert_array_equal(pids[b].cpu().numpy(), rt)
         np.testing.assert_array_equal(plog[b].cpu().numpy(), rl.astype(np.float32))
+
+
+@pytest.mark.parametrize("V,C,H,K,B,packed,protos", [
+    (65536, 256, 128, 32, 128, False, 0),     # two k-blocks per unit, ticketed hand-out
+    (65536, 256, 192, 16, 64, True, 0),       # three k-blocks, packed table, ticketed
+    (32768, 512, 64, 64, 96, True, 0),        # 64-position clusters: paired short chunks, one k-block
+    (32768, 512, 256, 32, 40, True, 0),       # paired chunks, round-robin, 32-row units
+    (65536, 1024, 64, 16, 20, True, 0),       # paired chunks, tiny buckets, round-robin
+    (131072, 1024, 320, 8, 256, False, 4),    # five k-blocks; four prototypes x 64 rows: 64-row
+])                                            # buckets span two 32-row units
+def test_tensor_core_gather_shape_matrix(build_lib, V, C, H, K, B, packed, protos):
+    """Integer inputs (every sum exact, so bit-for-bit against the oracle) over shapes that
+    cross the tensor-core gather's switches: units of one to five k-blocks against the B
+    warps' signal lag, ticketed and round-robin hand-out, paired short chunks, bucket-row
+    caps of 16 to 64 rows and buckets spanning several units.  Argmax, scatter and sparse
+    pair; the device error word must stay clear (a stalled pipeline ends in a timeout)."""
+    m = build_lib
+    g = np.random.default_rng(V + C + H + K + B)
+    cw = synth.bf16_bits(g.integers(-8, 9, size=(C, H)).astype(np.float32))
+    ew = synth.bf16_bits(g.integers(-8, 9, size=(V, H)).astype(np.float32))
+    perm = g.permutation(V).astype(np.int32)
+    rows = g.integers(-16, 17, size=(protos or B, H)).astype(np.float32)
+    hid = synth.bf16_bits(np.repeat(rows, B // protos, axis=0) if protos else rows)
+    oh = oracle.Head(cw, ew, perm, None, K)
+    dh = m.MaskedHead(helpers.bf16_tensor(cw), helpers.bf16_tensor(ew), torch.from_numpy(perm).cuda(), K)
+    if packed:
+        dh.use_packed_table()
+    m.mtp_force_gather("tensor_core")
+    try:
+        h = helpers.bf16_tensor(hid)
+        tok, mx = m.mtp_masked_topk_tokens(dh, h)
+        torch.cuda.synchronize()
+        assert m.mtp_read_device_error(dh.workspace(B)) == 0
+        sc = m.mtp_masked_scatter_logits(dh, h)
+        torch.cuda.synchronize()
+        assert m.mtp_read_device_error(dh.workspace(B)) == 0
+        plog, pids = m.mtp_select_and_score(dh, h)
+        torch.cuda.synchronize()
+        assert m.mtp_read_device_error(dh.workspace(B)) == 0
+    finally:
+        m.mtp_force_gather(None)
+    ref = oracle.masked_topk_tokens(oh, hid)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref["tokens"])
+    np.testing.assert_array_equal(mx.cpu().numpy(), ref["max_logit"].astype(np.float32))
+    some = list(range(0, B, max(1, B // 6)))
+    np.testing.assert_array_equal(sc[some].cpu().numpy(),
+                                  oracle.masked_scatter_logits(oh, hid[some]).astype(np.float32))
+    for b in some:
+        rl, rt = oracle.select_and_score_row(oh, hid, b)
+        np.testing.assert_array_equal(pids[b].cpu().numpy(), rt)
+        np.testing.assert_array_equal(plog[b].cpu().numpy(), rl.astype(np.float32))
+
+
+def test_smoke_entry_point(build_lib):
+    """The smoke run the package entry point offers (one small invocation of every gather
+    against the oracle) passes: it asserts which gather each of its calls runs, so a change
+    of the library's plan shows here first."""
+    import __graft_entry__
+    __graft_entry__.smoke()
