@@ -91,7 +91,12 @@ constexpr int kSelectGatherMaxK = 1024;
 // Wall-clock limit of a bounded mbarrier wait in the pipelined gather (mtp_wait_test
 // can change it for a test).
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+// CTAs per SM of the fused kernel: more rows in flight with three, except for a single
+// row (its ticket's arrivals) and long rows (measured on GB300: H=1536 B=2, 4, 8 21.4,
+// 26.2, 36.7 against 21.8, 27.2, 38.1 us per call with two; B=1 19.6 against 19.3;
+// H=2560 B=8 53.6 against 52.9)
 constexpr int kSelectGatherCtasPerSm = 2;
+constexpr int kSelectGatherCtasPerSmShort = 3;   // batches of 2 or more rows, H <= 1536
 cudaError_t launch_fill(float *out, size_t n, float value, cudaStream_t s);
 // Copy `bytes` (a multiple of 16, both ends 16-byte aligned) from memory the device can
 // read (pinned host memory included) to device memory with one kernel.

@@ -238,7 +238,8 @@ cudaError_t run_select_gather(const GatherParams &p, cudaStream_t s)
     const void *fn = (const void *)k_select_gather<NCH, SCATTER>;
     cudaError_t e = allow_smem(fn, smem);
     if (e != cudaSuccess) return e;
-    const int per_sm = std::max(1, std::min(kSelectGatherCtasPerSm, blocks_per_sm(fn, kTopkThreads, smem)));
+    const int want = p.B >= 2 && p.H <= 1536 ? kSelectGatherCtasPerSmShort : kSelectGatherCtasPerSm;
+    const int per_sm = std::max(1, std::min(want, blocks_per_sm(fn, kTopkThreads, smem)));
     const int grid = std::max(p.B, per_sm * sm_count());
     return launch_dependent(k_select_gather<NCH, SCATTER>, dim3((unsigned)grid), dim3(kTopkThreads), smem, s, p);
 }
