@@ -1290,12 +1290,15 @@ def test_tensor_core_gather_one_k_block_large_buckets(build_lib, B):
     (32768, 512, 256, 32, 40, True, 0),       # paired chunks, round-robin, 32-row units
     (65536, 1024, 64, 16, 20, True, 0),       # paired chunks, tiny buckets, round-robin
     (131072, 1024, 320, 8, 256, False, 4),    # five k-blocks; four prototypes x 64 rows: 64-row
-])                                            # buckets span two 32-row units
+                                              # buckets span two 32-row units
+    (32768, 512, 128, 32, 256, True, 4),      # ticketed, paired short chunks beside buckets of
+])                                            # several 64-row blocks (items per block)
 def test_tensor_core_gather_shape_matrix(build_lib, V, C, H, K, B, packed, protos):
     """Integer inputs (every sum exact, so bit-for-bit against the oracle) over shapes that
     cross the tensor-core gather's switches: units of one to five k-blocks against the B
     warps' signal lag, ticketed and round-robin hand-out, paired short chunks, bucket-row
-    caps of 16 to 64 rows and buckets spanning several units.  Argmax, scatter and sparse
+    caps of 16 to 64 rows and buckets spanning several units (one work item per block of
+    a bucket's rows).  Argmax, scatter and sparse
     pair; the device error word must stay clear (a stalled pipeline ends in a timeout)."""
     m = build_lib
     g = np.random.default_rng(V + C + H + K + B)
