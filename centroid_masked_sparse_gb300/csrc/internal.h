@@ -134,12 +134,16 @@ struct TcGemmArgs {
     uint32_t *zero;         // words cleared at kernel start (may be null)
     int zero_words;
 };
-// The projection runs on tensor cores from batch 4 up once B * H exceeds this; below,
-// the CUDA-core GEMV (whose per-row work grows with B * H while both read the table
-// once) is ahead: measured at H=1536 B=4 28.3 vs 30.3 us per call, B=8 level; at
-// H=256 B=8 27.8 vs 30.3 us; at H=2560 B=8 54.9 vs 50.8 us.
-constexpr int kTcProjMinBatch = 4;
-constexpr long long kCudaCoreProjMaxWork = 8192;
+// The projection runs on tensor cores for batches above kCudaCoreProjBatch rows once
+// B * H exceeds kCudaCoreProjMaxWork; otherwise the CUDA-core GEMV (whose per-row work
+// grows with B * H while both read the table once, and which reduces up to eight rows
+// at once) is ahead.  Measured on GB300 per call against the earlier rule (tensor cores
+// from 4 rows once B * H > 8192): H=256 B=16 28.0 vs 30.9 us, B=32 31.9 vs 37.2, B=64
+// 38.8 vs 41.5; H=1536 B=6 30.2 vs 31.8, B=8 34.1 vs 35.9; H=2560 B=4 33.5 vs 38.2, B=6
+// 41.9 vs 45.1, B=8 49.3 vs 52.8.  Beyond the limit the GEMV lost: H=1536 B=12 45.3 vs
+// 44.4, B=20 59.6 vs 57.8; H=2560 B=12 73.2 vs 66.4.
+constexpr int kCudaCoreProjBatch = 8;
+constexpr long long kCudaCoreProjMaxWork = 16384;
 int tc_splits(int M, int N, int K);
 cudaError_t launch_tc_gemm(const TcGemmArgs &a, cudaStream_t s);
 

@@ -245,7 +245,7 @@ mtp_status run_select(const mtp_head_desc *d, const void *hidden, int B, float *
                       int32_t *topk, char *ws, const Layout *L, int chunk, cudaStream_t s,
                       bool after_fill = false, bool after_stage = false)
 {
-    if (B >= kTcProjMinBatch && (long long)B * d->hidden_size > kCudaCoreProjMaxWork) {
+    if (B > kCudaCoreProjBatch && (long long)B * d->hidden_size > kCudaCoreProjMaxWork) {
         // tensor cores: M = C centroid rows, N = batch, K = H, split-K in a cluster
         TcGemmArgs g{};
         g.table = d->centroid_w;

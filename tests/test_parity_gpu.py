@@ -191,18 +191,24 @@ def test_k_equals_c_is_dense(build_lib):
 
 
 def test_projection_paths_agree(build_lib):
-    """Batches below 4 rows use the CUDA-core projection, larger ones the tensor-core
-    GEMM with a cluster split-K: the same rows must score alike either way."""
+    """Batches of at most 8 rows use the CUDA-core projection (which reduces 1, 2, 4 or
+    8 rows at once, the last group padded), larger ones at H=1536 the tensor-core GEMM
+    with a cluster split-K: the same rows must score alike either way, and the CUDA-core
+    scores of a row must not depend on the batch it came in (the same bits)."""
     m = build_lib
     oh, dh = device_head(m, "uniform")
     hidden = synth.hidden_batch("uniform", 24, row0=900)
     h = helpers.bf16_tensor(hidden)
     big, big_top = m.mtp_centroid_scores(dh, h)
     small = torch.cat([m.mtp_centroid_scores(dh, h[i:i + 1])[0] for i in range(24)])
+    cuts = [0, 8, 13, 16, 18, 24]   # batches of 8, 5, 3, 2 and 6 rows
+    grouped = torch.cat([m.mtp_centroid_scores(dh, h[a:b])[0] for a, b in zip(cuts, cuts[1:])])
     torch.cuda.synchronize()
     ref = oracle.centroid_scores(oh, hidden)
     helpers.assert_close(big.cpu().numpy(), ref, "tensor-core projection")
     helpers.assert_close(small.cpu().numpy(), ref, "CUDA-core projection")
+    helpers.assert_close(grouped.cpu().numpy(), ref, "CUDA-core projection, row groups")
+    assert torch.equal(grouped, small)
     d = np.abs(big.cpu().numpy().astype(np.float64) - small.cpu().numpy())
     assert d.max() < 1e-3
 
