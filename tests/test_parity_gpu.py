@@ -222,6 +222,18 @@ def test_ragged_batches(build_lib, B):
     check_topk(build_lib, "uniform", B, row0=1000)
 
 
+@pytest.mark.parametrize("name,B", [("uniform", 10), ("uniform", 11), ("draft256", 64), ("draft256", 65)])
+def test_projection_plan_boundary(build_lib, name, B):
+    """Either side of the projection plan's switch (the CUDA-core GEMV up to B*H = 16384,
+    tensor cores beyond it): H=1536 at 10 rows (GEMV, a padded second group of 8) and 11
+    (tensor cores), H=256 at 64 rows (GEMV, eight groups of 8) and 65 (tensor cores);
+    selections and tokens against the oracle."""
+    m = build_lib
+    hidden, ref = check_topk(m, name, B, row0=3000)
+    oh, dh = device_head(m, name)
+    check_selection(m, dh, oh, hidden, ref["sel"])
+
+
 def test_maximum_batch(build_lib):
     check_topk(build_lib, "tiny", 1024)
 
