@@ -332,9 +332,11 @@ constexpr int kSmallHidden = 256;
 // With the packed embedding table it also takes calls with fewer (row, cluster) pairs: its
 // block copies stream HBM faster than the CUDA-core gather's row copies and read
 // no padding rows.  Running two or three CTAs per SM, it is ahead (measured on
-// GB300) from B*K >= C/4 at H = 1536 and 2560 (behind at C/8) and from B*K >= C/16
-// at H = 256, where the CUDA-core gather's per-row costs weigh most (behind at
-// C/64).  Smaller calls keep more
+// GB300) from B*K >= C/5 with uniform clusters (K=32, C=2048, H=1536: B=13, 14 48.4,
+// 50.1 against 49.2, 52.7 us with the pipelined CUDA-core gather), from B*K >= C/4 with
+// ragged ones (H=2560: B=13, 14 75.2, 75.9 against 72.6, 75.3 us, B=15 77.1 against
+// 78.0; behind at C/8) and from B*K >= C/16 at H = 256, where the CUDA-core gather's
+// per-row costs weigh most (behind at C/64).  Smaller calls keep more
 // SMs busy with the CUDA-core gather's finer work items.  Its chunk is the largest
 // of 128, 64, 32 positions that still gives about two work items per SM.
 bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
@@ -343,7 +345,8 @@ bool tc_gather_plan(const mtp_head_desc *d, int B, int *chunk)
     const long long C = d->num_centroids;
     const bool large = pairs >= (long long)kTcGatherMinReuse * C;
     const bool packed_reuse =
-        d->embed_packed && (4 * pairs >= C || (d->hidden_size <= kSmallHidden && 16 * pairs >= C));
+        d->embed_packed && ((d->cluster_offsets ? 4 : 5) * pairs >= C ||
+                            (d->hidden_size <= kSmallHidden && 16 * pairs >= C));
     if (d->embed_packed && (large || packed_reuse)) {
         const double avg = (double)d->vocab_size / d->num_centroids;
         const double clusters = (double)std::min<long long>(pairs, d->num_centroids);

@@ -383,8 +383,10 @@ MTP_API mtp_status mtp_graph_destroy(mtp_graph *graph);
  * itself right behind the projection (batches of at most 8 rows with K <= 1024 and
  * H > 256), else 2 for the direct CUDA-core gather (those batches at H <= 256, and
  * at most 12 rows where the tensor-core gather would not run), else 1 for the
- * tensor-core gather (large buckets, batch * K >= 4C; or batch * K >= C/4 with a
- * packed table or H <= 256, or >= C/16 with a packed table and H <= 256), else 0 for the pipelined CUDA-core gather; a negative mtp_status for
+ * tensor-core gather (large buckets, batch * K >= 4C; or with a packed table batch *
+ * K >= C/5 for uniform clusters and >= C/4 with cluster_offsets; or batch * K >= C/4
+ * at H <= 256; or >= C/16 with a packed table and H <= 256), else 0 for the pipelined
+ * CUDA-core gather; a negative mtp_status for
  * an invalid descriptor or batch, or MTP_ERR_UNSUPPORTED when mtp_force_gather
  * forces a kernel that cannot run this call.  The sparse pair runs only kernels 0
  * and 1.  Host-only; for profiling and benchmarks (the calls choose by

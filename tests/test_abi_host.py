@@ -190,14 +190,15 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), -1) == -2
     assert L.mtp_gather_plan(ctypes.byref(d), 2000) == -6
     assert L.mtp_gather_plan(ctypes.byref(_desc(K=0)), 8) == -2
-    d.embed_packed = 0xA000                                  # packed table: from B*K >= C/4
+    d.embed_packed = 0xA000                                  # packed table: from B*K >= C/5
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 15) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 13) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 12) == 2       # below: up to 12 rows direct
     d = _desc(K=16)                                          # the same rule at any batch size
     d.embed_packed = 0xA000
-    assert L.mtp_gather_plan(ctypes.byref(d), 31) == 0
-    assert L.mtp_gather_plan(ctypes.byref(d), 32) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 25) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 26) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 65) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 128) == 1
     d = _desc(H=256)                                         # small hidden size, token order:
@@ -210,11 +211,12 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2       # up to 8 rows of 512 bytes: direct
     assert L.mtp_gather_plan(ctypes.byref(d), 3) == 2
     assert L.mtp_gather_plan(ctypes.byref(_desc(H=512)), 8) == 3   # above H=256: fused
-    d = _desc(offsets=0x5000)                                # ragged clusters: the same rules
+    d = _desc(offsets=0x5000)                                # ragged clusters: the same rules but C/4
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 15) == 0       # packed, ragged: from B*K >= C/4
     assert L.mtp_gather_plan(ctypes.byref(d), 8) == 3
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1
 
