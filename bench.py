@@ -62,11 +62,13 @@ def file_sha(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(kernel_file, workload, batch):
-    """DRAM bytes per launch from a committed ncu summary, if it still matches the kernel source."""
+def profiled_traffic(kernel_file, workload, batch, layout="packed"):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches the kernel source
+    (summaries of the token-order table carry `_token` after the workload's name)."""
     if kernel_file is None:
         return None
-    prof = os.path.join(ROOT, "profiles", f"{kernel_file}_{workload}_b{batch}.md")
+    suffix = "_token" if layout == "token" else ""
+    prof = os.path.join(ROOT, "profiles", f"{kernel_file}_{workload}{suffix}_b{batch}.md")
     src = os.path.join(ROOT, "centroid_masked_sparse_gb300", "csrc", f"{kernel_file}.cu")
     try:
         text = open(prof).read()
@@ -505,7 +507,7 @@ def gpu_main(args):
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": hbm, "peak_source": f"{hbm_src} HBM copy GB/s", "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
-                "traffic": profiled_traffic(kfile, name, B),
+                "traffic": profiled_traffic(kfile, name, B, args.layout),
                 "algorithmic_bytes": int(res["bytes"]["gather"]),
                 "kernel_us": round(res["kernel_ms"] * 1e3, 2)}
     call_gbs = res["bytes"]["call"] / (res["call_ms"] * 1e-3) / 1e9

@@ -81,7 +81,7 @@ constexpr int kMaxN = 64;          // bucket rows per unit (at most): with four 
                                    // then takes at most half the TMEM, so two CTAs fit on an SM
                                    // (three with the 32-row units of calls with small buckets)
 constexpr int kMeta = 8;           // unit-metadata ring
-constexpr int kAcc = 4;            // TMEM accumulators: the epilogues of the last units overlap the MMAs
+constexpr int kAcc = 4;            // TMEM accumulators (at most): the epilogues of the last units overlap the MMAs
 constexpr int kMaxStages = 32;
 constexpr uint32_t kSmTmemCols = 512;  // TMEM columns of one SM
 constexpr uint32_t kRowBytes = kTileK * 2;
@@ -136,6 +136,7 @@ struct Params {
     int handout;    // items past the first round by ticket (large buckets), else round-robin
     int num_kb;
     int stages;
+    int n_acc;      // TMEM accumulators in use (2 or kAcc)
     uint32_t a_bytes, b_bytes;   // stage sizes
     uint32_t tmem_cols;
 };
@@ -755,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (p.packed) prefetch_l2_table(p.poff, (size_t)(p.C + 1) * sizeof(int32_t));
     // the work items and buckets come from the top-K kernel before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t acc_cols = p.tmem_cols / kAcc;
+    const uint32_t acc_cols = p.tmem_cols / (uint32_t)p.n_acc;
 
     if (warp == 4) {
         if (!publish_units<PAIR>(p, meta, mfull0, mempty0, lane) && lane == 0) timeout(p);
@@ -811,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                     break;
                 }
                 mma_commit(tfull0 + 8u * acc);
-                if (++acc == kAcc) {
+                if (++acc == p.n_acc) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -911,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 mbar_arrive(tempty0 + 8u * acc);
                 mbar_arrive(mempty0 + 8u * um);
             }
-            if (++acc == kAcc) {
+            if (++acc == p.n_acc) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -1075,7 +1076,16 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     p.a_bytes = (uint32_t)a_rows * kRowBytes;
     p.b_bytes = (uint32_t)p.nmax * kRowBytes;
     uint32_t cols = 32;
-    while (cols < (uint32_t)kAcc * (uint32_t)p.nmax) cols <<= 1;
+    // Argmax calls with units of 64 bucket rows gathered from the token-order table run
+    // three CTAs per SM with two accumulators (and two stages) each: its four-row gathers
+    // keep each CTA's pipeline short of the HBM rate, so more CTAs count for more than a
+    // deeper pipeline (measured on GB300 per call: shared-centroid workload B=256 166.7
+    // against 184.0 us, uniform clusters B=256 216.1 against 279.2 us).  Not on the packed
+    // table, whose block copies fill two CTAs' pipelines (137 against 126 us), nor for the
+    // scatter, whose stores need the four accumulators' overlap (249.9 against 241.0 us).
+    p.n_acc = (!g.packed && p.nmax == kMaxN && !scatter) ? 2 : kAcc;
+    const int min_stages = p.n_acc == 2 ? 2 : 3;
+    while (cols < (uint32_t)p.n_acc * (uint32_t)p.nmax) cols <<= 1;
     p.tmem_cols = cols;
     auto kernel = [&]() {
         if (scatter) return pair ? k_gather_tc<true, true> : k_gather_tc<true, false>;
@@ -1117,7 +1127,7 @@ cudaError_t launch_gather_tc(const GatherParams &g, bool scatter, cudaStream_t s
     for (int n = max_per_sm; n >= 2; --n) {
         if ((uint32_t)n * p.tmem_cols > kSmTmemCols) continue;
         const int st = fit_stages((size_t)(220 / n) * 1024);
-        if (st >= 3 && ctas_fit(kfn, smem_bytes(p, st), n)) {
+        if (st >= min_stages && ctas_fit(kfn, smem_bytes(p, st), n)) {
             per_sm = n;
             stages = st;
             break;
