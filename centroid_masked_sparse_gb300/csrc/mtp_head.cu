@@ -372,8 +372,17 @@ std::atomic<int> g_stall_test{0};
 
 // Batches that run the fused top-K + gather kernel (select_gather.cu) behind the
 // projection instead of the top-K kernel and a gather, for hidden sizes above
-// kSmallHidden; at or below it the same batches take the direct gather.
+// kSmallHidden; at or below it the same batches take the direct gather.  With uniform
+// clusters and H <= 1536 the fused kernel also takes 9 and 10 rows (measured on GB300
+// against the direct gather: B=9 38.2 vs 40.1 us, B=10 40.2 vs 41.6; B=11 43.4 vs 42.5;
+// ragged clusters at H=2560, B=9 and 10: 58.3 vs 54.4 and 61.5 vs 57.7).
 constexpr int kFusedMaxBatch = 8;
+constexpr int kFusedMaxBatchUniform = 10;
+
+int fused_max_batch(const mtp_head_desc *d)
+{
+    return !d->cluster_offsets && d->hidden_size <= 1536 ? kFusedMaxBatchUniform : kFusedMaxBatch;
+}
 
 // Whether a gather kernel can run a masked call of this shape.
 bool gather_can_run(const mtp_head_desc *d, int B, bool sparse, GatherKind k)
@@ -387,7 +396,7 @@ bool gather_can_run(const mtp_head_desc *d, int B, bool sparse, GatherKind k)
     }
 }
 
-// The gather a masked call runs.  Batches of at most kFusedMaxBatch rows take the
+// The gather a masked call runs.  Batches of at most fused_max_batch rows take the
 // fused kernel, which selects each row's top-K in the gather CTAs themselves.  The
 // direct CUDA-core gather (each warp loads candidate rows straight into registers; no
 // producer, ring or hand-off, so its latency chain is short) takes up to 12 rows
@@ -409,7 +418,7 @@ GatherKind gather_kind(const mtp_head_desc *d, int B, bool sparse, int *chunk)
     if (forced >= 0) {
         k = (GatherKind)forced;
         if (!gather_can_run(d, B, sparse, k)) return kGatherNone;
-    } else if (!sparse && B <= kFusedMaxBatch && d->hidden_size > kSmallHidden &&
+    } else if (!sparse && B <= fused_max_batch(d) && d->hidden_size > kSmallHidden &&
                gather_can_run(d, B, sparse, kGatherFused)) {
         k = kGatherFused;
     } else if (!sparse && B <= kFusedMaxBatch && gather_can_run(d, B, sparse, kGatherDirect)) {

@@ -380,7 +380,8 @@ MTP_API mtp_status mtp_graph_destroy(mtp_graph *graph);
 
 /* Which gather kernel a masked argmax or scatter call with this descriptor and
  * batch runs: 3 for the fused small-batch kernel, which selects each row's top-K
- * itself right behind the projection (batches of at most 8 rows with K <= 1024 and
+ * itself right behind the projection (batches of at most 8 rows, 10 with uniform
+ * clusters and H <= 1536, with K <= 1024 and
  * H > 256), else 2 for the direct CUDA-core gather (those batches at H <= 256, and
  * at most 12 rows where the tensor-core gather would not run), else 1 for the
  * tensor-core gather (large buckets, batch * K >= 4C; or with a packed table batch *

@@ -181,8 +181,9 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0      # B*K = C: CUDA-core gather
     assert L.mtp_gather_plan(ctypes.byref(d), 13) == 0
     assert L.mtp_gather_plan(ctypes.byref(d), 12) == 2      # a dozen rows: the direct one
-    assert L.mtp_gather_plan(ctypes.byref(d), 9) == 2
-    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 3       # up to 8 rows: the fused kernel
+    assert L.mtp_gather_plan(ctypes.byref(d), 11) == 2
+    assert L.mtp_gather_plan(ctypes.byref(d), 10) == 3      # up to 10 rows (uniform clusters,
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 3       # H <= 1536): the fused kernel
     assert L.mtp_gather_plan(ctypes.byref(d), 1) == 3
     assert L.mtp_gather_plan(ctypes.byref(_desc(K=1025, C=2048)), 1) == 2   # fused: K <= 1024
     assert L.mtp_gather_plan(ctypes.byref(d), 256) == 1     # B*K = 4C: large buckets
@@ -213,6 +214,8 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(_desc(H=512)), 8) == 3   # above H=256: fused
     d = _desc(offsets=0x5000)                                # ragged clusters: the same rules but C/4
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 0
+    assert L.mtp_gather_plan(ctypes.byref(d), 9) == 2        # and the fused kernel to 8 rows
+    assert L.mtp_gather_plan(ctypes.byref(_desc(H=2048)), 9) == 2   # (also above H=1536)
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1

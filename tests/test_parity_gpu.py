@@ -225,9 +225,10 @@ def test_ragged_batches(build_lib, B):
 @pytest.mark.parametrize("name,B", [("uniform", 10), ("uniform", 11), ("draft256", 64), ("draft256", 65)])
 def test_projection_plan_boundary(build_lib, name, B):
     """Either side of the projection plan's switch (the CUDA-core GEMV up to B*H = 16384,
-    tensor cores beyond it): H=1536 at 10 rows (GEMV, a padded second group of 8) and 11
-    (tensor cores), H=256 at 64 rows (GEMV, eight groups of 8) and 65 (tensor cores);
-    selections and tokens against the oracle."""
+    tensor cores beyond it): H=1536 at 10 rows (GEMV, a padded second group of 8; the fused
+    kernel's last batch size) and 11 (tensor cores, the direct gather), H=256 at 64 rows
+    (GEMV, eight groups of 8) and 65 (tensor cores); selections and tokens against the
+    oracle."""
     m = build_lib
     hidden, ref = check_topk(m, name, B, row0=3000)
     oh, dh = device_head(m, name)
@@ -475,7 +476,7 @@ def test_overlapping_offsets_overflow_the_item_list(build_lib):
 # every gather kernel at the drafter's small batches; the fused small-batch kernel
 
 
-@pytest.mark.parametrize("B", [1, 3, 8])
+@pytest.mark.parametrize("B", [1, 3, 8, 10])
 @pytest.mark.parametrize("kind", ["fused", "cuda_core_direct", "cuda_core", "tensor_core"])
 def test_every_gather_kernel_small_batches(build_lib, B, kind):
     """The uniform workload at small batches through each gather kernel (forced): token
