@@ -378,6 +378,10 @@ std::atomic<int> g_stall_test{0};
 // ragged clusters at H=2560, B=9 and 10: 58.3 vs 54.4 and 61.5 vs 57.7).
 constexpr int kFusedMaxBatch = 8;
 constexpr int kFusedMaxBatchUniform = 10;
+// The direct gather's batches at H <= kSmallHidden: up to 10 rows (measured on GB300 with
+// the packed table against the tensor-core gather: B=9 24.1 vs 26.5 us, B=10 25.5 vs 25.8;
+// B=12 level, B=14 27.7 vs 27.2).
+constexpr int kDirectMaxBatchSmallHidden = 10;
 
 int fused_max_batch(const mtp_head_desc *d)
 {
@@ -421,7 +425,8 @@ GatherKind gather_kind(const mtp_head_desc *d, int B, bool sparse, int *chunk)
     } else if (!sparse && B <= fused_max_batch(d) && d->hidden_size > kSmallHidden &&
                gather_can_run(d, B, sparse, kGatherFused)) {
         k = kGatherFused;
-    } else if (!sparse && B <= kFusedMaxBatch && gather_can_run(d, B, sparse, kGatherDirect)) {
+    } else if (!sparse && B <= (d->hidden_size <= kSmallHidden ? kDirectMaxBatchSmallHidden : kFusedMaxBatch) &&
+               gather_can_run(d, B, sparse, kGatherDirect)) {
         k = kGatherDirect;
     } else if (!sparse && !tc && B <= 12) {
         k = kGatherDirect;

@@ -208,8 +208,9 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), 15) == 0
     d = _desc(H=256)                                         # and packed: from B*K >= C/16
     d.embed_packed = 0xA000
-    assert L.mtp_gather_plan(ctypes.byref(d), 9) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2       # up to 8 rows of 512 bytes: direct
+    assert L.mtp_gather_plan(ctypes.byref(d), 11) == 1
+    assert L.mtp_gather_plan(ctypes.byref(d), 10) == 2      # up to 10 rows of 512 bytes: direct
+    assert L.mtp_gather_plan(ctypes.byref(d), 8) == 2
     assert L.mtp_gather_plan(ctypes.byref(d), 3) == 2
     assert L.mtp_gather_plan(ctypes.byref(_desc(H=512)), 8) == 3   # above H=256: fused
     d = _desc(offsets=0x5000)                                # ragged clusters: the same rules but C/4
