@@ -378,10 +378,13 @@ std::atomic<int> g_stall_test{0};
 // ragged clusters at H=2560, B=9 and 10: 58.3 vs 54.4 and 61.5 vs 57.7).
 constexpr int kFusedMaxBatch = 8;
 constexpr int kFusedMaxBatchUniform = 10;
-// The direct gather's batches at H <= kSmallHidden: up to 10 rows (measured on GB300 with
-// the packed table against the tensor-core gather: B=9 24.1 vs 26.5 us, B=10 25.5 vs 25.8;
-// B=12 level, B=14 27.7 vs 27.2).
+// The direct gather's batches at H <= kSmallHidden: up to 10 rows with the packed table
+// (measured on GB300 against the tensor-core gather: B=9 24.1 vs 26.5 us, B=10 25.5 vs
+// 25.8; B=12 level, B=14 27.7 vs 27.2), up to 20 on the token-order table (against the
+// pipelined gather B=13, 15 27.4, 28.2 vs 40.3, 41.6 us; against the tensor-core one B=16,
+// 20 29.4, 33.2 vs 32.4, 34.4; B=24 35.3 vs 34.9, B=32 40.7 vs 36.5).
 constexpr int kDirectMaxBatchSmallHidden = 10;
+constexpr int kDirectMaxBatchSmallHiddenTokenOrder = 20;
 
 int fused_max_batch(const mtp_head_desc *d)
 {
@@ -425,7 +428,10 @@ GatherKind gather_kind(const mtp_head_desc *d, int B, bool sparse, int *chunk)
     } else if (!sparse && B <= fused_max_batch(d) && d->hidden_size > kSmallHidden &&
                gather_can_run(d, B, sparse, kGatherFused)) {
         k = kGatherFused;
-    } else if (!sparse && B <= (d->hidden_size <= kSmallHidden ? kDirectMaxBatchSmallHidden : kFusedMaxBatch) &&
+    } else if (!sparse &&
+               B <= (d->hidden_size > kSmallHidden ? kFusedMaxBatch
+                     : d->embed_packed             ? kDirectMaxBatchSmallHidden
+                                                   : kDirectMaxBatchSmallHiddenTokenOrder) &&
                gather_can_run(d, B, sparse, kGatherDirect)) {
         k = kGatherDirect;
     } else if (!sparse && !tc && B <= 12) {

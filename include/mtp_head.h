@@ -382,7 +382,8 @@ MTP_API mtp_status mtp_graph_destroy(mtp_graph *graph);
  * batch runs: 3 for the fused small-batch kernel, which selects each row's top-K
  * itself right behind the projection (batches of at most 8 rows, 10 with uniform
  * clusters and H <= 1536, with K <= 1024 and
- * H > 256), else 2 for the direct CUDA-core gather (up to 10 rows at H <= 256, and
+ * H > 256), else 2 for the direct CUDA-core gather (at H <= 256 up to 10 rows with a
+ * packed table and 20 without, and
  * at most 12 rows where the tensor-core gather would not run), else 1 for the
  * tensor-core gather (large buckets, batch * K >= 4C; or with a packed table batch *
  * K >= C/5 for uniform clusters and >= C/4 with cluster_offsets; or batch * K >= C/4

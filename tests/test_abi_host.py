@@ -203,9 +203,10 @@ def test_gather_plan(L):
     assert L.mtp_gather_plan(ctypes.byref(d), 65) == 1
     assert L.mtp_gather_plan(ctypes.byref(d), 128) == 1
     d = _desc(H=256)                                         # small hidden size, token order:
-    assert L.mtp_gather_plan(ctypes.byref(d), 16) == 1       # tensor cores from B*K >= C/4
+    assert L.mtp_gather_plan(ctypes.byref(d), 20) == 2       # the direct gather up to 20 rows,
+    assert L.mtp_gather_plan(ctypes.byref(d), 13) == 2
+    assert L.mtp_gather_plan(ctypes.byref(d), 21) == 1       # then tensor cores (B*K >= C/4)
     assert L.mtp_gather_plan(ctypes.byref(d), 64) == 1
-    assert L.mtp_gather_plan(ctypes.byref(d), 15) == 0
     d = _desc(H=256)                                         # and packed: from B*K >= C/16
     d.embed_packed = 0xA000
     assert L.mtp_gather_plan(ctypes.byref(d), 11) == 1

@@ -222,14 +222,15 @@ def test_ragged_batches(build_lib, B):
     check_topk(build_lib, "uniform", B, row0=1000)
 
 
-@pytest.mark.parametrize("name,B", [("uniform", 10), ("uniform", 11), ("draft256", 10), ("draft256", 64),
-                                    ("draft256", 65)])
+@pytest.mark.parametrize("name,B", [("uniform", 10), ("uniform", 11), ("draft256", 10), ("draft256", 20),
+                                    ("draft256", 64), ("draft256", 65)])
 def test_projection_plan_boundary(build_lib, name, B):
     """Either side of the projection plan's switch (the CUDA-core GEMV up to B*H = 16384,
     tensor cores beyond it): H=1536 at 10 rows (GEMV, a padded second group of 8; the fused
-    kernel's last batch size) and 11 (tensor cores, the direct gather), H=256 at 10 rows (the
-    direct gather's last batch size there), 64 (GEMV, eight groups of 8) and 65 (tensor
-    cores); selections and tokens against the oracle."""
+    kernel's last batch size) and 11 (tensor cores, the direct gather), H=256 on the
+    token-order table at 10 and 20 rows (the direct gather, 20 its last batch size there),
+    64 (GEMV, eight groups of 8) and 65 (tensor cores); selections and tokens against the
+    oracle."""
     m = build_lib
     hidden, ref = check_topk(m, name, B, row0=3000)
     oh, dh = device_head(m, name)
