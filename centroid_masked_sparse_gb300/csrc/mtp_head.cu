@@ -403,19 +403,18 @@ bool gather_can_run(const mtp_head_desc *d, int B, bool sparse, GatherKind k)
     }
 }
 
-// The gather a masked call runs.  Batches of at most fused_max_batch rows take the
-// fused kernel, which selects each row's top-K in the gather CTAs themselves.  The
+// The gather a masked call runs.  Batches of at most fused_max_batch rows at H > 256 take
+// the fused kernel, which selects each row's top-K in the gather CTAs themselves.  The
 // direct CUDA-core gather (each warp loads candidate rows straight into registers; no
-// producer, ring or hand-off, so its latency chain is short) takes up to 12 rows
-// where the tensor-core gather would not run, and the fused kernel's batches at
-// H <= 256, whose 512-byte rows make the fused kernel's row stream (every row's
-// candidates, no dedup) the slower one.  Measured on GB300 against the alternatives:
-// uniform clusters B=12 ~46 vs ~47.5 us (pipelined), B=16 ~56.5 vs ~54.5 us (tensor
-// cores); H=256 B=16 38.5 vs 32.4 us (tensor cores); H=256 with the packed table,
-// direct against fused (and tensor cores): B=1 18.1 vs 19.2, B=2 18.3 vs 19.9, B=4
-// 21.1 vs 20.4, B=6 22.8 vs 26.6 (24.4), B=8 24.7 vs 26.9 (26.9) us.  The sparse
-// pair keeps the pipelined and tensor-core gathers.  A kind forced by
-// mtp_force_gather that cannot run the call gives kGatherNone.
+// producer, ring or hand-off, so its latency chain is short) takes the small batches at
+// H <= 256 (up to the limits above), whose 512-byte rows make the fused kernel's row
+// stream (every row's candidates, no dedup) the slower one, and up to 12 rows elsewhere
+// where the tensor-core gather would not run.  Measured on GB300 against the
+// alternatives: uniform clusters B=12 ~46 vs ~47.5 us (pipelined), B=16 ~56.5 vs ~54.5 us
+// (tensor cores); H=256 with the packed table, direct against fused (and tensor cores):
+// B=1 18.1 vs 19.2, B=2 18.3 vs 19.9, B=4 21.1 vs 20.4, B=6 22.8 vs 26.6 (24.4), B=8 24.7
+// vs 26.9 (26.9) us.  The sparse pair keeps the pipelined and tensor-core gathers.  A
+// kind forced by mtp_force_gather that cannot run the call gives kGatherNone.
 GatherKind gather_kind(const mtp_head_desc *d, int B, bool sparse, int *chunk)
 {
     int tc_chunk = 0;
