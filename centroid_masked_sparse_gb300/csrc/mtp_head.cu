@@ -773,7 +773,7 @@ const char *mtp_status_string(mtp_status status)
     case MTP_ERR_ALIGN: return "a pointer or row stride is not 16-byte aligned";
     case MTP_ERR_WORKSPACE: return "workspace missing or smaller than mtp_workspace_bytes";
     case MTP_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
-    case MTP_ERR_UNSUPPORTED: return "sizes outside this build's limits";
+    case MTP_ERR_UNSUPPORTED: return "sizes outside the library's limits";
     }
     return "unknown status";
 }

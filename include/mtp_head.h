@@ -69,10 +69,10 @@ typedef enum mtp_status {
     MTP_ERR_ALIGN = -3,       /* a pointer or row stride is not 16-byte aligned     */
     MTP_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than mtp_workspace_bytes */
     MTP_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed               */
-    MTP_ERR_UNSUPPORTED = -6  /* valid but outside this build's limits (see below)  */
+    MTP_ERR_UNSUPPORTED = -6  /* valid but outside the library's limits (see below) */
 } mtp_status;
 
-/* Limits of this build (MTP_ERR_UNSUPPORTED beyond them):
+/* Limits of the library (MTP_ERR_UNSUPPORTED beyond them):
  *   H % 8 == 0 and 8 <= H <= 4096; 1 <= K <= C <= 16384; 1 <= batch <= 1024;
  *   1 <= V < 2^31; uniform clusters need V % C == 0. */
 #define MTP_MAX_HIDDEN 4096
