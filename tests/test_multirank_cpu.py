@@ -140,3 +140,25 @@ def test_sharded_argmax_exchange_is_a_max_all_reduce():
     res = dict(q.get(timeout=5) for _ in range(2))
     want = [_key(2.5, 99), _key(2.0, 7), _key(0.25, 3), _key(-2.0, 6)]
     assert res[0] == want and res[1] == want
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """The bench's `roofline.traffic` comes from a committed ncu summary only while the
+    summary's source hash matches the kernel file, and summaries of the token-order table
+    are looked up under `_token` (a packed-table summary never stands in for them)."""
+    import bench
+    csrc = tmp_path / "centroid_masked_sparse_gb300" / "csrc"
+    prof = tmp_path / "profiles"
+    csrc.mkdir(parents=True)
+    prof.mkdir()
+    (csrc / "gather_tc.cu").write_text("// kernel source\n")
+    sha = bench.file_sha(str(csrc / "gather_tc.cu"))
+    (prof / "gather_tc_shared_b256.md").write_text(f"dram_bytes_per_launch: 1000\nsource_sha256_16: {sha}\n")
+    (prof / "gather_tc_shared_token_b256.md").write_text(f"dram_bytes_per_launch: 2000\nsource_sha256_16: {sha}\n")
+    (prof / "gather_tc_uniform_b64.md").write_text("dram_bytes_per_launch: 3000\nsource_sha256_16: 0000000000000000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("gather_tc", "shared", 256) == 1000.0
+    assert bench.profiled_traffic("gather_tc", "shared", 256, "token") == 2000.0
+    assert bench.profiled_traffic("gather_tc", "uniform", 64) is None          # stale hash
+    assert bench.profiled_traffic("gather_tc", "uniform", 64, "token") is None # no summary
+    assert bench.profiled_traffic(None, "shared", 256) is None
